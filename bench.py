@@ -1,0 +1,431 @@
+#!/usr/bin/env python
+"""Benchmark of the gated delta rule library on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One JSON line on rank 0.  A step is one gdn_prefill call over the
+B=1, T=4096, Hk=16, Hv=32, Dk=Dv=128, bf16, chunk-64 workload with its
+inputs resident in HBM; `value` is tokens/s (B*T per step).  The line also
+carries the decode workload (B=64, Hk=16, Hv=32, 256 successive steps in one
+CUDA graph, state updated in place) as `decode`, the roofline of each, the
+end-to-end number through the C ABI from pinned host buffers (`e2e`) and the
+fp64 oracle timed on the host cores (`cpu_baseline`).
+
+Timing: W untimed warm-up steps; then exactly K steps, each bracketed by
+CUDA events on the launching stream, with a 256 MiB write between steps to
+flush the L2 (outside the events); barrier + synchronize on both sides; the
+max over ranks.  N > 1 runs one independent replica per GPU (the heads of the
+rule are independent; there is no exchange), so scaling is weak.
+
+`--impl reference` times the fp64 oracle (the only reference this method has)
+on the host cores on a bounded sample of the same workload, in the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import gdn_inputs  # noqa: E402
+
+FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ----------------------------------------------------------------------------
+# helpers
+# ----------------------------------------------------------------------------
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def prefill_alg_bytes(w):
+    """q, k, v, g, beta, y once each, plus the state in and out (fp32)."""
+    eb = 4 if w.dtype == "f32" else 2
+    tok = w.B * w.T
+    return (tok * w.Hk * w.Dk * 2 * eb + tok * w.Hv * w.Dv * 2 * eb
+            + tok * w.Hv * 2 * eb + 2 * w.B * w.Hv * w.Dv * w.Dk * 4)
+
+
+def prefill_alg_flops(w):
+    """6 D^2 + 8 C D per token per value head (chunk form, full C x C grams)."""
+    D = w.Dk
+    return w.B * w.T * w.Hv * (6 * D * D + 8 * w.chunk * D)
+
+
+def decode_alg_bytes(w):
+    eb = 4 if w.dtype == "f32" else 2
+    return (2 * w.B * w.Hv * w.Dv * w.Dk * 4 + w.B * w.Hk * w.Dk * 2 * eb
+            + w.B * w.Hv * w.Dv * 2 * eb + w.B * w.Hv * 2 * eb)
+
+
+def roofline(alg_bytes, seconds, hbm_gbs, kind):
+    achieved = alg_bytes / seconds / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_gbs,
+            "unit": "GB/s", "frac": round(achieved / hbm_gbs, 4), "traffic": None,
+            "peak_kind": kind}
+
+
+def median_ms(pairs):
+    return [a.elapsed_time(b) for a, b in pairs]
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+def bench_prefill(gdn, w, dev, steps, warmup, world):
+    ins = {n: t.to(dev) for n, t in gdn_inputs.workload_inputs(w).items()}
+    y = torch.empty((w.B, w.T, w.Hv, w.Dv), dtype=w.torch_dtype, device=dev)
+    s_out = torch.empty((w.B, w.Hv, w.Dv, w.Dk), dtype=torch.float32, device=dev)
+    nbytes = gdn.gdn_prefill_workspace_bytes(w.B, w.T, w.Hk, w.Hv, w.Dk, w.Dv,
+                                             w.chunk, w.torch_dtype)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        gdn.gdn_prefill(ins["q"], ins["k"], ins["v"], ins["g"], ins["beta"], ins["s0"],
+                        s_out, y, w.chunk, workspace=ws, stream=stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    pairs = []
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        pairs.append((a, b))
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    wall = time.perf_counter() - t0
+    times = median_ms(pairs)
+    return sum(times) / len(times), wall
+
+
+def bench_prefill_e2e(gdn, w, dev, steps, warmup):
+    """Through the C ABI from pinned host buffers: H2D of the step's inputs,
+    gdn_prefill, D2H of y and the final state, every step."""
+    host = {n: t.pin_memory() for n, t in gdn_inputs.workload_inputs(w).items()}
+    dv = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+    y = torch.empty((w.B, w.T, w.Hv, w.Dv), dtype=w.torch_dtype, device=dev)
+    s_out = torch.empty((w.B, w.Hv, w.Dv, w.Dk), dtype=torch.float32, device=dev)
+    y_h = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    s_h = torch.empty(s_out.shape, dtype=s_out.dtype).pin_memory()
+    nbytes = gdn.gdn_prefill_workspace_bytes(w.B, w.T, w.Hk, w.Hv, w.Dk, w.Dv,
+                                             w.chunk, w.torch_dtype)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = y.numel() * y.element_size() + s_out.numel() * 4
+
+    def step():
+        for n in host:
+            dv[n].copy_(host[n], non_blocking=True)
+        gdn.gdn_prefill(dv["q"], dv["k"], dv["v"], dv["g"], dv["beta"], dv["s0"], s_out,
+                        y, w.chunk, workspace=ws, stream=stream)
+        y_h.copy_(y, non_blocking=True)
+        s_h.copy_(s_out, non_blocking=True)
+        torch.cuda.synchronize(dev)   # the host reads the step's result
+
+    for _ in range(warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    sec = (time.perf_counter() - t0) / steps
+    return {"value": round(w.B * w.T / sec, 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(sec * 1e3, 4)}
+
+
+def bench_decode(gdn, w, dev, replays=3):
+    """256 successive decode steps captured in one CUDA graph (state in place);
+    the state (134 MB) is larger than the L2."""
+    steps = w.steps
+    s = gdn_inputs.workload_inputs(w, step=0)["s0"].to(dev)
+    step_in = []
+    for i in range(steps):
+        ins = gdn_inputs.workload_inputs(w, step=i)
+        step_in.append({n: ins[n].to(dev) for n in ("q", "k", "v", "g", "beta")})
+    ys = torch.empty((steps, w.B, 1, w.Hv, w.Dv), dtype=w.torch_dtype, device=dev)
+    side = torch.cuda.Stream(dev)
+    s_work = s.clone()
+
+    def run_all(stream):
+        for i in range(steps):
+            d = step_in[i]
+            gdn.gdn_decode_step(d["q"], d["k"], d["v"], d["g"], d["beta"], s_work, s_work,
+                                ys[i], stream=stream)
+
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        run_all(side)          # warm-up outside capture
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        run_all(side)
+    torch.cuda.synchronize(dev)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    times = []
+    for _ in range(replays):
+        s_work.copy_(s)
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        graph.replay()
+        b.record()
+        torch.cuda.synchronize(dev)
+        times.append(a.elapsed_time(b))
+    ms_graph = min(times)
+    us_step = ms_graph * 1e3 / steps
+    return us_step
+
+
+def oracle_sample(w, n_kh):
+    """The workload's first ``n_kh`` key heads and their value heads (every
+    token, every batch row) as a stand-alone problem for the oracle."""
+    ins = gdn_inputs.workload_inputs(w)
+    grp = w.Hv // w.Hk
+    n_kh = max(1, min(n_kh, w.Hk))
+    hv = n_kh * grp
+    sub = {"q": ins["q"][:, :, :n_kh], "k": ins["k"][:, :, :n_kh],
+           "v": ins["v"][:, :, :hv], "g": ins["g"][:, :, :hv],
+           "beta": ins["beta"][:, :, :hv], "s0": ins["s0"][:, :hv]}
+    return {n: t.contiguous() for n, t in sub.items()}, hv
+
+
+def time_oracle(sub, reps=1):
+    import oracle
+    names = ("q", "k", "v", "g", "beta")
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.gdn_sequential(*(sub[n] for n in names), sub["s0"])
+    return (time.perf_counter() - t0) / reps
+
+
+def oracle_threads(work_items):
+    import oracle
+    return max(1, min(oracle.num_threads(), work_items))
+
+
+def cpu_baseline_prefill(w):
+    """The fp64 oracle, as it stands, on the host cores over whole heads of the
+    workload (every token); enough heads to give every core one."""
+    cores = os.cpu_count() or 1
+    grp = w.Hv // w.Hk
+    sub, hv = oracle_sample(w, -(-cores // grp))
+    time_oracle(sub)                       # first call builds / loads the oracle
+    dt = time_oracle(sub)
+    value = w.B * w.T * hv / w.Hv / dt     # whole-workload tokens/s equivalent
+    return {"value": round(value, 2), "unit": "tokens/s",
+            "cores": oracle_threads(w.B * hv), "kind": "oracle",
+            "sample": f"{hv} of {w.Hv} value heads x B={w.B} x T={w.T} (every token), "
+                      f"fp64, {dt:.2f} s; tokens/s scaled by {hv}/{w.Hv}"}
+
+
+# ----------------------------------------------------------------------------
+# reference arm: the fp64 oracle on the host cores
+# ----------------------------------------------------------------------------
+def run_reference(args, w):
+    world, rank, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return 0
+    cores = os.cpu_count() or 1
+    grp = w.Hv // w.Hk
+    sub, hv = oracle_sample(w, -(-cores // grp))
+    for _ in range(args.warmup):
+        time_oracle(sub)
+    sec = time_oracle(sub, reps=args.steps)
+    value = w.B * w.T * hv / w.Hv / sec
+    sample = (f"{hv} of {w.Hv} value heads x B={w.B} x T={w.T} (every token) per step, "
+              f"fp64; tokens/s scaled by {hv}/{w.Hv}")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2),
+        "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "Hk": w.Hk, "Hv": w.Hv,
+                   "Dk": w.Dk, "Dv": w.Dv, "chunk": w.chunk, "input_dtype": w.dtype},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s",
+                         "cores": oracle_threads(w.B * hv), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+METRIC = "GDN prefill tokens/s (B=1 T=4096 Hk=16 Hv=32 D=128 bf16 C=64) and decode steps/s"
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="prefill_t4096")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip decode, e2e and cpu_baseline (for profiling runs)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    w = gdn_inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import gated_delta_rule_02_gb300 as gdn
+    world, rank, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    gdn.lib()
+    hbm, bf16, peak_kind = load_peaks()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    ms, wall = bench_prefill(gdn, w, dev, args.steps, args.warmup, world)
+    clocks = sampler.stop()
+    ms = max_over_ranks(ms, world)
+    tokens_per_s = world * w.B * w.T / (ms / 1e3)
+
+    line = {
+        "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "Hk": w.Hk, "Hv": w.Hv,
+                   "Dk": w.Dk, "Dv": w.Dv, "chunk": w.chunk, "state": "fp32",
+                   "l2": "256 MiB flush write between timed steps",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline(prefill_alg_bytes(w), ms / 1e3, hbm, peak_kind),
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    line["roofline"]["scope"] = "whole gdn_prefill call (all its kernels)"
+    line["roofline"]["tensor_tflops"] = round(prefill_alg_flops(w) / (ms / 1e3) / 1e12, 2)
+
+    if not args.no_extras:
+        if rank == 0 or world > 1:
+            line["e2e"] = bench_prefill_e2e(gdn, w, dev, max(3, args.steps // 5), 2)
+        dw = gdn_inputs.WORKLOADS["decode_b64"]
+        us = bench_decode(gdn, dw, dev)
+        line["decode"] = {
+            "workload": dw.name, "steps_per_s": round(1e6 / us, 1),
+            "tokens_per_s": round(dw.B * 1e6 / us, 1), "us_per_step": round(us, 3),
+            "timing": "256 steps in one CUDA graph, state in place (134 MB > L2)",
+            "roofline": roofline(decode_alg_bytes(dw), us / 1e6, hbm, peak_kind)}
+        if rank == 0 and world == 1:
+            line["cpu_baseline"] = cpu_baseline_prefill(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

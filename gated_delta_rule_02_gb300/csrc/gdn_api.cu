@@ -1,0 +1,87 @@
+// The C ABI of libgdn.so (declared in include/gdn.h): argument checking and
+// dispatch.  Every check runs on the host before anything is enqueued, so a
+// rejected call leaves every output untouched.
+#include "../../include/gdn.h"
+#include "gdn_internal.cuh"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_common(int B, int T, int Hk, int Hv, int Dk, int Dv, int dtype) {
+  if (B <= 0 || T <= 0 || Hk <= 0 || Hv <= 0 || Dk <= 0 || Dv <= 0) return GDN_ERR_INVALID;
+  if (Hv % Hk != 0) return GDN_ERR_INVALID;
+  if (Dk != gdn::kHeadDim || Dv != gdn::kHeadDim) return GDN_ERR_UNSUPPORTED;
+  if (dtype != GDN_DTYPE_F32 && dtype != GDN_DTYPE_BF16) return GDN_ERR_UNSUPPORTED;
+  return GDN_OK;
+}
+
+int check_pointers(const void* const* ptrs, int n) {
+  for (int i = 0; i < n; ++i)
+    if (ptrs[i] == nullptr) return GDN_ERR_INVALID;
+  for (int i = 0; i < n; ++i)
+    if (!aligned16(ptrs[i])) return GDN_ERR_ALIGNMENT;
+  return GDN_OK;
+}
+}  // namespace
+
+extern "C" {
+
+size_t gdn_prefill_workspace_bytes(int B, int T, int Hk, int Hv, int Dk, int Dv,
+                                   int chunk, int dtype) {
+  if (check_common(B, T, Hk, Hv, Dk, Dv, dtype) != GDN_OK) return 0;
+  if (chunk != 16 && chunk != 32 && chunk != 64) return 0;
+  return gdn::prefill_simt_workspace_bytes(B, T, Hv, chunk);
+}
+
+int gdn_prefill(const void* q, const void* k, const void* v, const void* g,
+                const void* beta, const float* state_in, float* state_out, void* y,
+                int B, int T, int Hk, int Hv, int Dk, int Dv, int chunk, int dtype,
+                void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_common(B, T, Hk, Hv, Dk, Dv, dtype);
+  if (st != GDN_OK) return st;
+  if (chunk != 16 && chunk != 32 && chunk != 64) return GDN_ERR_UNSUPPORTED;
+  const void* req[] = {q, k, v, g, beta, state_out, y};
+  st = check_pointers(req, 7);
+  if (st != GDN_OK) return st;
+  if (state_in && !aligned16(state_in)) return GDN_ERR_ALIGNMENT;
+  const size_t need = gdn_prefill_workspace_bytes(B, T, Hk, Hv, Dk, Dv, chunk, dtype);
+  if (need > 0) {
+    if (workspace == nullptr || workspace_bytes < need) return GDN_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDN_ERR_ALIGNMENT;
+  }
+  gdn::PrefillArgs a{q, k, v, g, beta, state_in, state_out, y, B, T, Hk, Hv, chunk,
+                     dtype, workspace, workspace_bytes,
+                     static_cast<cudaStream_t>(stream)};
+  cudaError_t e = gdn::launch_prefill_simt(a);
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int gdn_decode_step(const void* q, const void* k, const void* v, const void* g,
+                    const void* beta, const float* state_in, float* state_out,
+                    void* y, int B, int Hk, int Hv, int Dk, int Dv, int dtype,
+                    void* stream) {
+  int st = check_common(B, 1, Hk, Hv, Dk, Dv, dtype);
+  if (st != GDN_OK) return st;
+  const void* req[] = {q, k, v, g, beta, state_in, state_out, y};
+  st = check_pointers(req, 8);
+  if (st != GDN_OK) return st;
+  gdn::DecodeArgs a{q, k, v, g, beta, state_in, state_out, y, B, Hk, Hv, dtype,
+                    static_cast<cudaStream_t>(stream)};
+  cudaError_t e = gdn::launch_decode(a);
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+const char* gdn_status_string(int status) {
+  switch (status) {
+    case GDN_OK: return "ok";
+    case GDN_ERR_INVALID: return "invalid argument (null pointer, size <= 0 or Hv % Hk != 0)";
+    case GDN_ERR_UNSUPPORTED: return "unsupported shape, chunk or dtype (Dk = Dv = 128, chunk 16/32/64, f32/bf16)";
+    case GDN_ERR_ALIGNMENT: return "pointer not 16-byte aligned (workspace: 256-byte)";
+    case GDN_ERR_WORKSPACE: return "workspace missing or smaller than gdn_prefill_workspace_bytes()";
+    case GDN_ERR_CUDA: return "CUDA launch error";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,77 @@
+// Internal interface between the C ABI (gdn_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace gdn {
+
+constexpr int kHeadDim = 128;  // Dk = Dv = 128 is the compiled head size
+
+struct PrefillArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* g;
+  const void* beta;
+  const float* state_in;  // may be nullptr (zero initial state)
+  float* state_out;
+  void* y;
+  int B, T, Hk, Hv, chunk, dtype;
+  void* workspace;
+  size_t workspace_bytes;
+  cudaStream_t stream;
+};
+
+struct DecodeArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* g;
+  const void* beta;
+  const float* state_in;
+  float* state_out;
+  void* y;
+  int B, Hk, Hv, dtype;
+  cudaStream_t stream;
+};
+
+// fp32 SIMT chunked path (any dtype; the exact path for fp32 inputs).
+size_t prefill_simt_workspace_bytes(int B, int T, int Hv, int chunk);
+cudaError_t launch_prefill_simt(const PrefillArgs& a);
+
+// Streaming single-step decode.
+cudaError_t launch_decode(const DecodeArgs& a);
+
+// ---------------------------------------------------------------------------
+// Small device helpers shared by the kernel files.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// Four consecutive elements widened to fp32 (16-byte / 8-byte aligned loads).
+__device__ __forceinline__ void load4(const float* p, float* out) {
+  const float4 t = *reinterpret_cast<const float4*>(p);
+  out[0] = t.x; out[1] = t.y; out[2] = t.z; out[3] = t.w;
+}
+__device__ __forceinline__ void load4(const __nv_bfloat16* p, float* out) {
+  const uint2 t = *reinterpret_cast<const uint2*>(p);
+  const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&t.x);
+  const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&t.y);
+  const float2 a = __bfloat1622float2(lo), b = __bfloat1622float2(hi);
+  out[0] = a.x; out[1] = a.y; out[2] = b.x; out[3] = b.y;
+}
+
+}  // namespace gdn

@@ -72,11 +72,12 @@ def _unit_rows(x: torch.Tensor) -> torch.Tensor:
 
 
 def make_inputs(B, T, Hk, Hv, Dk, Dv, dtype=torch.bfloat16, seed=0, u_max=0.1,
-                s0_std=0.1, heavy_frac=0.0, heavy_umax=5.0):
+                s0_std=0.1, heavy_frac=0.0, heavy_umax=5.0, draw_state=True):
     """One seeded draw of (q, k, v, g, beta, s0) on the CPU.
 
     Returns a dict of CPU tensors: q, k [B,T,Hk,Dk], v [B,T,Hv,Dv],
-    g, beta [B,T,Hv] in ``dtype`` and s0 [B,Hv,Dv,Dk] in fp32.
+    g, beta [B,T,Hv] in ``dtype`` and s0 [B,Hv,Dv,Dk] in fp32 (drawn last,
+    so ``draw_state=False`` leaves the other tensors unchanged and omits it).
     """
     if isinstance(dtype, str):
         dtype = torch.float32 if dtype == "f32" else torch.bfloat16
@@ -90,13 +91,13 @@ def make_inputs(B, T, Hk, Hv, Dk, Dv, dtype=torch.bfloat16, seed=0, u_max=0.1,
         u = torch.where(heavy, torch.rand((B, T, Hv), generator=gen) * heavy_umax, u)
     g = torch.exp(-u)
     beta = torch.sigmoid(torch.randn((B, T, Hv), generator=gen))
-    if s0_std > 0.0:
-        s0 = torch.randn((B, Hv, Dv, Dk), generator=gen) * s0_std
-    else:
-        s0 = torch.zeros((B, Hv, Dv, Dk))
     out = {name: t.to(dtype).contiguous() for name, t in
            (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta))}
-    out["s0"] = s0.contiguous()
+    if draw_state:
+        if s0_std > 0.0:
+            out["s0"] = (torch.randn((B, Hv, Dv, Dk), generator=gen) * s0_std).contiguous()
+        else:
+            out["s0"] = torch.zeros((B, Hv, Dv, Dk))
     return out
 
 
@@ -105,8 +106,9 @@ def workload_inputs(w: Workload, step: int | None = None):
 
     Decode steps draw fresh, independent inputs per step from seed
     ``w.seed + 7919 * step`` (T = 1); the initial state comes from step 0's
-    draw and is carried by the caller afterwards.
+    draw (later steps carry no ``s0``) and is carried by the caller afterwards.
     """
     seed = w.seed if step is None else w.seed + 7919 * step
     return make_inputs(w.B, w.T, w.Hk, w.Hv, w.Dk, w.Dv, w.torch_dtype, seed,
-                       w.u_max, w.s0_std, w.heavy_frac, w.heavy_umax)
+                       w.u_max, w.s0_std, w.heavy_frac, w.heavy_umax,
+                       draw_state=not step)

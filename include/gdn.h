@@ -1,0 +1,116 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) gated delta rule library, libgdn.so.
+ *
+ * The operation (ferrox-core `gdn_chunk.rs`, module docs, "The algebra";
+ * metaltile-std `gated_delta_wy.rs`, module docs, "Algorithm"): for every
+ * batch b and value head hv a state S (Dv x Dk, fp32) is carried through the
+ * tokens t of a sequence as
+ *
+ *     d_t = beta_t (v_t - g_t S_{t-1} k_t)
+ *     S_t = g_t S_{t-1} + d_t k_t^T
+ *     y_t = S_t q_t / sqrt(Dk)
+ *
+ * where g_t in (0, 1] is a multiplicative decay, beta_t the write strength,
+ * and q_t, k_t are read from key head hk = hv / (Hv / Hk) (grouped GQA map,
+ * metaltile-std `gated_delta_wy.rs`, "Layouts").
+ *
+ * Layouts (row-major, contiguous, every pointer a DEVICE pointer):
+ *     q, k        [B, T, Hk, Dk]     dtype
+ *     v, y        [B, T, Hv, Dv]     dtype
+ *     g, beta     [B, T, Hv]         dtype
+ *     state_in    [B, Hv, Dv, Dk]    fp32 (always)
+ *     state_out   [B, Hv, Dv, Dk]    fp32 (always)
+ * (metaltile-std `gated_delta_wy.rs`, "Layouts"; the state stays fp32.)
+ *
+ * Ownership: the caller owns every buffer, including any workspace; the
+ * library allocates no device memory.  All work is enqueued on `stream`
+ * (a cudaStream_t; NULL means the legacy default stream) and the calls
+ * return without synchronising.  state_in == state_out (in place) is
+ * allowed; any other overlap between inputs and outputs is undefined.
+ *
+ * Errors: every argument is checked on the host before anything is
+ * launched; on a non-zero return nothing has been enqueued and the outputs
+ * are untouched (except GDN_ERR_CUDA, see below).  No exception crosses
+ * the ABI.  gdn_status_string() names a code.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define GDN_OK                  0
+#define GDN_ERR_INVALID       (-1) /* NULL required pointer, a size <= 0, Hv % Hk != 0 */
+#define GDN_ERR_UNSUPPORTED   (-2) /* Dk/Dv other than 128, chunk not 16/32/64, bad dtype */
+#define GDN_ERR_ALIGNMENT     (-3) /* a pointer that is not 16-byte aligned */
+#define GDN_ERR_WORKSPACE     (-4) /* workspace NULL or smaller than gdn_prefill_workspace_bytes */
+#define GDN_ERR_CUDA          (-5) /* the CUDA runtime reported an error at launch; the
+                                      outputs are then unspecified */
+
+/* Element types of q, k, v, g, beta and y. */
+#define GDN_DTYPE_F32   0
+#define GDN_DTYPE_BF16  1
+
+/*
+ * Bytes of device workspace gdn_prefill needs for this shape (0 if none).
+ * Returns 0 as well for arguments gdn_prefill would reject.
+ */
+GDN_API size_t gdn_prefill_workspace_bytes(int B, int T, int Hk, int Hv, int Dk, int Dv,
+                                   int chunk, int dtype);
+
+/*
+ * Prefill: run T tokens of every (b, hv) through the rule, chunk by chunk
+ * (the chunked Woodbury-Young form of metaltile-std `gated_delta_wy.rs`,
+ * "Algorithm" steps 1-9, with the decay ratios formed as products as in
+ * ferrox-core `gdn_chunk.rs`, "The algebra").  Writes y for every token and
+ * the state after token T-1 into state_out.
+ *
+ *   state_in   NULL means S_0 = 0.
+ *   chunk      tokens per chunk: 16, 32 or 64.  Any T >= 1 is accepted; a
+ *              last chunk shorter than `chunk` behaves as if padded with
+ *              g = 1, beta = 0 tokens (metaltile-std kernel, chunk loop).
+ *   workspace  device scratch of at least gdn_prefill_workspace_bytes(...)
+ *              bytes, 256-byte aligned, owned by the caller; its contents on
+ *              entry do not matter and on return are unspecified.  It must
+ *              not be used by anything else until the work on `stream` is done.
+ *   stream     cudaStream_t, or NULL.
+ * Dk = Dv = 128.  Returns GDN_OK or a GDN_ERR_* code.
+ */
+GDN_API int gdn_prefill(const void *q, const void *k, const void *v, const void *g,
+                const void *beta, const float *state_in, float *state_out, void *y,
+                int B, int T, int Hk, int Hv, int Dk, int Dv, int chunk,
+                int dtype, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Decode: one token (T = 1) of every (b, hv) through the rule, streaming
+ * the state once (the single-step recurrence above; row packing after the
+ * MLX `gated_delta_seq` packed layout, PR "Pack gated_delta_seq: 8 value
+ * rows per SIMD-group").
+ *
+ *   q, k [B, 1, Hk, Dk]; v, y [B, 1, Hv, Dv]; g, beta [B, 1, Hv]
+ *   state_in must not be NULL; state_out may equal state_in (in place).
+ * Dk = Dv = 128.  No workspace.  Returns GDN_OK or a GDN_ERR_* code.
+ */
+GDN_API int gdn_decode_step(const void *q, const void *k, const void *v, const void *g,
+                    const void *beta, const float *state_in, float *state_out,
+                    void *y, int B, int Hk, int Hv, int Dk, int Dv, int dtype,
+                    void *stream);
+
+/* A static, NUL-terminated description of a status code. */
+GDN_API const char *gdn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

@@ -1,0 +1,72 @@
+"""Shared helpers for the parity tests: run the CUDA path and the oracle on
+the same seeded inputs and compare them.
+
+Tolerances (max |gpu - oracle| <= tol * max |oracle|, on y and on the final
+state): 1e-4 for fp32 inputs and 2e-2 for bf16 inputs.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
+NAMES = ("q", "k", "v", "g", "beta")
+
+
+def rel_err(a, ref) -> float:
+    a = np.asarray(a, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    scale = max(float(np.max(np.abs(ref))), 1e-30)
+    return float(np.max(np.abs(a - ref)) / scale)
+
+
+def to_device(ins, dev):
+    return {n: t.to(dev) for n, t in ins.items() if t is not None}
+
+
+def gpu_prefill(ins, chunk, dev, state_mode="given"):
+    """state_mode: 'given' (s0 -> new state_out), 'null' (state_in = NULL),
+    'inplace' (state_in is state_out)."""
+    import gated_delta_rule_02_gb300 as gdn
+    d = to_device(ins, dev)
+    B, T, Hk, Dk = d["q"].shape
+    Hv, Dv = d["v"].shape[2], d["v"].shape[3]
+    y = torch.empty((B, T, Hv, Dv), dtype=d["q"].dtype, device=dev)
+    if state_mode == "inplace":
+        s_in = s_out = d["s0"].clone()
+    else:
+        s_in = None if state_mode == "null" else d["s0"]
+        s_out = torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=dev)
+    gdn.gdn_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], s_in, s_out, y, chunk)
+    torch.cuda.synchronize(dev)
+    return y.float().cpu().numpy(), s_out.cpu().numpy()
+
+
+def oracle_prefill(ins, zero_state=False):
+    s0 = None if zero_state else ins["s0"]
+    return oracle.gdn_sequential(*(ins[n] for n in NAMES), s0)
+
+
+def head_slice(ins, heads):
+    """Inputs restricted to the listed (b, hv) heads, stacked as a batch of
+    single-head problems (Hk = Hv = 1), so the oracle can follow a few heads
+    of a large workload over the whole sequence."""
+    Hk, Hv = ins["q"].shape[2], ins["v"].shape[2]
+    grp = Hv // Hk
+    out = {}
+    for n in ("q", "k"):
+        out[n] = torch.stack([ins[n][b, :, hv // grp] for b, hv in heads])[:, :, None]
+    out["v"] = torch.stack([ins["v"][b, :, hv] for b, hv in heads])[:, :, None]
+    for n in ("g", "beta"):
+        out[n] = torch.stack([ins[n][b, :, hv] for b, hv in heads])[:, :, None]
+    out["s0"] = torch.stack([ins["s0"][b, hv] for b, hv in heads])[:, None]
+    return out
+
+
+def pick_heads(y, s, heads):
+    """Select (b, hv) heads from full GPU outputs, in head_slice's layout."""
+    ys = np.stack([y[b, :, hv] for b, hv in heads])[:, :, None]
+    ss = np.stack([s[b, hv] for b, hv in heads])[:, None]
+    return ys, ss
