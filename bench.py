@@ -313,19 +313,22 @@ def oracle_threads(work_items):
     return max(1, min(oracle.num_threads(), work_items))
 
 
-def cpu_baseline_prefill(w):
-    """The fp64 oracle, as it stands, on the host cores over whole heads of the
-    workload (every token); enough heads to give every core one."""
-    cores = os.cpu_count() or 1
-    grp = w.Hv // w.Hk
-    sub, hv = oracle_sample(w, -(-cores // grp))
+def cpu_baseline_prefill(w, min_seconds=10.0, max_reps=50):
+    """The fp64 oracle, as it stands, on the host cores over the whole
+    workload (every head, every token), repeated until about ten seconds of
+    CPU work have been timed."""
+    sub, hv = oracle_sample(w, w.Hk)
     time_oracle(sub)                       # first call builds / loads the oracle
-    dt = time_oracle(sub)
-    value = w.B * w.T * hv / w.Hv / dt     # whole-workload tokens/s equivalent
+    reps, total = 0, 0.0
+    while total < min_seconds and reps < max_reps:
+        total += time_oracle(sub)
+        reps += 1
+    dt = total / reps
+    value = w.B * w.T * hv / w.Hv / dt
     return {"value": round(value, 2), "unit": "tokens/s",
             "cores": oracle_threads(w.B * hv), "kind": "oracle",
-            "sample": f"{hv} of {w.Hv} value heads x B={w.B} x T={w.T} (every token), "
-                      f"fp64, {dt:.2f} s; tokens/s scaled by {hv}/{w.Hv}"}
+            "sample": f"the whole workload ({hv} value heads x B={w.B} x T={w.T}), fp64, "
+                      f"{reps} runs, {total:.1f} s"}
 
 
 # ----------------------------------------------------------------------------
@@ -374,6 +377,8 @@ def main():
     ap.add_argument("--workload", default="prefill_t4096")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip decode, e2e and cpu_baseline (for profiling runs)")
+    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode"],
+                    help="profiling runs: time one path only (prints a partial line)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = gdn_inputs.WORKLOADS[args.workload]
@@ -386,6 +391,16 @@ def main():
     torch.cuda.set_device(dev)
     gdn.lib()
     hbm, bf16, peak_kind = load_peaks()
+    if args.only == "decode":
+        dw = gdn_inputs.WORKLOADS["decode_b64"]
+        us = bench_decode(gdn, dw, dev)
+        print(json.dumps({"partial": "decode only", "workload": dw.name,
+                          "us_per_step": round(us, 3),
+                          "roofline": roofline(decode_alg_bytes(dw), us / 1e6, hbm,
+                                               peak_kind)}), flush=True)
+        return 0
+    if args.only == "prefill":
+        args.no_extras = True
 
     sampler = ClockSampler(local)
     sampler.start()
