@@ -32,6 +32,7 @@ GDN_ERR_UNSUPPORTED = -2
 GDN_ERR_ALIGNMENT = -3
 GDN_ERR_WORKSPACE = -4
 GDN_ERR_CUDA = -5
+GDN_ERR_DEVICE_TIMEOUT = -6
 GDN_DTYPE_F32 = 0
 GDN_DTYPE_BF16 = 1
 
@@ -65,12 +66,20 @@ def lib() -> ctypes.CDLL:
             L.gdn_decode_step.restype = i
             L.gdn_status_string.argtypes = [i]
             L.gdn_status_string.restype = ctypes.c_char_p
+            L.gdn_device_status.argtypes = [i]
+            L.gdn_device_status.restype = i
             _lib = L
     return _lib
 
 
 def gdn_status_string(status: int) -> str:
     return lib().gdn_status_string(int(status)).decode()
+
+
+def gdn_device_status(clear: bool = False) -> int:
+    """GDN_OK, or GDN_ERR_DEVICE_TIMEOUT if a kernel's bounded wait gave up
+    (synchronises the device)."""
+    return int(lib().gdn_device_status(1 if clear else 0))
 
 
 def gdn_prefill_workspace_bytes(B, T, Hk, Hv, Dk, Dv, chunk, dtype) -> int:

@@ -31,6 +31,7 @@ size_t gdn_prefill_workspace_bytes(int B, int T, int Hk, int Hv, int Dk, int Dv,
                                    int chunk, int dtype) {
   if (check_common(B, T, Hk, Hv, Dk, Dv, dtype) != GDN_OK) return 0;
   if (chunk != 16 && chunk != 32 && chunk != 64) return 0;
+  if (dtype == GDN_DTYPE_BF16) return gdn::prefill_tc_workspace_bytes(B, T, Hv);
   return gdn::prefill_simt_workspace_bytes(B, T, Hv, chunk);
 }
 
@@ -53,7 +54,8 @@ int gdn_prefill(const void* q, const void* k, const void* v, const void* g,
   gdn::PrefillArgs a{q, k, v, g, beta, state_in, state_out, y, B, T, Hk, Hv, chunk,
                      dtype, workspace, workspace_bytes,
                      static_cast<cudaStream_t>(stream)};
-  cudaError_t e = gdn::launch_prefill_simt(a);
+  cudaError_t e = dtype == GDN_DTYPE_BF16 ? gdn::launch_prefill_tc(a)
+                                           : gdn::launch_prefill_simt(a);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -72,6 +74,12 @@ int gdn_decode_step(const void* q, const void* k, const void* v, const void* g,
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+int gdn_device_status(int clear) {
+  const int v = gdn::prefill_tc_device_error(clear != 0);
+  if (v < 0) return GDN_ERR_CUDA;
+  return v ? GDN_ERR_DEVICE_TIMEOUT : GDN_OK;
+}
+
 const char* gdn_status_string(int status) {
   switch (status) {
     case GDN_OK: return "ok";
@@ -80,6 +88,7 @@ const char* gdn_status_string(int status) {
     case GDN_ERR_ALIGNMENT: return "pointer not 16-byte aligned (workspace: 256-byte)";
     case GDN_ERR_WORKSPACE: return "workspace missing or smaller than gdn_prefill_workspace_bytes()";
     case GDN_ERR_CUDA: return "CUDA launch error";
+    case GDN_ERR_DEVICE_TIMEOUT: return "a device-side wait gave up (bounded wait timed out)";
     default: return "unknown status";
   }
 }

@@ -43,6 +43,13 @@ struct DecodeArgs {
 size_t prefill_simt_workspace_bytes(int B, int T, int Hv, int chunk);
 cudaError_t launch_prefill_simt(const PrefillArgs& a);
 
+// tcgen05 chunked path (bf16 inputs): prep + scan launches.
+size_t prefill_tc_workspace_bytes(int B, int T, int Hv);
+cudaError_t launch_prefill_tc(const PrefillArgs& a);
+// Reads (and optionally clears) the tensor-core kernels' device error word;
+// -1 if it cannot be read.
+int prefill_tc_device_error(bool clear);
+
 // Streaming single-step decode.
 cudaError_t launch_decode(const DecodeArgs& a);
 

@@ -56,6 +56,7 @@ extern "C" {
 #define GDN_ERR_WORKSPACE     (-4) /* workspace NULL or smaller than gdn_prefill_workspace_bytes */
 #define GDN_ERR_CUDA          (-5) /* the CUDA runtime reported an error at launch; the
                                       outputs are then unspecified */
+#define GDN_ERR_DEVICE_TIMEOUT (-6) /* a kernel's bounded wait gave up (see gdn_device_status) */
 
 /* Element types of q, k, v, g, beta and y. */
 #define GDN_DTYPE_F32   0
@@ -105,6 +106,16 @@ GDN_API int gdn_decode_step(const void *q, const void *k, const void *v, const v
                     const void *beta, const float *state_in, float *state_out,
                     void *y, int B, int Hk, int Hv, int Dk, int Dv, int dtype,
                     void *stream);
+
+/*
+ * Device-side health: every wait inside the tensor-core kernels (on an
+ * mbarrier fed by TMA or by the tensor core) is bounded; a wait that gives up
+ * sets a device error word and the kernel returns early, leaving its outputs
+ * unspecified.  This call synchronises the device, reads that word and
+ * returns GDN_OK, GDN_ERR_DEVICE_TIMEOUT, or GDN_ERR_CUDA if it cannot be
+ * read.  A non-zero `clear` resets the word.
+ */
+GDN_API int gdn_device_status(int clear);
 
 /* A static, NUL-terminated description of a status code. */
 GDN_API const char *gdn_status_string(int status);

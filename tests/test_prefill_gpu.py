@@ -112,3 +112,9 @@ def test_prefill_full_size_sampled_heads(cuda_device, name):
     yg, sg = pick_heads(y, s, heads)
     assert rel_err(yg, yo) <= TOL[BF16], rel_err(yg, yo)
     assert rel_err(sg, so) <= TOL[BF16], rel_err(sg, so)
+
+
+def test_no_device_wait_timed_out(cuda_device):
+    """No bounded device-side wait gave up during the runs above."""
+    import gated_delta_rule_02_gb300 as gdn
+    assert gdn.gdn_device_status() == gdn.GDN_OK
