@@ -39,7 +39,6 @@ using bf16 = __nv_bfloat16;
 
 constexpr int kTile = 64;   // tokens per tile
 constexpr int kD = kHeadDim;
-constexpr int kLdC = 65;    // padded fp32 row stride of the 64 x 64 matrices
 
 // ------------------------------- workspace --------------------------------
 struct WsLayout {
@@ -92,6 +91,11 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
                : "memory");
   return v;
 }
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
 __device__ __forceinline__ void unpack8(uint4 v, float* f) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -111,30 +115,30 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
 // prep kernel
 // ============================================================================
 constexpr int kPrepThreads = 256;
-// shared-memory map (bytes from the 1024-aligned base)
-constexpr uint32_t kOffKQ = 0;               // [K;Q] 2 halves x 128 rows x 128 B
-constexpr uint32_t kOffV = 32 * 1024;        // V   2 halves x 64 rows x 128 B
-constexpr uint32_t kOffA = 48 * 1024;        // A2 then A3: 2 halves x 128 rows x 128 B
-constexpr uint32_t kOffB3 = 80 * 1024;       // [P; U] MN-major, 2 atoms x 128 rows x 128 B
-constexpr uint32_t kOffF = 112 * 1024;       // fp32 area
-constexpr int kMatF = 64 * kLdC;             // floats per 64 x 64 padded matrix
-constexpr uint32_t kPrepSmem = kOffF + (5 * kMatF + 6 * 256 + 4 * 64) * 4 + 1024;
+// Shared-memory map (bytes from the 1024-aligned base); two CTAs fit per SM.
+constexpr uint32_t kOffKQ = 0;              // [K;Q]: 2 halves x (64 K rows + 64 Q rows) x 128 B
+constexpr uint32_t kOffV = 32 * 1024;       // V: 2 halves x 64 rows x 128 B
+constexpr uint32_t kOffA = 48 * 1024;       // A2 then A3: 128 rows x 64 K-cols (one 128B half)
+constexpr uint32_t kOffB = 64 * 1024;       // X, T_L (fp32) during the inverse; then P, U (MN-major)
+constexpr uint32_t kOffQK = 96 * 1024;      // QK^T, bf16 [64][64]
+constexpr uint32_t kOffSmall = 104 * 1024;  // lraw, lam, bta, gsuf [64]; gc[4]; Z[3*256]
+constexpr uint32_t kPrepSmem = kOffSmall + (64 * 4 + 4 + 3 * 256) * 4 + 1024;
 
-struct PrepF {            // fp32 views into the fp32 area
-  float *kk, *qk, *gam, *tl, *ta, *z0, *z1, *g, *b, *gpre, *gsuf;
-};
+// fp32 64 x 64 matrix with the column index XORed by the row's low 5 bits:
+// a warp touching one column of 32 consecutive rows hits 32 banks.
+__device__ __forceinline__ int fsw(int r, int c) { return r * 64 + (c ^ (r & 31)); }
 
-// Inverse of the unit lower-triangular (I + X), X strictly lower and block
-// diagonal by chunk, by blocked forward substitution with 16 x 16 diagonal
-// blocks; 128 threads (`u` = 0..127) cooperate, `bar` is their named barrier.
-//   diagonal blocks: T_ii = (I + X_ii)^-1, one column per thread
-//   block row i > 0: Z_ij = sum_{k=j}^{i-1} X_ik T_kj,  T_ij = -T_ii Z_ij
-template <int C, typename XF>
-__device__ void invert_unit_lower(XF X, float* Tm, float* Z, int u, int bar) {
-  // zero the blocks above the diagonal
-  for (int idx = u; idx < 64 * 64; idx += 128) {
+// T = (I + X)^-1 for X strictly lower triangular and block diagonal by chunk
+// (zero across chunks), by blocked forward substitution on 16 x 16 blocks
+// with all 256 threads:
+//   diagonal blocks  T_ii = (I + X_ii)^-1            (one column per thread)
+//   block row i > 0  Z_ij = sum_{k=j}^{i-1} X_ik T_kj,  T_ij = -T_ii Z_ij
+// Blocks of different chunks are zero and are written as such.
+template <int C>
+__device__ void invert_unit_lower(const float* X, float* Tm, float* Z, int u) {
+  for (int idx = u; idx < 64 * 64; idx += kPrepThreads) {
     const int r = idx >> 6, c = idx & 63;
-    if ((c >> 4) > (r >> 4)) Tm[r * kLdC + c] = 0.f;
+    if ((c >> 4) > (r >> 4) || (c / C) != (r / C)) Tm[fsw(r, c)] = 0.f;
   }
   if (u < 64) {
     const int bi = u >> 4, jj = u & 15, base = bi * 16;
@@ -143,47 +147,43 @@ __device__ void invert_unit_lower(XF X, float* Tm, float* Z, int u, int bar) {
     for (int r = 0; r < 16; ++r) {
       float acc = (r == jj) ? 1.f : 0.f;
 #pragma unroll
-      for (int s = 0; s < r; ++s) acc = fmaf(-X(base + r, base + s), x[s], acc);
+      for (int s = 0; s < r; ++s) acc = fmaf(-X[fsw(base + r, base + s)], x[s], acc);
       x[r] = acc;
     }
 #pragma unroll
-    for (int r = 0; r < 16; ++r) Tm[(base + r) * kLdC + base + jj] = x[r];
+    for (int r = 0; r < 16; ++r) Tm[fsw(base + r, base + jj)] = x[r];
   }
-  named_bar_sync(bar, 128);
-  if (C == 16) {
-    for (int idx = u; idx < 64 * 64; idx += 128) {
-      const int r = idx >> 6, c = idx & 63;
-      if ((c >> 4) < (r >> 4)) Tm[r * kLdC + c] = 0.f;
-    }
-    named_bar_sync(bar, 128);
-    return;
-  }
+  __syncthreads();
+  if constexpr (C != 16) {
   for (int bi = 1; bi < 4; ++bi) {
-    // Z_{bi, bj} for bj < bi: bi * 256 outputs
-    for (int idx = u; idx < bi * 256; idx += 128) {
-      const int bj = idx >> 8, r = (idx >> 4) & 15, c = idx & 15;
+    const int bj0 = ((bi * 16) / C) * (C / 16);  // first block of bi's chunk
+    const int nb = bi - bj0;                      // blocks to fill in this row
+    if (nb <= 0) continue;
+    for (int idx = u; idx < nb * 256; idx += kPrepThreads) {
+      const int bj = bj0 + (idx >> 8), r = (idx >> 4) & 15, c = idx & 15;
       float acc = 0.f;
       for (int k = bj; k < bi; ++k)
 #pragma unroll
         for (int s = 0; s < 16; ++s)
-          acc = fmaf(X(bi * 16 + r, k * 16 + s), Tm[(k * 16 + s) * kLdC + bj * 16 + c], acc);
+          acc = fmaf(X[fsw(bi * 16 + r, k * 16 + s)], Tm[fsw(k * 16 + s, bj * 16 + c)], acc);
       Z[idx] = acc;
     }
-    named_bar_sync(bar, 128);
-    for (int idx = u; idx < bi * 256; idx += 128) {
-      const int bj = idx >> 8, r = (idx >> 4) & 15, c = idx & 15;
+    __syncthreads();
+    for (int idx = u; idx < nb * 256; idx += kPrepThreads) {
+      const int bj = bj0 + (idx >> 8), r = (idx >> 4) & 15, c = idx & 15;
       float acc = 0.f;
 #pragma unroll
       for (int s = 0; s < 16; ++s)
-        acc = fmaf(Tm[(bi * 16 + r) * kLdC + bi * 16 + s], Z[bj * 256 + s * 16 + c], acc);
-      Tm[(bi * 16 + r) * kLdC + bj * 16 + c] = -acc;
+        acc = fmaf(Tm[fsw(bi * 16 + r, bi * 16 + s)], Z[(idx & ~255) + s * 16 + c], acc);
+      Tm[fsw(bi * 16 + r, bj * 16 + c)] = -acc;
     }
-    named_bar_sync(bar, 128);
+    __syncthreads();
+  }
   }
 }
 
 template <int C>
-__global__ void __launch_bounds__(kPrepThreads, 1)
+__global__ void __launch_bounds__(kPrepThreads, 2)
 prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_v, const bf16* __restrict__ g,
                const bf16* __restrict__ beta, bf16* __restrict__ wsA1, bf16* __restrict__ wsUY,
@@ -195,12 +195,15 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   __shared__ uint32_t tmem_base_sh;
   const uint32_t sbase = smem_u32(sm);
   const uint32_t bar_tma = smem_u32(&bars[0]), bar_mma = smem_u32(&bars[1]);
-
-  float* fa = reinterpret_cast<float*>(sm + kOffF);
-  PrepF f;
-  f.kk = fa; f.qk = fa + kMatF; f.gam = fa + 2 * kMatF; f.tl = fa + 3 * kMatF;
-  f.ta = fa + 4 * kMatF; f.z0 = fa + 5 * kMatF; f.z1 = f.z0 + 3 * 256;
-  f.g = f.z1 + 3 * 256; f.b = f.g + 64; f.gpre = f.b + 64; f.gsuf = f.gpre + 64;
+  float* X = reinterpret_cast<float*>(sm + kOffB);          // 64 x 64 fp32
+  float* TL = reinterpret_cast<float*>(sm + kOffB + 16384);  // 64 x 64 fp32
+  bf16* sQK = reinterpret_cast<bf16*>(sm + kOffQK);          // 64 x 64 bf16
+  float* lraw = reinterpret_cast<float*>(sm + kOffSmall);    // log2 g per token
+  float* lam = lraw + 64;                                     // chunk-local prefix of lraw
+  float* bta = lam + 64;
+  float* gsuf = bta + 64;                                     // g_{t+1} .. g_{chunk end}
+  float* gc = gsuf + 64;                                      // G at each chunk's end
+  float* Z = gc + 4;
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int tile = blockIdx.x, bh = blockIdx.y;
@@ -214,14 +217,13 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(smem_u32(&tmem_base_sh), 512);
+    tmem_alloc(smem_u32(&tmem_base_sh), 256);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-  const uint32_t tD1 = tmem, tD2 = tmem + 64, tD3 = tmem + 192;
 
   if (tid == 0) {
     prefetch_tmap(&tm_k);
@@ -236,42 +238,40 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     tma_load_4d(sbase + kOffV + 8192, &tm_v, bar_tma, 64, hv, t0, b);
   }
 
-  // Gates of the tile's tokens; padded tokens take g = 1, beta = 0.
+  // Gates (step 2).  Padded tokens take g = 1, beta = 0.  The decay products
+  // are carried as chunk-local prefix sums of log2 g, so that
+  // G_t = 2^lam_t and Gam[t][j] = 2^(lam_t - lam_j), j <= t: no division, and
+  // a vanishing product underflows to 0.
   if (tid < 64) {
     const int tok = t0 + tid;
     const bool valid = tok < T;
     const size_t gi = ((size_t)b * T + tok) * Hv + hv;
-    f.g[tid] = valid ? __bfloat162float(g[gi]) : 1.f;
-    f.b[tid] = valid ? __bfloat162float(beta[gi]) : 0.f;
+    bta[tid] = valid ? __bfloat162float(beta[gi]) : 0.f;
+    lraw[tid] = valid ? fmaxf(__log2f(__bfloat162float(g[gi])), -1000.f) : 0.f;
   }
   __syncthreads();
   if (tid < 64) {
     const int t = tid, cs = (t / C) * C, ce = cs + C - 1;
-    float pre = 1.f;
-    for (int i = cs; i <= t; ++i) pre *= f.g[i];
-    float suf = 1.f;
-    for (int i = t + 1; i <= ce; ++i) suf *= f.g[i];
-    f.gpre[t] = pre;
-    f.gsuf[t] = suf;
-    float* row = f.gam + t * kLdC;
-    for (int j = 0; j < 64; ++j) row[j] = 0.f;
-    float r = 1.f;
-    row[t] = 1.f;
-    for (int j = t - 1; j >= cs; --j) {
-      r *= f.g[j + 1];
-      row[j] = r;
+    float pre = 0.f, all = 0.f;
+    for (int i = cs; i <= ce; ++i) {
+      const float l = lraw[i];
+      all += l;
+      if (i <= t) pre += l;
     }
+    lam[t] = pre;
+    gsuf[t] = exp2f(all - pre);
+    if (t == ce) gc[t / C] = exp2f(all);
   }
 
   bool ok = mbar_wait(bar_tma, 0);
-  // G1: D1[128 x 64] = [K; Q] K^T.
+  // G1: D[128 x 64] = [K; Q] K^T  (TMEM columns 0..63).
   if (ok && tid == 0) {
     tc_fence_after();
     const uint32_t id1 = idesc_bf16(128, 64, false, false);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       const uint32_t a = sbase + kOffKQ + (kk >> 2) * 16384 + (kk & 3) * 32;
-      mma_bf16_ss(tD1, smem_desc(a, 16, 1024, kSw128), smem_desc(a, 16, 1024, kSw128), id1,
+      mma_bf16_ss(tmem, smem_desc(a, 16, 1024, kSw128), smem_desc(a, 16, 1024, kSw128), id1,
                   kk > 0);
     }
     mma_commit(bar_mma);
@@ -279,64 +279,70 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   ok = ok && mbar_wait(bar_mma, 0);
   tc_fence_after();
   if (ok && tid < 128) {
+    // Row t of KK^T -> row t of X = L (step 4): X[t][j] = beta_j KK^T[t][j],
+    // j < t in t's chunk.  Row t of QK^T -> bf16 for the A3 operand.
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    float* dst = tid < 64 ? f.kk + tid * kLdC : f.qk + (tid - 64) * kLdC;
+    const int t = tid & 63;
+    const int cs = (t / C) * C;
 #pragma unroll
-    for (int c = 0; c < 64; c += 16) {
+    for (int c0 = 0; c0 < 64; c0 += 16) {
       float v[16];
-      tmem_ld16(tD1 + lane_base + c, v);
+      tmem_ld16(tmem + lane_base + c0, v);
       tmem_wait_ld();
+      if (tid < 64) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) dst[c + j] = v[j];
+        for (int e = 0; e < 16; ++e) {
+          const int j = c0 + e;
+          X[fsw(t, j)] = (j < t && j >= cs) ? bta[j] * v[e] : 0.f;
+        }
+      } else {
+        *reinterpret_cast<uint4*>(sQK + t * 64 + c0) = pack8(v);
+        *reinterpret_cast<uint4*>(sQK + t * 64 + c0 + 8) = pack8(v + 8);
+      }
     }
   }
   ok = __syncthreads_and(ok);
 
-  // Steps 4 and 5: the two triangular inverses, one per 128-thread group.
-  if (ok) {
-    const float* kk = f.kk;
-    const float* gam = f.gam;
-    const float* bb = f.b;
-    if (tid < 128) {
-      auto XL = [=](int t, int j) { return j / C == t / C ? bb[j] * kk[t * kLdC + j] : 0.f; };
-      invert_unit_lower<C>(XL, f.tl, f.z0, tid, 1);
-    } else {
-      auto XA = [=](int t, int j) { return bb[t] * gam[t * kLdC + j] * kk[t * kLdC + j]; };
-      invert_unit_lower<C>(XA, f.ta, f.z1, tid - 128, 2);
-    }
-  }
-  __syncthreads();
+  // Step 4: T_L = (I + L)^-1.  Step 5 needs no second inverse:
+  // (I + A)^-1 diag(beta) = diag(beta) (Gam . T_L) for A[t][j] = beta_t Gam[t][j] KK^T[t][j].
+  if (ok) invert_unit_lower<C>(X, TL, Z, tid);
+  else __syncthreads();
 
-  // A2 = [T_L 0; 0 T_A diag(beta)] (K-major, 128B swizzle).
+  // A2 = [T_L; diag(beta) (Gam . T_L)]: 128 rows x 64 K-cols, K-major 128B swizzle.
   if (ok) {
-    for (int idx = tid; idx < 128 * 16; idx += kPrepThreads) {
-      const int row = idx >> 4, ch = idx & 15, col0 = ch * 8;
+    for (int idx = tid; idx < 128 * 8; idx += kPrepThreads) {
+      const int row = idx >> 3, col0 = (idx & 7) * 8;
+      const int t = row & 63, cs = (t / C) * C;
       float v[8];
-      const bool top = row < 64;
-      const int t = row & 63;
-      const bool live = top ? (col0 < 64) : (col0 >= 64);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const int c = (col0 + e) & 63;
-        v[e] = !live ? 0.f : (top ? f.tl[t * kLdC + c] : f.ta[t * kLdC + c] * f.b[c]);
+        const int j = col0 + e;
+        const float tl = TL[fsw(t, j)];
+        v[e] = row < 64 ? tl
+                        : ((j <= t && j >= cs) ? bta[t] * exp2f(lam[t] - lam[j]) * tl : 0.f);
       }
-      st_shared_v4(sbase + kOffA + (col0 >> 6) * 16384 + sw128(row, col0 & 63), pack8(v));
+      st_shared_v4(sbase + kOffA + sw128(row, col0), pack8(v));
     }
     fence_proxy_async();
   }
   ok = __syncthreads_and(ok);
 
-  // G2: D2[128 x 128] = A2 [K; V]  (B MN-major: tokens are the reduction).
+  // G2: D2a = A2 K (cols 0..127; rows 0..63 = P = T_L K) and
+  //     D2b = A2 V (cols 128..255; rows 64..127 = U = T_A (beta V)).
   if (ok && tid == 0) {
     tc_fence_after();
     const uint32_t id2 = idesc_bf16(128, 128, false, true);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t a = sbase + kOffA + (kk >> 2) * 16384 + (kk & 3) * 32;
-      const uint64_t bdesc =
-          kk < 4 ? smem_desc(sbase + kOffKQ + kk * 2048, 16384, 1024, kSw128)
-                 : smem_desc(sbase + kOffV + (kk - 4) * 2048, 8192, 1024, kSw128);
-      mma_bf16_ss(tD2, smem_desc(a, 16, 1024, kSw128), bdesc, id2, kk > 0);
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint64_t ad = smem_desc(sbase + kOffA + kk * 32, 16, 1024, kSw128);
+      mma_bf16_ss(tmem, ad, smem_desc(sbase + kOffKQ + kk * 2048, 16384, 1024, kSw128), id2,
+                  kk > 0);
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint64_t ad = smem_desc(sbase + kOffA + kk * 32, 16, 1024, kSw128);
+      mma_bf16_ss(tmem + 128, ad, smem_desc(sbase + kOffV + kk * 2048, 8192, 1024, kSw128), id2,
+                  kk > 0);
     }
     mma_commit(bar_mma);
   }
@@ -344,69 +350,67 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   tc_fence_after();
 
   if (ok && tid < 128) {
-    // Rows of D2: P (lanes 0..63) and U (lanes 64..127) -> B3 (bf16) and the
-    // workspace rows Pt = G_C beta P and Ut = Gam[C-1][.] U.
+    // P rows (lanes 0..63) and U rows (lanes 64..127): bf16 into the G3 operand
+    // and, scaled, into the workspace: Pt = G_C beta P (step 9), Ut = Gam[C-1][.] U.
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const int m = tid & 63;
-    const int c = m / C;
-    const int brow = tid;  // B3 K-row: P rows 0..63, U rows 64..127
-    float scale;
-    bf16* gdst;
-    if (tid < 64) {
-      scale = f.gpre[c * C + C - 1] * f.b[m];
-      gdst = wsA1 + (tile_id * 128 + 2 * C * c + (m % C)) * kD;
-    } else {
-      scale = f.gsuf[m];
-      gdst = wsUY + (tile_id * 128 + m) * kD;
-    }
+    const bool top = tid < 64;
+    const int t = tid & 63;
+    const uint32_t src = tmem + lane_base + (top ? 0 : 128);
+    const uint32_t bdst = sbase + kOffB + (top ? 0 : 16384);
+    const float scale = top ? gc[t / C] * bta[t] : gsuf[t];
+    bf16* gdst = top ? wsA1 + (tile_id * 128 + 2 * C * (t / C) + (t % C)) * kD
+                     : wsUY + (tile_id * 128 + t) * kD;
 #pragma unroll
     for (int col = 0; col < 128; col += 16) {
       float v[16];
-      tmem_ld16(tD2 + lane_base + col, v);
+      tmem_ld16(src + col, v);
       tmem_wait_ld();
-      const uint4 raw0 = pack8(v), raw1 = pack8(v + 8);
-      const int atom = col >> 6, cc = col & 63;
-      st_shared_v4(sbase + kOffB3 + atom * 16384 + sw128(brow, cc), raw0);
-      st_shared_v4(sbase + kOffB3 + atom * 16384 + sw128(brow, cc + 8), raw1);
-      float w[16];
+      const uint32_t atom = bdst + (col >> 6) * 8192;
+      st_shared_v4(atom + sw128(t, col & 63), pack8(v));
+      st_shared_v4(atom + sw128(t, (col & 63) + 8), pack8(v + 8));
 #pragma unroll
-      for (int j = 0; j < 16; ++j) w[j] = v[j] * scale;
-      *reinterpret_cast<uint4*>(gdst + col) = pack8(w);
-      *reinterpret_cast<uint4*>(gdst + col + 8) = pack8(w + 8);
+      for (int j = 0; j < 16; ++j) v[j] *= scale;
+      *reinterpret_cast<uint4*>(gdst + col) = pack8(v);
+      *reinterpret_cast<uint4*>(gdst + col + 8) = pack8(v + 8);
     }
   } else if (ok) {
-    // A3 = [diag(G) M 0; 0 Gam.QK^T] with M[t][i] = beta_i QK^T[t][i], i <= t.
-    for (int idx = tid - 128; idx < 128 * 16; idx += 128) {
-      const int row = idx >> 4, ch = idx & 15, col0 = ch * 8;
-      const bool top = row < 64;
-      const int t = row & 63;
-      const bool live = top ? (col0 < 64) : (col0 >= 64);
-      float v[8];
+    // A3 = [diag(G) M; Gam . QK^T] (128 x 64), M[t][i] = beta_i QK^T[t][i], i <= t.
+    for (int idx = tid - 128; idx < 128 * 8; idx += 128) {
+      const int row = idx >> 3, col0 = (idx & 7) * 8;
+      const int t = row & 63, cs = (t / C) * C;
+      float q[8], v[8];
+      unpack8(*reinterpret_cast<const uint4*>(sQK + t * 64 + col0), q);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const int j = (col0 + e) & 63;
-        const bool causal = j <= t && j / C == t / C;  // same chunk, j <= t
-        float val = 0.f;
-        if (live && causal)
-          val = top ? f.gpre[t] * f.b[j] * f.qk[t * kLdC + j]
-                    : f.gam[t * kLdC + j] * f.qk[t * kLdC + j];
-        v[e] = val;
+        const int j = col0 + e;
+        const bool causal = j <= t && j >= cs;
+        v[e] = !causal ? 0.f
+                       : (row < 64 ? exp2f(lam[t]) * bta[j] * q[e]
+                                   : exp2f(lam[t] - lam[j]) * q[e]);
       }
-      st_shared_v4(sbase + kOffA + (col0 >> 6) * 16384 + sw128(row, col0 & 63), pack8(v));
+      st_shared_v4(sbase + kOffA + sw128(row, col0), pack8(v));
     }
   }
   if (ok) fence_proxy_async();
   ok = __syncthreads_and(ok);
 
-  // G3: D3[128 x 128] = A3 [P; U].
+  // G3: D3a = A3 P (cols 0..127; rows 0..63 = G M P),
+  //     D3b = A3 U (cols 128..255; rows 64..127 = y_loc).
   if (ok && tid == 0) {
     tc_fence_after();
     const uint32_t id3 = idesc_bf16(128, 128, false, true);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t a = sbase + kOffA + (kk >> 2) * 16384 + (kk & 3) * 32;
-      const uint64_t bdesc = smem_desc(sbase + kOffB3 + kk * 2048, 16384, 1024, kSw128);
-      mma_bf16_ss(tD3, smem_desc(a, 16, 1024, kSw128), bdesc, id3, kk > 0);
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint64_t ad = smem_desc(sbase + kOffA + kk * 32, 16, 1024, kSw128);
+      mma_bf16_ss(tmem, ad, smem_desc(sbase + kOffB + kk * 2048, 8192, 1024, kSw128), id3,
+                  kk > 0);
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint64_t ad = smem_desc(sbase + kOffA + kk * 32, 16, 1024, kSw128);
+      mma_bf16_ss(tmem + 128, ad,
+                  smem_desc(sbase + kOffB + 16384 + kk * 2048, 8192, 1024, kSw128), id3,
+                  kk > 0);
     }
     mma_commit(bar_mma);
   }
@@ -415,34 +419,34 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 
   if (ok && tid < 128) {
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const int m = tid & 63;
-    const int c = m / C;
     const bool top = tid < 64;
-    bf16* gdst = top ? wsA1 + (tile_id * 128 + 2 * C * c + C + (m % C)) * kD
-                     : wsUY + (tile_id * 128 + 64 + m) * kD;
-    const float gm = f.gpre[m];
+    const int t = tid & 63;
+    const uint32_t src = tmem + lane_base + (top ? 0 : 128);
+    bf16* gdst = top ? wsA1 + (tile_id * 128 + 2 * C * (t / C) + C + (t % C)) * kD
+                     : wsUY + (tile_id * 128 + 64 + t) * kD;
+    const float gt = exp2f(lam[t]);
 #pragma unroll
     for (int col = 0; col < 128; col += 16) {
       float v[16];
-      tmem_ld16(tD3 + lane_base + col, v);
+      tmem_ld16(src + col, v);
       tmem_wait_ld();
-      if (top) {  // Qh = G q - D3
-        const int half = col >> 6, cc = col & 63;
+      if (top) {  // Qh = G q - G M P  (step 7, state-free part)
+        const uint32_t qa = sbase + kOffKQ + (col >> 6) * 16384 + 8192;
         float q[16];
-        unpack8(ld_shared_v4(sbase + kOffKQ + half * 16384 + 8192 + sw128(m, cc)), q);
-        unpack8(ld_shared_v4(sbase + kOffKQ + half * 16384 + 8192 + sw128(m, cc + 8)), q + 8);
+        unpack8(ld_shared_v4(qa + sw128(t, col & 63)), q);
+        unpack8(ld_shared_v4(qa + sw128(t, (col & 63) + 8)), q + 8);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = gm * q[j] - v[j];
+        for (int j = 0; j < 16; ++j) v[j] = gt * q[j] - v[j];
       }
       *reinterpret_cast<uint4*>(gdst + col) = pack8(v);
       *reinterpret_cast<uint4*>(gdst + col + 8) = pack8(v + 8);
     }
   }
-  if (ok && tid < 64 / C) wsGC[tile_id * 4 + tid] = f.gpre[tid * C + C - 1];
+  if (ok && tid < 64 / C) wsGC[tile_id * 4 + tid] = gc[tid];
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 512);
+  if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
 // ============================================================================
@@ -456,7 +460,8 @@ struct ScanSmem {
   static constexpr uint32_t kA1 = 32 * 1024;
   static constexpr uint32_t kK = 16 * 1024;
   static constexpr uint32_t kUY = 2 * 64 * 2 * R;
-  static constexpr uint32_t kStage = ((kA1 + kK + kUY) + 1023) & ~1023u;
+  static constexpr uint32_t kGC = 16;           // G_C of the tile's chunks (fp32 x 4)
+  static constexpr uint32_t kStage = ((kA1 + kK + kUY + kGC) + 1023) & ~1023u;
   static constexpr uint32_t kS = 128 * 2 * R;  // S operand: 128 K-rows x R
   static constexpr uint32_t kW = 64 * 2 * R;   // W operand: up to 64 K-rows x R
   static constexpr uint32_t kOffS = kStages * kStage;
@@ -516,7 +521,9 @@ scan_tc_kernel(const __grid_constant__ CUtensorMap tm_a1, const __grid_constant_
         if (n >= kStages && !mbar_wait(empty_bar(s), ((n / kStages) - 1) & 1)) break;
         const uint32_t st = sbase + s * SM::kStage;
         const int row = (int)(((size_t)bh * NT + n) * 128);
-        mbar_expect_tx(full_bar(s), SM::kA1 + SM::kK + SM::kUY);
+        mbar_expect_tx(full_bar(s), SM::kA1 + SM::kK + SM::kUY + SM::kGC);
+        bulk_load(st + SM::kA1 + SM::kK + SM::kUY, wsGC + ((size_t)bh * NT + n) * 4, SM::kGC,
+                  full_bar(s));
         tma_load_2d(st, &tm_a1, full_bar(s), 0, row);
         tma_load_2d(st + 16384, &tm_a1, full_bar(s), 64, row);
         tma_load_4d(st + SM::kA1, &tm_k, full_bar(s), 0, hk, n * kTile, b);
@@ -563,7 +570,14 @@ scan_tc_kernel(const __grid_constant__ CUtensorMap tm_a1, const __grid_constant_
     for (int c = 0; c < kTile / C; ++c) {
       const int tok0 = n * kTile + c * C;
       if (tok0 >= T) break;
-      const float Gc = wsGC[((size_t)bh * NT + n) * 4 + c];
+      const float Gc = ld_shared_f32(st + SM::kA1 + SM::kK + SM::kUY + 4 * c);
+      // This thread's addend row (Ut for W, Yloc for y), fetched before the MMA wait.
+      uint4 addend[R / 8];
+      if (L < 2 * C) {
+        const uint32_t arow = L < C ? stU + (c * C + L) * (2 * R) : stY + (c * C + L - C) * (2 * R);
+#pragma unroll
+        for (int ch = 0; ch < R / 8; ++ch) addend[ch] = ld_shared_v4(arow + ch * 16);
+      }
       if (issuer) {
         tc_fence_after();
 #pragma unroll
@@ -583,12 +597,11 @@ scan_tc_kernel(const __grid_constant__ CUtensorMap tm_a1, const __grid_constant_
       tmem_wait_ld();
       if (L < C) {
         // W = Ut - S Pt^T for this chunk's token L.
-        const uint32_t urow = stU + (c * C + L) * kRowBytes;
         float w[R];
 #pragma unroll
         for (int ch = 0; ch < R / 8; ++ch) {
           float u8[8];
-          unpack8(ld_shared_v4(urow + ch * 16), u8);
+          unpack8(addend[ch], u8);
 #pragma unroll
           for (int e = 0; e < 8; ++e) w[ch * 8 + e] = u8[e] - d[ch * 8 + e];
         }
@@ -596,12 +609,11 @@ scan_tc_kernel(const __grid_constant__ CUtensorMap tm_a1, const __grid_constant_
       } else if (L < 2 * C) {
         const int tl = L - C;
         if (tok0 + tl < T) {
-          const uint32_t yrow = stY + (c * C + tl) * kRowBytes;
           bf16* yp = y + (((size_t)b * T + tok0 + tl) * Hv + hv) * kD + r0;
 #pragma unroll
           for (int ch = 0; ch < R / 8; ++ch) {
             float y8[8];
-            unpack8(ld_shared_v4(yrow + ch * 16), y8);
+            unpack8(addend[ch], y8);
 #pragma unroll
             for (int e = 0; e < 8; ++e) y8[e] = (y8[e] + d[ch * 8 + e]) * scale;
             *reinterpret_cast<uint4*>(yp + ch * 8) = pack8(y8);
