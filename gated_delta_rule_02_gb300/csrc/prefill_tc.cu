@@ -116,69 +116,101 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
 // ============================================================================
 constexpr int kPrepThreads = 256;
 // Shared-memory map (bytes from the 1024-aligned base); two CTAs fit per SM.
-constexpr uint32_t kOffKQ = 0;              // [K;Q]: 2 halves x (64 K rows + 64 Q rows) x 128 B
-constexpr uint32_t kOffV = 32 * 1024;       // V: 2 halves x 64 rows x 128 B
-constexpr uint32_t kOffA = 48 * 1024;       // A2 then A3: 128 rows x 64 K-cols (one 128B half)
-constexpr uint32_t kOffB = 64 * 1024;       // X, T_L (fp32) during the inverse; then P, U (MN-major)
-constexpr uint32_t kOffQK = 96 * 1024;      // QK^T, bf16 [64][64]
-constexpr uint32_t kOffSmall = 104 * 1024;  // lraw, lam, bta, gsuf [64]; gc[4]; Z[3*256]
-constexpr uint32_t kPrepSmem = kOffSmall + (64 * 4 + 4 + 3 * 256) * 4 + 1024;
+constexpr uint32_t kOffKQ = 0;        // [K;Q]: 2 halves x (64 K rows + 64 Q rows) x 128 B
+constexpr uint32_t kOffV = 32768;     // V: 2 halves x 64 rows x 128 B
+constexpr uint32_t kOffA = 49152;     // A2 then A3 (128 rows x 64 K-cols, one 128B half);
+                                      // before A2: the inverse's Z scratch
+constexpr uint32_t kOffB = 65536;     // X, T_L (fp32, row stride 68) during the inverse;
+                                      // then P, U (bf16, MN-major, 16 KB each)
+constexpr int kLdX = 68;
+constexpr uint32_t kOffQK = kOffB + 2 * 64 * kLdX * 4;  // QK^T bf16 [64][64]
+constexpr uint32_t kOffSmall = kOffQK + 64 * 64 * 2;    // per-token scalars
+constexpr uint32_t kPrepSmem = kOffSmall + (64 * 5 + 256 + 4) * 4 + 1024;
 
-// fp32 64 x 64 matrix with the column index XORed by the row's low 5 bits:
-// a warp touching one column of 32 consecutive rows hits 32 banks.
-__device__ __forceinline__ int fsw(int r, int c) { return r * 64 + (c ^ (r & 31)); }
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // T = (I + X)^-1 for X strictly lower triangular and block diagonal by chunk
-// (zero across chunks), by blocked forward substitution on 16 x 16 blocks
-// with all 256 threads:
-//   diagonal blocks  T_ii = (I + X_ii)^-1            (one column per thread)
+// (zero across chunks): blocked forward substitution on 16 x 16 blocks, all
+// 256 threads.
+//   diagonal blocks  T_ii = (I + X_ii)^-1                 (one column per thread)
 //   block row i > 0  Z_ij = sum_{k=j}^{i-1} X_ik T_kj,  T_ij = -T_ii Z_ij
-// Blocks of different chunks are zero and are written as such.
+// In the block rows each thread owns one (r, c) position of every block of
+// the row, so the X value it loads serves all of them.
 template <int C>
-__device__ void invert_unit_lower(const float* X, float* Tm, float* Z, int u) {
+__device__ void invert_unit_lower(const float* X, float* Tm, float* Zs, int u) {
   for (int idx = u; idx < 64 * 64; idx += kPrepThreads) {
     const int r = idx >> 6, c = idx & 63;
-    if ((c >> 4) > (r >> 4) || (c / C) != (r / C)) Tm[fsw(r, c)] = 0.f;
+    if ((c >> 4) > (r >> 4) || (c / C) != (r / C)) Tm[r * kLdX + c] = 0.f;
   }
   if (u < 64) {
-    const int bi = u >> 4, jj = u & 15, base = bi * 16;
+    const int base = (u >> 4) * 16, jj = u & 15;
     float x[16];
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
-      float acc = (r == jj) ? 1.f : 0.f;
+      float a0 = (r == jj) ? 1.f : 0.f, a1 = 0.f;
+      const float* xr = X + (base + r) * kLdX + base;
 #pragma unroll
-      for (int s = 0; s < r; ++s) acc = fmaf(-X[fsw(base + r, base + s)], x[s], acc);
-      x[r] = acc;
+      for (int s = 0; s + 1 < r; s += 2) {
+        a0 = fmaf(-xr[s], x[s], a0);
+        a1 = fmaf(-xr[s + 1], x[s + 1], a1);
+      }
+      if (r & 1) a0 = fmaf(-xr[r - 1], x[r - 1], a0);
+      x[r] = a0 + a1;
     }
 #pragma unroll
-    for (int r = 0; r < 16; ++r) Tm[fsw(base + r, base + jj)] = x[r];
+    for (int r = 0; r < 16; ++r) Tm[(base + r) * kLdX + base + jj] = x[r];
   }
   __syncthreads();
-  if constexpr (C != 16) {
-  for (int bi = 1; bi < 4; ++bi) {
-    const int bj0 = ((bi * 16) / C) * (C / 16);  // first block of bi's chunk
-    const int nb = bi - bj0;                      // blocks to fill in this row
-    if (nb <= 0) continue;
-    for (int idx = u; idx < nb * 256; idx += kPrepThreads) {
-      const int bj = bj0 + (idx >> 8), r = (idx >> 4) & 15, c = idx & 15;
-      float acc = 0.f;
-      for (int k = bj; k < bi; ++k)
+  if constexpr (C > 16) {
+    const int r = u >> 4, c = u & 15;
 #pragma unroll
-        for (int s = 0; s < 16; ++s)
-          acc = fmaf(X[fsw(bi * 16 + r, k * 16 + s)], Tm[fsw(k * 16 + s, bj * 16 + c)], acc);
-      Z[idx] = acc;
-    }
-    __syncthreads();
-    for (int idx = u; idx < nb * 256; idx += kPrepThreads) {
-      const int bj = bj0 + (idx >> 8), r = (idx >> 4) & 15, c = idx & 15;
-      float acc = 0.f;
+    for (int bi = 1; bi < 4; ++bi) {
+      const int bj0 = ((bi * 16) / C) * (C / 16);  // first block of bi's chunk
+      const int nb = bi - bj0;
+      if (nb > 0) {
+        float acc[3] = {0.f, 0.f, 0.f};
+        const float* xr = X + (bi * 16 + r) * kLdX;
 #pragma unroll
-      for (int s = 0; s < 16; ++s)
-        acc = fmaf(Tm[fsw(bi * 16 + r, bi * 16 + s)], Z[(idx & ~255) + s * 16 + c], acc);
-      Tm[fsw(bi * 16 + r, bj * 16 + c)] = -acc;
+        for (int k = bj0; k < bi; ++k) {
+#pragma unroll
+          for (int s = 0; s < 16; ++s) {
+            const float xv = xr[k * 16 + s];
+            const float* tr = Tm + (k * 16 + s) * kLdX + c;
+#pragma unroll
+            for (int q = 0; q < 3; ++q)
+              if (q <= k - bj0) acc[q] = fmaf(xv, tr[(bj0 + q) * 16], acc[q]);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 3; ++q)
+          if (q < nb) Zs[q * 256 + r * 16 + c] = acc[q];
+      }
+      __syncthreads();
+      if (nb > 0) {
+        float acc[3] = {0.f, 0.f, 0.f};
+        const float* tr = Tm + (bi * 16 + r) * kLdX + bi * 16;
+#pragma unroll
+        for (int s = 0; s < 16; ++s) {
+          const float tv = tr[s];
+#pragma unroll
+          for (int q = 0; q < 3; ++q)
+            if (q < nb) acc[q] = fmaf(tv, Zs[q * 256 + s * 16 + c], acc[q]);
+        }
+#pragma unroll
+        for (int q = 0; q < 3; ++q)
+          if (q < nb) Tm[(bi * 16 + r) * kLdX + (bj0 + q) * 16 + c] = -acc[q];
+      }
+      __syncthreads();
     }
-    __syncthreads();
-  }
   }
 }
 
@@ -193,17 +225,20 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                                            ~(uintptr_t)1023);
   __shared__ uint64_t bars[2];
   __shared__ uint32_t tmem_base_sh;
+  __shared__ float carry_sh;
   const uint32_t sbase = smem_u32(sm);
   const uint32_t bar_tma = smem_u32(&bars[0]), bar_mma = smem_u32(&bars[1]);
-  float* X = reinterpret_cast<float*>(sm + kOffB);          // 64 x 64 fp32
-  float* TL = reinterpret_cast<float*>(sm + kOffB + 16384);  // 64 x 64 fp32
-  bf16* sQK = reinterpret_cast<bf16*>(sm + kOffQK);          // 64 x 64 bf16
-  float* lraw = reinterpret_cast<float*>(sm + kOffSmall);    // log2 g per token
-  float* lam = lraw + 64;                                     // chunk-local prefix of lraw
+  float* X = reinterpret_cast<float*>(sm + kOffB);               // 64 x 68 fp32
+  float* TL = X + 64 * kLdX;                                     // 64 x 68 fp32
+  float* Zs = reinterpret_cast<float*>(sm + kOffA);              // 3 x 16 x 16 fp32
+  bf16* sQK = reinterpret_cast<bf16*>(sm + kOffQK);               // 64 x 64 bf16
+  float* lam = reinterpret_cast<float*>(sm + kOffSmall);         // chunk-local sum of log2 g
   float* bta = lam + 64;
-  float* gsuf = bta + 64;                                     // g_{t+1} .. g_{chunk end}
-  float* gc = gsuf + 64;                                      // G at each chunk's end
-  float* Z = gc + 4;
+  float* gsuf = bta + 64;   // g_{t+1} ... g_{chunk end}
+  float* gpw = gsuf + 64;   // G_t = g_{chunk start} ... g_t
+  float* sfac = gpw + 64;   // 2^(lam[end of t's 16-block] - lam_t)
+  float* rfac = sfac + 64;  // [64][4]: 2^(lam_t - lam[end of block b]), b before t's block
+  float* gc = rfac + 256;   // G at each chunk's end
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int tile = blockIdx.x, bh = blockIdx.y;
@@ -238,29 +273,42 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     tma_load_4d(sbase + kOffV + 8192, &tm_v, bar_tma, 64, hv, t0, b);
   }
 
-  // Gates (step 2).  Padded tokens take g = 1, beta = 0.  The decay products
-  // are carried as chunk-local prefix sums of log2 g, so that
-  // G_t = 2^lam_t and Gam[t][j] = 2^(lam_t - lam_j), j <= t: no division, and
-  // a vanishing product underflows to 0.
+  // Gates (step 2).  Padded tokens take g = 1, beta = 0.  Decay products are
+  // carried as chunk-local prefix sums lam of log2 g: G_t = 2^lam_t and
+  // Gam[t][j] = 2^(lam_t - lam_j) (j <= t) -- never a quotient, so a vanishing
+  // product underflows to 0.  Gam is used factored per 16-token block b:
+  // Across 16-token blocks, Gam[t][j] = rfac[t][b(j)] * sfac[j] with the
+  // block end as the split point, so both factors are products of decays (<= 1);
+  // inside a block it is 2^(lam_t - lam_j) directly.
   if (tid < 64) {
-    const int tok = t0 + tid;
+    const int t = tid, lane = tid & 31;
+    const int tok = t0 + t;
     const bool valid = tok < T;
     const size_t gi = ((size_t)b * T + tok) * Hv + hv;
-    bta[tid] = valid ? __bfloat162float(beta[gi]) : 0.f;
-    lraw[tid] = valid ? fmaxf(__log2f(__bfloat162float(g[gi])), -1000.f) : 0.f;
-  }
-  __syncthreads();
-  if (tid < 64) {
-    const int t = tid, cs = (t / C) * C, ce = cs + C - 1;
-    float pre = 0.f, all = 0.f;
-    for (int i = cs; i <= ce; ++i) {
-      const float l = lraw[i];
-      all += l;
-      if (i <= t) pre += l;
+    bta[t] = valid ? __bfloat162float(beta[gi]) : 0.f;
+    float l = valid ? fmaxf(lg2(__bfloat162float(g[gi])), -1000.f) : 0.f;
+    constexpr int kSeg = C < 32 ? C : 32;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, l, off);
+      if ((lane % kSeg) >= off) l += y;
     }
-    lam[t] = pre;
-    gsuf[t] = exp2f(all - pre);
-    if (t == ce) gc[t / C] = exp2f(all);
+    if constexpr (C == 64) {
+      if (tid == 31) carry_sh = l;
+      named_bar_sync(1, 64);
+      if (tid >= 32) l += carry_sh;
+    }
+    lam[t] = l;
+    named_bar_sync(1, 64);
+    const int ce = (t / C) * C + C - 1, cs = (t / C) * C;
+    const float lend = lam[ce];
+    gsuf[t] = ex2(lend - l);
+    gpw[t] = ex2(l);
+    sfac[t] = ex2(lam[(t | 15)] - l);
+#pragma unroll
+    for (int bb = 0; bb < 4; ++bb)
+      rfac[t * 4 + bb] = (bb * 16 >= cs && bb < (t >> 4)) ? ex2(l - lam[bb * 16 + 15]) : 0.f;
+    if (t == ce) gc[t / C] = ex2(lend);
   }
 
   bool ok = mbar_wait(bar_tma, 0);
@@ -276,6 +324,7 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     }
     mma_commit(bar_mma);
   }
+  ok = __syncthreads_and(ok);  // also publishes the gate scalars
   ok = ok && mbar_wait(bar_mma, 0);
   tc_fence_after();
   if (ok && tid < 128) {
@@ -291,9 +340,14 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       tmem_wait_ld();
       if (tid < 64) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
+        for (int e = 0; e < 16; e += 4) {
+          float4 o;
           const int j = c0 + e;
-          X[fsw(t, j)] = (j < t && j >= cs) ? bta[j] * v[e] : 0.f;
+          o.x = (j + 0 < t && j + 0 >= cs) ? bta[j + 0] * v[e + 0] : 0.f;
+          o.y = (j + 1 < t && j + 1 >= cs) ? bta[j + 1] * v[e + 1] : 0.f;
+          o.z = (j + 2 < t && j + 2 >= cs) ? bta[j + 2] * v[e + 2] : 0.f;
+          o.w = (j + 3 < t && j + 3 >= cs) ? bta[j + 3] * v[e + 3] : 0.f;
+          *reinterpret_cast<float4*>(X + t * kLdX + j) = o;
         }
       } else {
         *reinterpret_cast<uint4*>(sQK + t * 64 + c0) = pack8(v);
@@ -305,21 +359,29 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 
   // Step 4: T_L = (I + L)^-1.  Step 5 needs no second inverse:
   // (I + A)^-1 diag(beta) = diag(beta) (Gam . T_L) for A[t][j] = beta_t Gam[t][j] KK^T[t][j].
-  if (ok) invert_unit_lower<C>(X, TL, Z, tid);
+  if (ok) invert_unit_lower<C>(X, TL, Zs, tid);
   else __syncthreads();
 
   // A2 = [T_L; diag(beta) (Gam . T_L)]: 128 rows x 64 K-cols, K-major 128B swizzle.
   if (ok) {
     for (int idx = tid; idx < 128 * 8; idx += kPrepThreads) {
       const int row = idx >> 3, col0 = (idx & 7) * 8;
-      const int t = row & 63, cs = (t / C) * C;
-      float v[8];
+      const int t = row & 63;
+      const float4 a = *reinterpret_cast<const float4*>(TL + t * kLdX + col0);
+      const float4 c4 = *reinterpret_cast<const float4*>(TL + t * kLdX + col0 + 4);
+      float v[8] = {a.x, a.y, a.z, a.w, c4.x, c4.y, c4.z, c4.w};
+      if (row >= 64) {
+        // T_L is zero above the diagonal and across chunks (rfac is 0 there too).
+        const int bj = col0 >> 4;
+        if (bj < (t >> 4)) {
+          const float rb = bta[t] * rfac[t * 4 + bj];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int j = col0 + e;
-        const float tl = TL[fsw(t, j)];
-        v[e] = row < 64 ? tl
-                        : ((j <= t && j >= cs) ? bta[t] * exp2f(lam[t] - lam[j]) * tl : 0.f);
+          for (int e = 0; e < 8; ++e) v[e] *= rb * sfac[col0 + e];
+        } else {
+          const float bt = bta[t], lt = lam[t];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] = (col0 + e <= t) ? v[e] * bt * ex2(lt - lam[col0 + e]) : 0.f;
+        }
       }
       st_shared_v4(sbase + kOffA + sw128(row, col0), pack8(v));
     }
@@ -380,13 +442,24 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       const int t = row & 63, cs = (t / C) * C;
       float q[8], v[8];
       unpack8(*reinterpret_cast<const uint4*>(sQK + t * 64 + col0), q);
+      if (row < 64) {
+        const float gt = gpw[t];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int j = col0 + e;
-        const bool causal = j <= t && j >= cs;
-        v[e] = !causal ? 0.f
-                       : (row < 64 ? exp2f(lam[t]) * bta[j] * q[e]
-                                   : exp2f(lam[t] - lam[j]) * q[e]);
+        for (int e = 0; e < 8; ++e) {
+          const int j = col0 + e;
+          v[e] = (j <= t && j >= cs) ? gt * bta[j] * q[e] : 0.f;
+        }
+      } else if ((col0 >> 4) < (t >> 4)) {
+        const float rb = rfac[t * 4 + (col0 >> 4)];  // 0 for blocks of an earlier chunk
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = rb * sfac[col0 + e] * q[e];
+      } else {
+        const float lt = lam[t];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int j = col0 + e;
+          v[e] = (j <= t) ? ex2(lt - lam[j]) * q[e] : 0.f;
+        }
       }
       st_shared_v4(sbase + kOffA + sw128(row, col0), pack8(v));
     }
@@ -424,7 +497,7 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const uint32_t src = tmem + lane_base + (top ? 0 : 128);
     bf16* gdst = top ? wsA1 + (tile_id * 128 + 2 * C * (t / C) + C + (t % C)) * kD
                      : wsUY + (tile_id * 128 + 64 + t) * kD;
-    const float gt = exp2f(lam[t]);
+    const float gt = gpw[t];
 #pragma unroll
     for (int col = 0; col < 128; col += 16) {
       float v[16];
