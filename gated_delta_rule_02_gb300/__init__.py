@@ -33,6 +33,8 @@ GDN_ERR_ALIGNMENT = -3
 GDN_ERR_WORKSPACE = -4
 GDN_ERR_CUDA = -5
 GDN_ERR_DEVICE_TIMEOUT = -6
+GDN_ERR_NOALLOC_LIMIT = -7
+GDN_NOALLOC_SCRATCH_BYTES = 32 << 20
 GDN_DTYPE_F32 = 0
 GDN_DTYPE_BF16 = 1
 
@@ -68,6 +70,8 @@ def lib() -> ctypes.CDLL:
             L.gdn_status_string.restype = ctypes.c_char_p
             L.gdn_device_status.argtypes = [i]
             L.gdn_device_status.restype = i
+            L.gdn_prefill_noalloc.argtypes = [vp] * 8 + [i] * 8 + [vp]
+            L.gdn_prefill_noalloc.restype = i
             _lib = L
     return _lib
 
@@ -131,6 +135,25 @@ def gdn_prefill(q, k, v, g, beta, state_in, state_out, y, chunk, workspace=None,
                            _ptr(workspace), ws_bytes, _stream_handle(stream, dev))
     if st != GDN_OK:
         raise GdnError(st, "gdn_prefill")
+
+
+def gdn_prefill_noalloc(q, k, v, g, beta, state_in, state_out, y, chunk, stream=None):
+    """Enqueue ``gdn_prefill_noalloc`` (include/gdn.h): the prefill without a
+    caller workspace, using the library's fixed scratch buffer instead."""
+    dt = q.dtype
+    if dt not in _DTYPES:
+        raise ValueError(f"unsupported dtype {dt}")
+    dev = q.device
+    _check([("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("y", y)], dt, dev)
+    _check([("state_in", state_in), ("state_out", state_out)], torch.float32, dev)
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    st = lib().gdn_prefill_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                   _ptr(state_in), _ptr(state_out), _ptr(y),
+                                   B, T, Hk, Hv, Dk, Dv, int(chunk), _DTYPES[dt],
+                                   _stream_handle(stream, dev))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_prefill_noalloc")
 
 
 def gdn_decode_step(q, k, v, g, beta, state_in, state_out, y, stream=None):

@@ -89,6 +89,8 @@ const char* gdn_status_string(int status) {
     case GDN_ERR_WORKSPACE: return "workspace missing or smaller than gdn_prefill_workspace_bytes()";
     case GDN_ERR_CUDA: return "CUDA launch error";
     case GDN_ERR_DEVICE_TIMEOUT: return "a device-side wait gave up (bounded wait timed out)";
+    case GDN_ERR_NOALLOC_LIMIT:
+      return "problem needs more scratch than gdn_prefill_noalloc's fixed buffer (GDN_NOALLOC_SCRATCH_BYTES)";
     default: return "unknown status";
   }
 }

@@ -57,6 +57,8 @@ extern "C" {
 #define GDN_ERR_CUDA          (-5) /* the CUDA runtime reported an error at launch; the
                                       outputs are then unspecified */
 #define GDN_ERR_DEVICE_TIMEOUT (-6) /* a kernel's bounded wait gave up (see gdn_device_status) */
+#define GDN_ERR_NOALLOC_LIMIT (-7) /* gdn_prefill_noalloc: the problem needs more scratch than
+                                      GDN_NOALLOC_SCRATCH_BYTES */
 
 /* Element types of q, k, v, g, beta and y. */
 #define GDN_DTYPE_F32   0
@@ -106,6 +108,38 @@ GDN_API int gdn_decode_step(const void *q, const void *k, const void *v, const v
                     const void *beta, const float *state_in, float *state_out,
                     void *y, int B, int Hk, int Hv, int Dk, int Dv, int dtype,
                     void *stream);
+
+/*
+ * Prefill for callers that cannot allocate device memory.  This entry point
+ * has no counterpart in the source pages; it exists for the library's users.
+ *
+ * gdn_prefill needs a caller-allocated workspace.  Callers that cannot call
+ * cudaMalloc -- code running while a CUDA graph is captured, plug-ins handed
+ * raw device pointers without an allocator of their own, paths that cannot
+ * afford cudaMalloc's implicit synchronisation -- can call this instead.  It
+ * computes exactly what gdn_prefill computes (same arguments and meaning,
+ * minus the workspace) and allocates nothing: its scratch is a fixed array
+ * of GDN_NOALLOC_SCRATCH_BYTES built into the library, one per GPU that loads
+ * the library, held until the process exits.
+ *
+ *   Limit: the problem's gdn_prefill_workspace_bytes(...) must not exceed
+ *   GDN_NOALLOC_SCRATCH_BYTES (32 MiB: for bf16 inputs, B*Hv*ceil(T/64) up to
+ *   511 tiles, e.g. T = 4096 with B*Hv = 7, or T = 1024 with B*Hv = 31);
+ *   larger problems return GDN_ERR_NOALLOC_LIMIT with nothing enqueued.
+ *   Set-up: the first call on each device (with that device current) looks
+ *   up the array's device address once; make that first call before any
+ *   stream capture.
+ *   Sharing: every call on a device uses the same array, and the array keeps
+ *   the previous call's contents (nothing in it needs to start at zero).  Two
+ *   calls whose work overlaps on the GPU (different streams, no ordering
+ *   between them) race on it and give undefined results; order them.
+ * Returns GDN_OK or a GDN_ERR_* code, as gdn_prefill.
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES (32u << 20)
+GDN_API int gdn_prefill_noalloc(const void *q, const void *k, const void *v, const void *g,
+                                const void *beta, const float *state_in, float *state_out,
+                                void *y, int B, int T, int Hk, int Hv, int Dk, int Dv,
+                                int chunk, int dtype, void *stream);
 
 /*
  * Device-side health: every wait inside the tensor-core kernels (on an
