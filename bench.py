@@ -39,6 +39,29 @@ import torch  # noqa: E402
 import gdn_inputs  # noqa: E402
 
 FLUSH_BYTES = 256 << 20
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per call from one
+# ncu capture, summarised under profiles/.  Valid only for the kernel sources
+# it was taken on (sha256 prefix of those files); otherwise reported as null.
+_KDIR = os.path.join(ROOT, "gated_delta_rule_02_gb300", "csrc")
+MEASURED_TRAFFIC = {
+    "prefill": {"sources": ["prefill_tc.cu", "sm100_ptx.cuh"], "sha": "42ab9df1c488e0c3",
+                "bytes": 320.1e6},
+    "decode": {"sources": ["decode.cu"], "sha": "76396f3fe1bee68d", "bytes": 211.9e6},
+}
+
+
+def measured_traffic(key):
+    import hashlib
+    entry = MEASURED_TRAFFIC[key]
+    m = hashlib.sha256()
+    try:
+        for name in entry["sources"]:
+            with open(os.path.join(_KDIR, name), "rb") as f:
+                m.update(f.read())
+    except OSError:
+        return None
+    return entry["bytes"] if m.hexdigest()[:16] == entry["sha"] else None
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -157,11 +180,12 @@ def decode_alg_bytes(w):
             + w.B * w.Hv * w.Dv * 2 * eb + w.B * w.Hv * 2 * eb)
 
 
-def roofline(alg_bytes, seconds, hbm_gbs, kind):
+def roofline(alg_bytes, seconds, hbm_gbs, kind, traffic=None):
     achieved = alg_bytes / seconds / 1e9
     return {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_gbs,
-            "unit": "GB/s", "frac": round(achieved / hbm_gbs, 4), "traffic": None,
-            "peak_kind": kind}
+            "unit": "GB/s", "frac": round(achieved / hbm_gbs, 4),
+            "traffic": None if traffic is None else round(traffic),
+            "algorithmic_bytes": alg_bytes, "peak_kind": kind}
 
 
 def median_ms(pairs):
@@ -418,7 +442,8 @@ def main():
                    "Dk": w.Dk, "Dv": w.Dv, "chunk": w.chunk, "state": "fp32",
                    "l2": "256 MiB flush write between timed steps",
                    "parallelism": f"replicas x{world}"},
-        "roofline": roofline(prefill_alg_bytes(w), ms / 1e3, hbm, peak_kind),
+        "roofline": roofline(prefill_alg_bytes(w), ms / 1e3, hbm, peak_kind,
+                             measured_traffic("prefill") if w.name == "prefill_t4096" else None),
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
     }
@@ -434,7 +459,8 @@ def main():
             "workload": dw.name, "steps_per_s": round(1e6 / us, 1),
             "tokens_per_s": round(dw.B * 1e6 / us, 1), "us_per_step": round(us, 3),
             "timing": "256 steps in one CUDA graph, state in place (134 MB > L2)",
-            "roofline": roofline(decode_alg_bytes(dw), us / 1e6, hbm, peak_kind)}
+            "roofline": roofline(decode_alg_bytes(dw), us / 1e6, hbm, peak_kind,
+                                 measured_traffic("decode"))}
         if rank == 0 and world == 1:
             line["cpu_baseline"] = cpu_baseline_prefill(w)
     if rank == 0:

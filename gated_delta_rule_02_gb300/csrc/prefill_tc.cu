@@ -118,13 +118,13 @@ constexpr int kPrepThreads = 256;
 // Shared-memory map (bytes from the 1024-aligned base); two CTAs fit per SM.
 constexpr uint32_t kOffKQ = 0;        // [K;Q]: 2 halves x (64 K rows + 64 Q rows) x 128 B
 constexpr uint32_t kOffV = 32768;     // V: 2 halves x 64 rows x 128 B
-constexpr uint32_t kOffA = 49152;     // A2 then A3 (128 rows x 64 K-cols, one 128B half);
-                                      // before A2: the inverse's Z scratch
-constexpr uint32_t kOffB = 65536;     // X, T_L (fp32, row stride 68) during the inverse;
+constexpr uint32_t kOffA3 = 49152;    // A3 (128 rows x 64 K-cols, one 128B half)
+constexpr uint32_t kOffB = 65536;     // X | T_L | Z (fp32) during the inverse; then A2 over X;
                                       // then P, U (bf16, MN-major, 16 KB each)
 constexpr int kLdX = 68;
-constexpr uint32_t kOffQK = kOffB + 2 * 64 * kLdX * 4;  // QK^T bf16 [64][64]
-constexpr uint32_t kOffSmall = kOffQK + 64 * 64 * 2;    // per-token scalars
+constexpr uint32_t kOffTL = kOffB + 64 * kLdX * 4;
+constexpr uint32_t kOffZ = kOffTL + 64 * kLdX * 4;       // 32 x 32 fp32
+constexpr uint32_t kOffSmall = kOffZ + 32 * 32 * 4;      // per-token scalars
 constexpr uint32_t kPrepSmem = kOffSmall + (64 * 5 + 256 + 4) * 4 + 1024;
 
 __device__ __forceinline__ float ex2(float x) {
@@ -138,13 +138,55 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
+// Warp-level 16 x 8 x 8 tf32 MMA (fp32 accumulate): the inverse's block
+// products are too small for tcgen05 (M >= 64) and too latency-sensitive for
+// scalar FMAs.  Fragment layout (g = lane / 4, t = lane % 4):
+//   A 16 x 8 row-major: a0 (g, t) a1 (g+8, t) a2 (g, t+4) a3 (g+8, t+4)
+//   B  8 x 8:           b0 (t, g) b1 (t+4, g)
+//   D 16 x 8:           d0 (g, 2t) d1 (g, 2t+1) d2 (g+8, 2t) d3 (g+8, 2t+1)
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void mma_tf32(float* d, const uint32_t* a, const uint32_t* bb) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(bb[0]), "r"(bb[1]));
+}
+// D(16 x 8) = A[ra.., ca..](16 x K) * B[rb.., cb..](K x 8), fp32 row-major
+// operands with row strides lda, ldb; K a multiple of 8.
+template <int K>
+__device__ __forceinline__ void warp_gemm_16x8(float* d, const float* A, int lda, const float* Bm,
+                                               int ldb, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  d[0] = d[1] = d[2] = d[3] = 0.f;
+#pragma unroll
+  for (int k0 = 0; k0 < K; k0 += 8) {
+    const uint32_t a[4] = {to_tf32(A[g * lda + k0 + t]), to_tf32(A[(g + 8) * lda + k0 + t]),
+                           to_tf32(A[g * lda + k0 + t + 4]),
+                           to_tf32(A[(g + 8) * lda + k0 + t + 4])};
+    const uint32_t bb[2] = {to_tf32(Bm[(k0 + t) * ldb + g]), to_tf32(Bm[(k0 + t + 4) * ldb + g])};
+    mma_tf32(d, a, bb);
+  }
+}
+__device__ __forceinline__ void warp_store_16x8(float* D, int ldd, const float* d, int lane,
+                                                float sign) {
+  const int g = lane >> 2, t = lane & 3;
+  D[g * ldd + 2 * t] = sign * d[0];
+  D[g * ldd + 2 * t + 1] = sign * d[1];
+  D[(g + 8) * ldd + 2 * t] = sign * d[2];
+  D[(g + 8) * ldd + 2 * t + 1] = sign * d[3];
+}
+
 // T = (I + X)^-1 for X strictly lower triangular and block diagonal by chunk
-// (zero across chunks): blocked forward substitution on 16 x 16 blocks, all
-// 256 threads.
-//   diagonal blocks  T_ii = (I + X_ii)^-1                 (one column per thread)
-//   block row i > 0  Z_ij = sum_{k=j}^{i-1} X_ik T_kj,  T_ij = -T_ii Z_ij
-// In the block rows each thread owns one (r, c) position of every block of
-// the row, so the X value it loads serves all of them.
+// (zero across chunks), by blocked forward substitution:
+//   16 x 16 diagonal blocks   T_ii = (I + X_ii)^-1       (one column per thread)
+//   32 x 32 blocks (C >= 32)  T_10 = -T_11 X_10 T_00      (per 16-block pair)
+//   64 x 64 (C = 64)          T_BA = -T_BB X_BA T_AA      (32-block halves)
+// The block products run on warp-level tf32 MMAs; all 256 threads call this.
 template <int C>
 __device__ void invert_unit_lower(const float* X, float* Tm, float* Zs, int u) {
   for (int idx = u; idx < 64 * 64; idx += kPrepThreads) {
@@ -170,47 +212,34 @@ __device__ void invert_unit_lower(const float* X, float* Tm, float* Zs, int u) {
     for (int r = 0; r < 16; ++r) Tm[(base + r) * kLdX + base + jj] = x[r];
   }
   __syncthreads();
-  if constexpr (C > 16) {
-    const int r = u >> 4, c = u & 15;
-#pragma unroll
-    for (int bi = 1; bi < 4; ++bi) {
-      const int bj0 = ((bi * 16) / C) * (C / 16);  // first block of bi's chunk
-      const int nb = bi - bj0;
-      if (nb > 0) {
-        float acc[3] = {0.f, 0.f, 0.f};
-        const float* xr = X + (bi * 16 + r) * kLdX;
-#pragma unroll
-        for (int k = bj0; k < bi; ++k) {
-#pragma unroll
-          for (int s = 0; s < 16; ++s) {
-            const float xv = xr[k * 16 + s];
-            const float* tr = Tm + (k * 16 + s) * kLdX + c;
-#pragma unroll
-            for (int q = 0; q < 3; ++q)
-              if (q <= k - bj0) acc[q] = fmaf(xv, tr[(bj0 + q) * 16], acc[q]);
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < 3; ++q)
-          if (q < nb) Zs[q * 256 + r * 16 + c] = acc[q];
-      }
-      __syncthreads();
-      if (nb > 0) {
-        float acc[3] = {0.f, 0.f, 0.f};
-        const float* tr = Tm + (bi * 16 + r) * kLdX + bi * 16;
-#pragma unroll
-        for (int s = 0; s < 16; ++s) {
-          const float tv = tr[s];
-#pragma unroll
-          for (int q = 0; q < 3; ++q)
-            if (q < nb) acc[q] = fmaf(tv, Zs[q * 256 + s * 16 + c], acc[q]);
-        }
-#pragma unroll
-        for (int q = 0; q < 3; ++q)
-          if (q < nb) Tm[(bi * 16 + r) * kLdX + (bj0 + q) * 16 + c] = -acc[q];
-      }
-      __syncthreads();
+  const int w = u >> 5, lane = u & 31;
+  if constexpr (C >= 32) {
+    // Pairs (0,1) and (2,3): warp w < 4 handles pair w/2, columns 8*(w%2)..
+    float d[4];
+    const int p = (w >> 1) & 1, nt = w & 1;
+    const int r0 = (2 * p + 1) * 16, c0 = 2 * p * 16;
+    if (w < 4) {
+      warp_gemm_16x8<16>(d, X + r0 * kLdX + c0, kLdX, Tm + c0 * kLdX + c0 + nt * 8, kLdX, lane);
+      warp_store_16x8(Zs + p * 256 + nt * 8, 16, d, lane, 1.f);
     }
+    __syncthreads();
+    if (w < 4) {
+      warp_gemm_16x8<16>(d, Tm + r0 * kLdX + r0, kLdX, Zs + p * 256 + nt * 8, 16, lane);
+      warp_store_16x8(Tm + r0 * kLdX + c0 + nt * 8, kLdX, d, lane, -1.f);
+    }
+    __syncthreads();
+  }
+  if constexpr (C == 64) {
+    // M = X[32:64][0:32] T[0:32][0:32], then T[32:64][0:32] = -T[32:64][32:64] M;
+    // warp w computes the 16 x 8 tile (w/4, w%4) of each.
+    float d[4];
+    const int mt = w >> 2, nt = w & 3;
+    warp_gemm_16x8<32>(d, X + (32 + mt * 16) * kLdX, kLdX, Tm + nt * 8, kLdX, lane);
+    warp_store_16x8(Zs + mt * 16 * 32 + nt * 8, 32, d, lane, 1.f);
+    __syncthreads();
+    warp_gemm_16x8<32>(d, Tm + (32 + mt * 16) * kLdX + 32, kLdX, Zs + nt * 8, 32, lane);
+    warp_store_16x8(Tm + (32 + mt * 16) * kLdX + nt * 8, kLdX, d, lane, -1.f);
+    __syncthreads();
   }
 }
 
@@ -229,9 +258,8 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   const uint32_t sbase = smem_u32(sm);
   const uint32_t bar_tma = smem_u32(&bars[0]), bar_mma = smem_u32(&bars[1]);
   float* X = reinterpret_cast<float*>(sm + kOffB);               // 64 x 68 fp32
-  float* TL = X + 64 * kLdX;                                     // 64 x 68 fp32
-  float* Zs = reinterpret_cast<float*>(sm + kOffA);              // 3 x 16 x 16 fp32
-  bf16* sQK = reinterpret_cast<bf16*>(sm + kOffQK);               // 64 x 64 bf16
+  float* TL = reinterpret_cast<float*>(sm + kOffTL);             // 64 x 68 fp32
+  float* Zs = reinterpret_cast<float*>(sm + kOffZ);              // 32 x 32 fp32
   float* lam = reinterpret_cast<float*>(sm + kOffSmall);         // chunk-local sum of log2 g
   float* bta = lam + 64;
   float* gsuf = bta + 64;   // g_{t+1} ... g_{chunk end}
@@ -328,11 +356,14 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   ok = ok && mbar_wait(bar_mma, 0);
   tc_fence_after();
   if (ok && tid < 128) {
-    // Row t of KK^T -> row t of X = L (step 4): X[t][j] = beta_j KK^T[t][j],
-    // j < t in t's chunk.  Row t of QK^T -> bf16 for the A3 operand.
+    // Row t of KK^T (lanes 0..63) -> row t of X = L (step 4):
+    //   X[t][j] = beta_j KK^T[t][j], j < t in t's chunk.
+    // Row t of QK^T (lanes 64..127) -> rows t and 64+t of
+    //   A3 = [diag(G) M; Gam . QK^T], M[t][i] = beta_i QK^T[t][i], i <= t (steps 6, 7).
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const int t = tid & 63;
-    const int cs = (t / C) * C;
+    const int cs = (t / C) * C, bt = t >> 4;
+    const float gt = gpw[t], lt = lam[t];
 #pragma unroll
     for (int c0 = 0; c0 < 64; c0 += 16) {
       float v[16];
@@ -350,8 +381,22 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           *reinterpret_cast<float4*>(X + t * kLdX + j) = o;
         }
       } else {
-        *reinterpret_cast<uint4*>(sQK + t * 64 + c0) = pack8(v);
-        *reinterpret_cast<uint4*>(sQK + t * 64 + c0 + 8) = pack8(v + 8);
+        const int cb = c0 >> 4;
+        float top[16], bot[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int j = c0 + e;
+          const bool causal = j <= t && j >= cs;
+          top[e] = causal ? gt * bta[j] * v[e] : 0.f;
+          float gam;
+          if (cb < bt) gam = rfac[t * 4 + cb] * sfac[j];   // 0 for an earlier chunk
+          else gam = causal ? ex2(lt - lam[j]) : 0.f;
+          bot[e] = gam * v[e];
+        }
+        st_shared_v4(sbase + kOffA3 + sw128(t, c0), pack8(top));
+        st_shared_v4(sbase + kOffA3 + sw128(t, c0 + 8), pack8(top + 8));
+        st_shared_v4(sbase + kOffA3 + sw128(64 + t, c0), pack8(bot));
+        st_shared_v4(sbase + kOffA3 + sw128(64 + t, c0 + 8), pack8(bot + 8));
       }
     }
   }
@@ -383,7 +428,7 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           for (int e = 0; e < 8; ++e) v[e] = (col0 + e <= t) ? v[e] * bt * ex2(lt - lam[col0 + e]) : 0.f;
         }
       }
-      st_shared_v4(sbase + kOffA + sw128(row, col0), pack8(v));
+      st_shared_v4(sbase + kOffB + sw128(row, col0), pack8(v));
     }
     fence_proxy_async();
   }
@@ -396,13 +441,13 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const uint32_t id2 = idesc_bf16(128, 128, false, true);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
-      const uint64_t ad = smem_desc(sbase + kOffA + kk * 32, 16, 1024, kSw128);
+      const uint64_t ad = smem_desc(sbase + kOffB + kk * 32, 16, 1024, kSw128);
       mma_bf16_ss(tmem, ad, smem_desc(sbase + kOffKQ + kk * 2048, 16384, 1024, kSw128), id2,
                   kk > 0);
     }
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
-      const uint64_t ad = smem_desc(sbase + kOffA + kk * 32, 16, 1024, kSw128);
+      const uint64_t ad = smem_desc(sbase + kOffB + kk * 32, 16, 1024, kSw128);
       mma_bf16_ss(tmem + 128, ad, smem_desc(sbase + kOffV + kk * 2048, 8192, 1024, kSw128), id2,
                   kk > 0);
     }
@@ -435,34 +480,6 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       *reinterpret_cast<uint4*>(gdst + col) = pack8(v);
       *reinterpret_cast<uint4*>(gdst + col + 8) = pack8(v + 8);
     }
-  } else if (ok) {
-    // A3 = [diag(G) M; Gam . QK^T] (128 x 64), M[t][i] = beta_i QK^T[t][i], i <= t.
-    for (int idx = tid - 128; idx < 128 * 8; idx += 128) {
-      const int row = idx >> 3, col0 = (idx & 7) * 8;
-      const int t = row & 63, cs = (t / C) * C;
-      float q[8], v[8];
-      unpack8(*reinterpret_cast<const uint4*>(sQK + t * 64 + col0), q);
-      if (row < 64) {
-        const float gt = gpw[t];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int j = col0 + e;
-          v[e] = (j <= t && j >= cs) ? gt * bta[j] * q[e] : 0.f;
-        }
-      } else if ((col0 >> 4) < (t >> 4)) {
-        const float rb = rfac[t * 4 + (col0 >> 4)];  // 0 for blocks of an earlier chunk
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = rb * sfac[col0 + e] * q[e];
-      } else {
-        const float lt = lam[t];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int j = col0 + e;
-          v[e] = (j <= t) ? ex2(lt - lam[j]) * q[e] : 0.f;
-        }
-      }
-      st_shared_v4(sbase + kOffA + sw128(row, col0), pack8(v));
-    }
   }
   if (ok) fence_proxy_async();
   ok = __syncthreads_and(ok);
@@ -474,13 +491,13 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const uint32_t id3 = idesc_bf16(128, 128, false, true);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
-      const uint64_t ad = smem_desc(sbase + kOffA + kk * 32, 16, 1024, kSw128);
+      const uint64_t ad = smem_desc(sbase + kOffA3 + kk * 32, 16, 1024, kSw128);
       mma_bf16_ss(tmem, ad, smem_desc(sbase + kOffB + kk * 2048, 8192, 1024, kSw128), id3,
                   kk > 0);
     }
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
-      const uint64_t ad = smem_desc(sbase + kOffA + kk * 32, 16, 1024, kSw128);
+      const uint64_t ad = smem_desc(sbase + kOffA3 + kk * 32, 16, 1024, kSw128);
       mma_bf16_ss(tmem + 128, ad,
                   smem_desc(sbase + kOffB + 16384 + kk * 2048, 8192, 1024, kSw128), id3,
                   kk > 0);
