@@ -355,21 +355,24 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   ok = __syncthreads_and(ok);  // also publishes the gate scalars
   ok = ok && mbar_wait(bar_mma, 0);
   tc_fence_after();
-  if (ok && tid < 128) {
-    // Row t of KK^T (lanes 0..63) -> row t of X = L (step 4):
+  if (ok) {
+    // Row t of KK^T (TMEM lanes 0..63) -> row t of X = L (step 4):
     //   X[t][j] = beta_j KK^T[t][j], j < t in t's chunk.
     // Row t of QK^T (lanes 64..127) -> rows t and 64+t of
     //   A3 = [diag(G) M; Gam . QK^T], M[t][i] = beta_i QK^T[t][i], i <= t (steps 6, 7).
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const int t = tid & 63;
+    // Warps w and w+4 share TMEM lane quadrant w % 4 and take 32 columns each.
+    const int q4 = warp & 3, lrow = q4 * 32 + (tid & 31);
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    const int t = lrow & 63;
     const int cs = (t / C) * C, bt = t >> 4;
     const float gt = gpw[t], lt = lam[t];
+    const int cbeg = (warp >> 2) * 32;
 #pragma unroll
-    for (int c0 = 0; c0 < 64; c0 += 16) {
+    for (int c0 = cbeg; c0 < cbeg + 32; c0 += 16) {
       float v[16];
       tmem_ld16(tmem + lane_base + c0, v);
       tmem_wait_ld();
-      if (tid < 64) {
+      if (lrow < 64) {
 #pragma unroll
         for (int e = 0; e < 16; e += 4) {
           float4 o;
@@ -456,19 +459,22 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   ok = ok && mbar_wait(bar_mma, 1);
   tc_fence_after();
 
-  if (ok && tid < 128) {
+  if (ok) {
     // P rows (lanes 0..63) and U rows (lanes 64..127): bf16 into the G3 operand
     // and, scaled, into the workspace: Pt = G_C beta P (step 9), Ut = Gam[C-1][.] U.
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const bool top = tid < 64;
-    const int t = tid & 63;
+    // Warps w and w+4 share a lane quadrant and take 64 columns each.
+    const int q4 = warp & 3, lrow = q4 * 32 + (tid & 31);
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    const bool top = lrow < 64;
+    const int t = lrow & 63;
     const uint32_t src = tmem + lane_base + (top ? 0 : 128);
     const uint32_t bdst = sbase + kOffB + (top ? 0 : 16384);
     const float scale = top ? gc[t / C] * bta[t] : gsuf[t];
     bf16* gdst = top ? wsA1 + (tile_id * 128 + 2 * C * (t / C) + (t % C)) * kD
                      : wsUY + (tile_id * 128 + t) * kD;
+    const int cbeg = (warp >> 2) * 64;
 #pragma unroll
-    for (int col = 0; col < 128; col += 16) {
+    for (int col = cbeg; col < cbeg + 64; col += 16) {
       float v[16];
       tmem_ld16(src + col, v);
       tmem_wait_ld();
@@ -507,16 +513,18 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   ok = ok && mbar_wait(bar_mma, 0);
   tc_fence_after();
 
-  if (ok && tid < 128) {
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const bool top = tid < 64;
-    const int t = tid & 63;
+  if (ok) {
+    const int q4 = warp & 3, lrow = q4 * 32 + (tid & 31);
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    const bool top = lrow < 64;
+    const int t = lrow & 63;
     const uint32_t src = tmem + lane_base + (top ? 0 : 128);
     bf16* gdst = top ? wsA1 + (tile_id * 128 + 2 * C * (t / C) + C + (t % C)) * kD
                      : wsUY + (tile_id * 128 + 64 + t) * kD;
     const float gt = gpw[t];
+    const int cbeg = (warp >> 2) * 64;
 #pragma unroll
-    for (int col = 0; col < 128; col += 16) {
+    for (int col = cbeg; col < cbeg + 64; col += 16) {
       float v[16];
       tmem_ld16(src + col, v);
       tmem_wait_ld();
