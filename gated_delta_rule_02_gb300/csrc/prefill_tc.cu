@@ -246,9 +246,10 @@ __device__ void invert_unit_lower(const float* X, float* Tm, float* Zs, int u) {
 template <int C>
 __global__ void __launch_bounds__(kPrepThreads, 2)
 prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
-               const __grid_constant__ CUtensorMap tm_v, const bf16* __restrict__ g,
-               const bf16* __restrict__ beta, bf16* __restrict__ wsA1, bf16* __restrict__ wsUY,
-               float* __restrict__ wsGC, int T, int Hk, int Hv, int NT) {
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_a1s,
+               const __grid_constant__ CUtensorMap tm_uys, const bf16* __restrict__ g,
+               const bf16* __restrict__ beta, float* __restrict__ wsGC, int T, int Hk, int Hv,
+               int NT) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~(uintptr_t)1023);
@@ -470,8 +471,10 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const uint32_t src = tmem + lane_base + (top ? 0 : 128);
     const uint32_t bdst = sbase + kOffB + (top ? 0 : 16384);
     const float scale = top ? gc[t / C] * bta[t] : gsuf[t];
-    bf16* gdst = top ? wsA1 + (tile_id * 128 + 2 * C * (t / C) + (t % C)) * kD
-                     : wsUY + (tile_id * 128 + t) * kD;
+    // Staging for the workspace rows (K and V are dead after G2): 128B-swizzled
+    // 64-column halves, stored below with TMA.
+    const uint32_t stage = top ? sbase + kOffKQ : sbase + kOffV;
+    const uint32_t half_stride = top ? 16384 : 8192;
     const int cbeg = (warp >> 2) * 64;
 #pragma unroll
     for (int col = cbeg; col < cbeg + 64; col += 16) {
@@ -483,12 +486,25 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       st_shared_v4(atom + sw128(t, (col & 63) + 8), pack8(v + 8));
 #pragma unroll
       for (int j = 0; j < 16; ++j) v[j] *= scale;
-      *reinterpret_cast<uint4*>(gdst + col) = pack8(v);
-      *reinterpret_cast<uint4*>(gdst + col + 8) = pack8(v + 8);
+      const uint32_t hs = stage + (col >> 6) * half_stride;
+      st_shared_v4(hs + sw128(t, col & 63), pack8(v));
+      st_shared_v4(hs + sw128(t, (col & 63) + 8), pack8(v + 8));
     }
   }
   if (ok) fence_proxy_async();
   ok = __syncthreads_and(ok);
+  if (ok && tid == 0) {
+    const int row0 = (int)(tile_id * 128);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int c = 0; c < 64 / C; ++c)  // Pt rows of chunk c
+        tma_store_2d(&tm_a1s, sbase + kOffKQ + h * 16384 + c * C * 128, 64 * h,
+                     row0 + 2 * C * c);
+      tma_store_2d(&tm_uys, sbase + kOffV + h * 8192, 64 * h, row0);  // Ut rows
+    }
+    bulk_commit();
+  }
 
   // G3: D3a = A3 P (cols 0..127; rows 0..63 = G M P),
   //     D3b = A3 U (cols 128..255; rows 64..127 = y_loc).
@@ -519,8 +535,8 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const bool top = lrow < 64;
     const int t = lrow & 63;
     const uint32_t src = tmem + lane_base + (top ? 0 : 128);
-    bf16* gdst = top ? wsA1 + (tile_id * 128 + 2 * C * (t / C) + C + (t % C)) * kD
-                     : wsUY + (tile_id * 128 + 64 + t) * kD;
+    // Staging (A3 and B3 are dead after G3).
+    const uint32_t stage = top ? sbase + kOffA3 : sbase + kOffB;
     const float gt = gpw[t];
     const int cbeg = (warp >> 2) * 64;
 #pragma unroll
@@ -536,11 +552,27 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] = gt * q[j] - v[j];
       }
-      *reinterpret_cast<uint4*>(gdst + col) = pack8(v);
-      *reinterpret_cast<uint4*>(gdst + col + 8) = pack8(v + 8);
+      const uint32_t hs = stage + (col >> 6) * 8192;
+      st_shared_v4(hs + sw128(t, col & 63), pack8(v));
+      st_shared_v4(hs + sw128(t, (col & 63) + 8), pack8(v + 8));
     }
   }
   if (ok && tid < 64 / C) wsGC[tile_id * 4 + tid] = gc[tid];
+  if (ok) fence_proxy_async();
+  ok = __syncthreads_and(ok);
+  if (ok && tid == 0) {
+    const int row0 = (int)(tile_id * 128);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int c = 0; c < 64 / C; ++c)  // Qh rows of chunk c
+        tma_store_2d(&tm_a1s, sbase + kOffA3 + h * 8192 + c * C * 128, 64 * h,
+                     row0 + 2 * C * c + C);
+      tma_store_2d(&tm_uys, sbase + kOffB + h * 8192, 64 * h, row0 + 64);  // y_loc rows
+    }
+    bulk_commit();
+    bulk_wait_all();  // the staging stays valid and the rows land before the CTA exits
+  }
 
   tc_fence_before();
   __syncthreads();
@@ -819,11 +851,13 @@ cudaError_t launch_c(const PrefillArgs& a) {
   float* wsGC = reinterpret_cast<float*>(ws + w.gc);
 
   if (!encode_fn()) return cudaErrorNotSupported;
-  CUtensorMap tk, tq, tv, ta1, tuy;
+  CUtensorMap tk, tq, tv, ta1, tuy, ta1s, tuys;
   if (!make_bthd_map(&tk, a.k, a.B, a.T, a.Hk) || !make_bthd_map(&tq, a.q, a.B, a.T, a.Hk) ||
       !make_bthd_map(&tv, a.v, a.B, a.T, a.Hv) ||
       !make_rows_map(&ta1, wsA1, (size_t)BH * NT * 128, 64, 128, true) ||
-      !make_rows_map(&tuy, wsUY, (size_t)BH * NT * 128, kScanRows, 64, false))
+      !make_rows_map(&tuy, wsUY, (size_t)BH * NT * 128, kScanRows, 64, false) ||
+      !make_rows_map(&ta1s, wsA1, (size_t)BH * NT * 128, 64, C, true) ||
+      !make_rows_map(&tuys, wsUY, (size_t)BH * NT * 128, 64, 64, true))
     return cudaErrorInvalidValue;
 
   cudaError_t e = cudaFuncSetAttribute(prep_tc_kernel<C>,
@@ -835,7 +869,7 @@ cudaError_t launch_c(const PrefillArgs& a) {
   if (e != cudaSuccess) return e;
 
   prep_tc_kernel<C><<<dim3(NT, BH), kPrepThreads, kPrepSmem, a.stream>>>(
-      tk, tq, tv, static_cast<const bf16*>(a.g), static_cast<const bf16*>(a.beta), wsA1, wsUY,
+      tk, tq, tv, ta1s, tuys, static_cast<const bf16*>(a.g), static_cast<const bf16*>(a.beta),
       wsGC, a.T, a.Hk, a.Hv, NT);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
