@@ -83,6 +83,19 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
                "r"(v.z), "r"(v.w)
                : "memory");
 }
+// 16 consecutive floats from a 16-byte-aligned shared address.
+__device__ __forceinline__ void ld16f(const float* p, float* o) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 f = *reinterpret_cast<const float4*>(p + 4 * i);
+    o[4 * i] = f.x; o[4 * i + 1] = f.y; o[4 * i + 2] = f.z; o[4 * i + 3] = f.w;
+  }
+}
+// 16-byte store through a generic pointer into shared memory: unlike the asm
+// form it lets the compiler schedule the surrounding shared loads freely.
+__device__ __forceinline__ void st_sm16(uint8_t* base, uint32_t off, uint4 v) {
+  *reinterpret_cast<uint4*>(base + off) = v;
+}
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
@@ -125,7 +138,8 @@ constexpr int kLdX = 68;
 constexpr uint32_t kOffTL = kOffB + 64 * kLdX * 4;
 constexpr uint32_t kOffZ = kOffTL + 64 * kLdX * 4;       // 32 x 32 fp32
 constexpr uint32_t kOffSmall = kOffZ + 32 * 32 * 4;      // per-token scalars
-constexpr uint32_t kPrepSmem = kOffSmall + (64 * 5 + 256 + 4) * 4 + 1024;
+constexpr int kLdGd = 20;                                 // row stride of the in-block ratios
+constexpr uint32_t kPrepSmem = kOffSmall + (64 * 6 + 256 + 4 + 64 * kLdGd) * 4 + 1024;
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -268,6 +282,8 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   float* sfac = gpw + 64;   // 2^(lam[end of t's 16-block] - lam_t)
   float* rfac = sfac + 64;  // [64][4]: 2^(lam_t - lam[end of block b]), b before t's block
   float* gc = rfac + 256;   // G at each chunk's end
+  float* graw = gc + 4;     // g_t
+  float* gdiag = graw + 64; // [64][17]: Gam[t][j] for j in t's 16-block, j <= t (products)
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int tile = blockIdx.x, bh = blockIdx.y;
@@ -315,7 +331,9 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const bool valid = tok < T;
     const size_t gi = ((size_t)b * T + tok) * Hv + hv;
     bta[t] = valid ? __bfloat162float(beta[gi]) : 0.f;
-    float l = valid ? fmaxf(lg2(__bfloat162float(g[gi])), -1000.f) : 0.f;
+    const float gv = valid ? __bfloat162float(g[gi]) : 1.f;
+    graw[t] = gv;
+    float l = fmaxf(lg2(gv), -1000.f);
     constexpr int kSeg = C < 32 ? C : 32;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -329,6 +347,15 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     }
     lam[t] = l;
     named_bar_sync(1, 64);
+    {  // in-block ratios as products of decays (ferrox-core "The algebra")
+      float r = 1.f;
+      float* gd = gdiag + t * kLdGd;
+      gd[t & 15] = 1.f;
+      for (int j = t - 1; j >= (t & ~15); --j) {
+        r *= graw[j + 1];
+        gd[j & 15] = r;
+      }
+    }
     const int ce = (t / C) * C + C - 1, cs = (t / C) * C;
     const float lend = lam[ce];
     gsuf[t] = ex2(lend - l);
@@ -366,41 +393,46 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     const int t = lrow & 63;
     const int cs = (t / C) * C, bt = t >> 4;
-    const float gt = gpw[t], lt = lam[t];
+    const float gt = gpw[t];
     const int cbeg = (warp >> 2) * 32;
 #pragma unroll
     for (int c0 = cbeg; c0 < cbeg + 32; c0 += 16) {
       float v[16];
       tmem_ld16(tmem + lane_base + c0, v);
       tmem_wait_ld();
+      // A 16-column block lies wholly inside or outside t's chunk (16 | C); it
+      // is before, on or after t's own 16-block.
+      const int cb = c0 >> 4, tt = t & 15;
+      const bool live = c0 >= cs && cb <= bt, diag = cb == bt;
+      float b16[16];
+      ld16f(bta + c0, b16);
       if (lrow < 64) {
+        float o[16];
 #pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-          float4 o;
-          const int j = c0 + e;
-          o.x = (j + 0 < t && j + 0 >= cs) ? bta[j + 0] * v[e + 0] : 0.f;
-          o.y = (j + 1 < t && j + 1 >= cs) ? bta[j + 1] * v[e + 1] : 0.f;
-          o.z = (j + 2 < t && j + 2 >= cs) ? bta[j + 2] * v[e + 2] : 0.f;
-          o.w = (j + 3 < t && j + 3 >= cs) ? bta[j + 3] * v[e + 3] : 0.f;
-          *reinterpret_cast<float4*>(X + t * kLdX + j) = o;
-        }
+        for (int e = 0; e < 16; ++e) o[e] = (live && (!diag || e < tt)) ? b16[e] * v[e] : 0.f;
+#pragma unroll
+        for (int e = 0; e < 16; e += 4)
+          *reinterpret_cast<float4*>(X + t * kLdX + c0 + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
       } else {
-        const int cb = c0 >> 4;
-        float top[16], bot[16];
+        float top[16], bot[16], gam[16];
+        if (diag) {
+          ld16f(gdiag + t * kLdGd, gam);
+        } else {
+          ld16f(sfac + c0, gam);
+          const float rb = rfac[t * 4 + cb];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) gam[e] *= rb;
+        }
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int j = c0 + e;
-          const bool causal = j <= t && j >= cs;
-          top[e] = causal ? gt * bta[j] * v[e] : 0.f;
-          float gam;
-          if (cb < bt) gam = rfac[t * 4 + cb] * sfac[j];   // 0 for an earlier chunk
-          else gam = causal ? ex2(lt - lam[j]) : 0.f;
-          bot[e] = gam * v[e];
+          const bool keep = live && (!diag || e <= tt);
+          top[e] = keep ? gt * b16[e] * v[e] : 0.f;
+          bot[e] = keep ? gam[e] * v[e] : 0.f;
         }
-        st_shared_v4(sbase + kOffA3 + sw128(t, c0), pack8(top));
-        st_shared_v4(sbase + kOffA3 + sw128(t, c0 + 8), pack8(top + 8));
-        st_shared_v4(sbase + kOffA3 + sw128(64 + t, c0), pack8(bot));
-        st_shared_v4(sbase + kOffA3 + sw128(64 + t, c0 + 8), pack8(bot + 8));
+        st_sm16(sm, kOffA3 + sw128(t, c0), pack8(top));
+        st_sm16(sm, kOffA3 + sw128(t, c0 + 8), pack8(top + 8));
+        st_sm16(sm, kOffA3 + sw128(64 + t, c0), pack8(bot));
+        st_sm16(sm, kOffA3 + sw128(64 + t, c0 + 8), pack8(bot + 8));
       }
     }
   }
@@ -422,17 +454,27 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       if (row >= 64) {
         // T_L is zero above the diagonal and across chunks (rfac is 0 there too).
         const int bj = col0 >> 4;
+        float f[8];
         if (bj < (t >> 4)) {
           const float rb = bta[t] * rfac[t * 4 + bj];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) v[e] *= rb * sfac[col0 + e];
+          const float4 s0 = *reinterpret_cast<const float4*>(sfac + col0);
+          const float4 s1 = *reinterpret_cast<const float4*>(sfac + col0 + 4);
+          f[0] = s0.x * rb; f[1] = s0.y * rb; f[2] = s0.z * rb; f[3] = s0.w * rb;
+          f[4] = s1.x * rb; f[5] = s1.y * rb; f[6] = s1.z * rb; f[7] = s1.w * rb;
         } else {
-          const float bt = bta[t], lt = lam[t];
+          const float bt = bta[t];
+          const float* gd = gdiag + t * kLdGd + (col0 & 15);
+          const float4 s0 = *reinterpret_cast<const float4*>(gd);
+          const float4 s1 = *reinterpret_cast<const float4*>(gd + 4);
+          f[0] = s0.x * bt; f[1] = s0.y * bt; f[2] = s0.z * bt; f[3] = s0.w * bt;
+          f[4] = s1.x * bt; f[5] = s1.y * bt; f[6] = s1.z * bt; f[7] = s1.w * bt;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) v[e] = (col0 + e <= t) ? v[e] * bt * ex2(lt - lam[col0 + e]) : 0.f;
+          for (int e = 0; e < 8; ++e) f[e] = (col0 + e <= t) ? f[e] : 0.f;
         }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] *= f[e];
       }
-      st_shared_v4(sbase + kOffB + sw128(row, col0), pack8(v));
+      st_sm16(sm, kOffB + sw128(row, col0), pack8(v));
     }
     fence_proxy_async();
   }
@@ -469,11 +511,11 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const bool top = lrow < 64;
     const int t = lrow & 63;
     const uint32_t src = tmem + lane_base + (top ? 0 : 128);
-    const uint32_t bdst = sbase + kOffB + (top ? 0 : 16384);
+    const uint32_t bdst = kOffB + (top ? 0 : 16384);
     const float scale = top ? gc[t / C] * bta[t] : gsuf[t];
     // Staging for the workspace rows (K and V are dead after G2): 128B-swizzled
     // 64-column halves, stored below with TMA.
-    const uint32_t stage = top ? sbase + kOffKQ : sbase + kOffV;
+    const uint32_t stage = top ? kOffKQ : kOffV;
     const uint32_t half_stride = top ? 16384 : 8192;
     const int cbeg = (warp >> 2) * 64;
 #pragma unroll
@@ -482,13 +524,13 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       tmem_ld16(src + col, v);
       tmem_wait_ld();
       const uint32_t atom = bdst + (col >> 6) * 8192;
-      st_shared_v4(atom + sw128(t, col & 63), pack8(v));
-      st_shared_v4(atom + sw128(t, (col & 63) + 8), pack8(v + 8));
+      st_sm16(sm, atom + sw128(t, col & 63), pack8(v));
+      st_sm16(sm, atom + sw128(t, (col & 63) + 8), pack8(v + 8));
 #pragma unroll
       for (int j = 0; j < 16; ++j) v[j] *= scale;
       const uint32_t hs = stage + (col >> 6) * half_stride;
-      st_shared_v4(hs + sw128(t, col & 63), pack8(v));
-      st_shared_v4(hs + sw128(t, (col & 63) + 8), pack8(v + 8));
+      st_sm16(sm, hs + sw128(t, col & 63), pack8(v));
+      st_sm16(sm, hs + sw128(t, (col & 63) + 8), pack8(v + 8));
     }
   }
   if (ok) fence_proxy_async();
@@ -536,7 +578,7 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const int t = lrow & 63;
     const uint32_t src = tmem + lane_base + (top ? 0 : 128);
     // Staging (A3 and B3 are dead after G3).
-    const uint32_t stage = top ? sbase + kOffA3 : sbase + kOffB;
+    const uint32_t stage = top ? kOffA3 : kOffB;
     const float gt = gpw[t];
     const int cbeg = (warp >> 2) * 64;
 #pragma unroll
@@ -545,16 +587,16 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       tmem_ld16(src + col, v);
       tmem_wait_ld();
       if (top) {  // Qh = G q - G M P  (step 7, state-free part)
-        const uint32_t qa = sbase + kOffKQ + (col >> 6) * 16384 + 8192;
+        const uint8_t* qa = sm + kOffKQ + (col >> 6) * 16384 + 8192;
         float q[16];
-        unpack8(ld_shared_v4(qa + sw128(t, col & 63)), q);
-        unpack8(ld_shared_v4(qa + sw128(t, (col & 63) + 8)), q + 8);
+        unpack8(*reinterpret_cast<const uint4*>(qa + sw128(t, col & 63)), q);
+        unpack8(*reinterpret_cast<const uint4*>(qa + sw128(t, (col & 63) + 8)), q + 8);
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] = gt * q[j] - v[j];
       }
       const uint32_t hs = stage + (col >> 6) * 8192;
-      st_shared_v4(hs + sw128(t, col & 63), pack8(v));
-      st_shared_v4(hs + sw128(t, (col & 63) + 8), pack8(v + 8));
+      st_sm16(sm, hs + sw128(t, col & 63), pack8(v));
+      st_sm16(sm, hs + sw128(t, (col & 63) + 8), pack8(v + 8));
     }
   }
   if (ok && tid < 64 / C) wsGC[tile_id * 4 + tid] = gc[tid];
@@ -571,7 +613,7 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       tma_store_2d(&tm_uys, sbase + kOffB + h * 8192, 64 * h, row0 + 64);  // y_loc rows
     }
     bulk_commit();
-    bulk_wait_all();  // the staging stays valid and the rows land before the CTA exits
+    bulk_wait_read_all();  // the staging must stay valid until the stores have read it
   }
 
   tc_fence_before();

@@ -117,9 +117,10 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src,
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-// Wait until every committed bulk store has completed (global writes done).
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+// Wait until every committed bulk store has finished reading shared memory
+// (the global writes complete on their own before the grid does).
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 // Generic-proxy shared-memory writes -> visible to the async proxy (MMA/TMA).
