@@ -21,11 +21,14 @@
 //   plus G_C (fp32) per chunk.
 // scan_tc_kernel, one CTA per (b, hv, tile of R value rows); S (R x 128, fp32)
 // lives in registers, one column per thread, and as a bf16 MMA operand in
-// shared memory.  Per chunk:
-//   MMA1  D1 = [Pt; Qh] S^T            -> S Pt^T and S Qh^T
-//         W = Ut - S Pt^T;  y = (S Qh^T + Yloc) / sqrt(Dk)            (steps 7-8)
-//   MMA2  D2 = K^T W^T                  S <- G_C S + (W K)           (step 9)
-// A warp-specialised TMA producer double-buffers the tile operands.
+// shared memory.  Step 9 is regrouped as S <- G_C S - S M + N with
+// M = Pt^T K and N = Ut^T K, so per chunk only the product with M waits for
+// the state:
+//   D  = K^T Ut + (-M^T) S^T;  S <- G_C S + D^T                       (step 9)
+//   Y  = Qh S^T;               y = (Y + Yloc) / sqrt(Dk)              (steps 7-8)
+// M^T = K^T Pt is formed one chunk ahead on the tensor cores.  Warp-specialised:
+// a TMA producer (three tile stages), an MMA issuer, the state group and an
+// auxiliary group (M^T to a bf16 operand, the y epilogue).
 #include "gdn_internal.cuh"
 #include "sm100_ptx.cuh"
 
@@ -624,212 +627,313 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 // ============================================================================
 // scan kernel
 // ============================================================================
-constexpr int kScanThreads = 160;  // warp 0: TMA producer; warps 1..4: compute
-constexpr int kStages = 2;
+// With M = Pt^T K (Dk x Dk) and N = Ut^T K, the state update of a chunk is
+//   S <- G_C S - S M + N,
+// so the only product that needs the state is S M; M, N and the output
+// product y = Yloc + Qh S^T are off the serial path.  Per chunk j:
+//   issuer  [M^T | N^T] = K^T [Pt | Ut]   (C/16 MMAs, N = 192; one chunk ahead)
+//           N^T += (-M^T) S_op^T           (8 MMAs, A = -M^T as bf16 in TMEM)
+//           Y    = Qh S_op^T               (8 MMAs, M = 64)
+//   state   S = G_C S + (N^T)^T; write S (bf16) as the next MMA operand
+//   aux     M^T (fp32) -> -M^T (bf16) in place; y = (Yloc + Y) / sqrt(Dk)
+// N^T is formed for the 64-wide value block holding this CTA's R rows.
+// Warp 0 is the TMA producer (three tile stages), warp 1 issues the MMAs and
+// owns the tensor memory, warps 2-5 hold S (thread = TMEM lane = key column k),
+// warps 6-9 are the auxiliary group.
+constexpr int kScanThreads = 320;
+constexpr int kStages = 3;
+constexpr uint32_t kScanTmemCols = 512;
 
 template <int R>
 struct ScanSmem {
-  static constexpr uint32_t kA1 = 32 * 1024;
-  static constexpr uint32_t kK = 16 * 1024;
-  static constexpr uint32_t kUY = 2 * 64 * 2 * R;
-  static constexpr uint32_t kGC = 16;           // G_C of the tile's chunks (fp32 x 4)
-  static constexpr uint32_t kStage = ((kA1 + kK + kUY + kGC) + 1023) & ~1023u;
-  static constexpr uint32_t kS = 128 * 2 * R;  // S operand: 128 K-rows x R
-  static constexpr uint32_t kW = 64 * 2 * R;   // W operand: up to 64 K-rows x R
+  // Pt (two 64-column halves of the [Pt; Qh] tile) and the 64-wide Ut block
+  // form three 128-row MN-major atoms 16 KB apart: the B operand of K^T [Pt | Ut].
+  // Chunk c's Ut rows sit at rows 2*C*c.., level with its Pt rows.
+  static constexpr uint32_t kA1 = 32 * 1024;  // [Pt; Qh]: 2 x 128 rows x 128 B
+  static constexpr uint32_t kOffU = kA1;      // Ut block, 128 rows x 128 B
+  static constexpr uint32_t kOffK = kOffU + 16384;  // K tile: 2 x 64 rows x 128 B
+  static constexpr uint32_t kOffY = kOffK + 16384;  // Yloc slice: 64 rows x R (MN-major)
+  static constexpr uint32_t kY = 64 * 2 * R;
+  static constexpr uint32_t kOffGC = kOffY + kY;    // G_C of the tile's chunks (fp32 x 4)
+  static constexpr uint32_t kGC = 16;
+  static constexpr uint32_t kStage = (kOffGC + kGC + 1023) & ~1023u;
+  static constexpr uint32_t kS = 128 * 2 * R;  // one S operand: 128 K-rows x R
   static constexpr uint32_t kOffS = kStages * kStage;
-  static constexpr uint32_t kOffW = kOffS + ((kS + 1023) & ~1023u);
-  static constexpr uint32_t kTotal = kOffW + ((kW + 1023) & ~1023u) + 1024;
+  static constexpr uint32_t kTotal = kOffS + 2 * ((kS + 1023) & ~1023u) + 1024;
+};
+
+// mbarrier slots
+enum : int {
+  kBFull = 0,                 // [kStages] tile landed (TMA)
+  kBEmpty = kBFull + kStages, // [kStages] tile consumed (256 thread arrivals)
+  kBDs = kBEmpty + kStages,   // serial product complete
+  kBY,                        // Y complete
+  kBM,                        // [2] [M^T | N^T] complete
+  kBSop = kBM + 2,            // S operand written (128 arrivals)
+  kBDsFree,                   // N^T read by the state group (128)
+  kBMt,                       // [2] -M^T operand written (128)
+  kBYFree = kBMt + 2,         // Y read by the aux group (128)
+  kBFin,                      // every MMA retired
+  kNumScanBars
 };
 
 template <int C, int R>
 __global__ void __launch_bounds__(kScanThreads, 1)
 scan_tc_kernel(const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_uy, const float* __restrict__ wsGC,
-               const float* state_in, float* state_out, bf16* __restrict__ y, int T, int Hk,
-               int Hv, int NT, float scale) {
+               const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_y,
+               const float* __restrict__ wsGC, const float* state_in, float* state_out,
+               bf16* __restrict__ y, int T, int Hk, int Hv, int NT, float scale) {
+  static_assert(R == 32 || R == 64, "value rows per CTA");
   using SM = ScanSmem<R>;
+  constexpr int kCt = kTile / C;  // chunks per tile
+  constexpr uint32_t kRowBytes = 2 * R;
+  constexpr uint32_t kMnLay = mn_layout<R>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~(uintptr_t)1023);
-  __shared__ uint64_t bars[2 * kStages + 1];
+  __shared__ uint64_t bars[kNumScanBars];
   __shared__ uint32_t tmem_base_sh;
-  __shared__ int abort_sh;
   const uint32_t sbase = smem_u32(sm);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tile = blockIdx.x, bh = blockIdx.y;
   const int b = bh / Hv, hv = bh - b * Hv, hk = hv / (Hv / Hk);
   const int r0 = tile * R;
-  auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
-  auto empty_bar = [&](int s) { return smem_u32(&bars[kStages + s]); };
-  const uint32_t bar_mma = smem_u32(&bars[2 * kStages]);
+  const int NC = (T + C - 1) / C;  // chunks holding at least one token
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(bar(kBFull + s), 1);
+      mbar_init(bar(kBEmpty + s), 256);
     }
-    mbar_init(bar_mma, 1);
-    abort_sh = 0;
+    mbar_init(bar(kBDs), 1);
+    mbar_init(bar(kBY), 1);
+    mbar_init(bar(kBM), 1);
+    mbar_init(bar(kBM + 1), 1);
+    mbar_init(bar(kBSop), 128);
+    mbar_init(bar(kBDsFree), 128);
+    mbar_init(bar(kBMt), 128);
+    mbar_init(bar(kBMt + 1), 128);
+    mbar_init(bar(kBYFree), 128);
+    mbar_init(bar(kBFin), 1);
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&tmem_base_sh), 2 * R < 32 ? 32 : 2 * R);
+    tmem_alloc(smem_u32(&tmem_base_sh), kScanTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-  const uint32_t tD1 = tmem, tD2 = tmem + R;
+  // Two 192-column buffers: cols 0-127 M^T (fp32; cols 0-63 then hold -M^T as
+  // bf16 pairs), cols 128-191 N^T of the 64-wide value block; then Y.
+  auto tMN = [&](int x) { return tmem + 192 * x; };
+  const uint32_t tY = tmem + 384;
+  const uint32_t nt_col = 128 + (r0 & 63);  // this CTA's R columns inside N^T
+  auto stage_addr = [&](int j) { return sbase + ((j / kCt) % kStages) * SM::kStage; };
+  auto sS = [&](int x) { return sbase + SM::kOffS + x * ((SM::kS + 1023) & ~1023u); };
+  auto last_of_tile = [&](int j) { return (j % kCt) == kCt - 1 || j == NC - 1; };
+  // Wait for the tile holding chunk j (used once per tile per role).
+  auto wait_tile = [&](int j) {
+    const int n = j / kCt;
+    return mbar_wait(bar(kBFull + n % kStages), (n / kStages) & 1);
+  };
 
   if (warp == 0) {
     // ------------------------------ producer ------------------------------
     if (lane == 0) {
       prefetch_tmap(&tm_a1);
       prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_uy);
-      for (int n = 0; n < NT; ++n) {
+      prefetch_tmap(&tm_u);
+      prefetch_tmap(&tm_y);
+      int n = 0;
+      for (; n < NT; ++n) {
         const int s = n % kStages;
-        if (n >= kStages && !mbar_wait(empty_bar(s), ((n / kStages) - 1) & 1)) break;
+        if (n >= kStages && !mbar_wait(bar(kBEmpty + s), ((n / kStages) - 1) & 1)) break;
         const uint32_t st = sbase + s * SM::kStage;
+        const uint32_t fb = bar(kBFull + s);
         const int row = (int)(((size_t)bh * NT + n) * 128);
-        mbar_expect_tx(full_bar(s), SM::kA1 + SM::kK + SM::kUY + SM::kGC);
-        bulk_load(st + SM::kA1 + SM::kK + SM::kUY, wsGC + ((size_t)bh * NT + n) * 4, SM::kGC,
-                  full_bar(s));
-        tma_load_2d(st, &tm_a1, full_bar(s), 0, row);
-        tma_load_2d(st + 16384, &tm_a1, full_bar(s), 64, row);
-        tma_load_4d(st + SM::kA1, &tm_k, full_bar(s), 0, hk, n * kTile, b);
-        tma_load_4d(st + SM::kA1 + 8192, &tm_k, full_bar(s), 64, hk, n * kTile, b);
-        tma_load_2d(st + SM::kA1 + SM::kK, &tm_uy, full_bar(s), r0, row);
-        tma_load_2d(st + SM::kA1 + SM::kK + 64 * 2 * R, &tm_uy, full_bar(s), r0, row + 64);
+        mbar_expect_tx(fb, SM::kA1 + kTile * 128 + 16384 + SM::kY + SM::kGC);
+        bulk_load(st + SM::kOffGC, wsGC + ((size_t)bh * NT + n) * 4, SM::kGC, fb);
+        tma_load_2d(st, &tm_a1, fb, 0, row);
+        tma_load_2d(st + 16384, &tm_a1, fb, 64, row);
+#pragma unroll
+        for (int c = 0; c < kCt; ++c)
+          tma_load_2d(st + SM::kOffU + 2 * C * c * 128, &tm_u, fb, r0 & ~63, row + c * C);
+        tma_load_4d(st + SM::kOffK, &tm_k, fb, 0, hk, n * kTile, b);
+        tma_load_4d(st + SM::kOffK + 8192, &tm_k, fb, 64, hk, n * kTile, b);
+        tma_load_2d(st + SM::kOffY, &tm_y, fb, r0, row + 64);
       }
+      // Let the last copies land before the CTA can exit (they have, unless a
+      // consumer gave up early).
+      for (int m = (n > kStages ? n - kStages : 0); m < n; ++m)
+        mbar_wait(bar(kBFull + m % kStages), (m / kStages) & 1);
     }
     return;
   }
 
-  // ------------------------------- compute --------------------------------
-  const int L = ((warp & 3) << 5) | lane;  // TMEM lane = value-column index of S
-  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-  const bool issuer = (warp == 1 && lane == 0);
-  const size_t sidx = ((size_t)bh * kD + r0) * kD + L;
-  float s[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) s[r] = state_in ? state_in[sidx + (size_t)r * kD] : 0.f;
-
-  auto write_rows = [&](uint32_t base, int row, const float* v) {
-#pragma unroll
-    for (int ch = 0; ch < R / 8; ++ch)
-      st_shared_v4(base + mn_row_chunk<R>(row, ch), pack8(v + 8 * ch));
-  };
-  const uint32_t sS = sbase + SM::kOffS, sW = sbase + SM::kOffW;
-  write_rows(sS, L, s);
-  fence_proxy_async();
-  named_bar_sync(1, 128);
-
-  const uint32_t id1 = idesc_bf16(128, R, false, true);
-  const uint32_t id2 = idesc_bf16(128, R, true, true);
-  constexpr uint32_t kMnLay = mn_layout<R>();
-  constexpr uint32_t kRowBytes = 2 * R;
-  uint32_t mma_phase = 0;
   bool ok = true;
-
-  for (int n = 0; n < NT && ok; ++n) {
-    const int st_i = n % kStages;
-    const uint32_t st = sbase + st_i * SM::kStage;
-    const uint32_t stK = st + SM::kA1, stU = st + SM::kA1 + SM::kK, stY = stU + 64 * 2 * R;
-    ok = mbar_wait(full_bar(st_i), (n / kStages) & 1);
-    if (!ok) break;
-    for (int c = 0; c < kTile / C; ++c) {
-      const int tok0 = n * kTile + c * C;
-      if (tok0 >= T) break;
-      const float Gc = ld_shared_f32(st + SM::kA1 + SM::kK + SM::kUY + 4 * c);
-      // This thread's addend row (Ut for W, Yloc for y), fetched before the MMA wait.
-      uint4 addend[R / 8];
-      if (L < 2 * C) {
-        const uint32_t arow = L < C ? stU + (c * C + L) * (2 * R) : stY + (c * C + L - C) * (2 * R);
+  if (warp == 1) {
+    // ---------------------------- MMA issuer -----------------------------
+    if (lane == 0) {
+      const uint32_t id_mn = idesc_bf16(128, 192, true, true);
+      const uint32_t id_s = idesc_bf16(128, R, false, true);
+      const uint32_t id_y = idesc_bf16(64, R, false, true);
+      // [M^T | N^T] of chunk j = K^T [Pt | Ut]: A = K^T, B = three MN-major atoms.
+      auto issue_mn = [&](int j) {
+        const uint32_t st = stage_addr(j);
+        const int c = j % kCt;
 #pragma unroll
-        for (int ch = 0; ch < R / 8; ++ch) addend[ch] = ld_shared_v4(arow + ch * 16);
+        for (int kk = 0; kk < C / 16; ++kk) {
+          const uint64_t a = smem_desc(st + SM::kOffK + (c * C + 16 * kk) * 128, 8192, 1024, kSw128);
+          const uint64_t bd = smem_desc(st + (2 * C * c + 16 * kk) * 128, 16384, 1024, kSw128);
+          mma_bf16_ss(tMN(j & 1), a, bd, id_mn, kk > 0);
+        }
+        mma_commit(bar(kBM + (j & 1)));
+      };
+      if (NC > 0) {
+        ok = wait_tile(0);
+        tc_fence_after();
+        if (ok) issue_mn(0);
       }
-      if (issuer) {
+      for (int j = 0; j < NC && ok; ++j) {
+        const int c = j % kCt;
+        const uint32_t st = stage_addr(j);
+        const uint32_t sop = sS(j & 1);
+        // N^T += (-M^T) S^T   (the serial step)
+        if (!(ok = mbar_wait(bar(kBSop), j & 1))) break;
+        if (!(ok = mbar_wait(bar(kBMt + (j & 1)), (j >> 1) & 1))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ts(tMN(j & 1) + nt_col, tMN(j & 1) + 8 * kk,
+                      smem_desc(sop + kk * 16 * kRowBytes, 0, 8 * kRowBytes, kMnLay), id_s, 1);
+        mma_commit(bar(kBDs));
+        // [M^T | N^T] of the next chunk, once the state group has read chunk j-1's.
+        if (j + 1 < NC) {
+          if (j > 0 && !(ok = mbar_wait(bar(kBDsFree), (j - 1) & 1))) break;
+          if ((j + 1) % kCt == 0 && !(ok = wait_tile(j + 1))) break;
+          tc_fence_after();
+          issue_mn(j + 1);
+        }
+        // Y = Qh S^T (M = 64: the chunk's Qh rows)
+        if (j > 0 && !(ok = mbar_wait(bar(kBYFree), (j - 1) & 1))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t a = st + (kk >> 2) * 16384 + (2 * C * c) * 128 + (kk & 3) * 32;
-          const uint64_t bd = smem_desc(sS + kk * 16 * kRowBytes, 0, 8 * kRowBytes, kMnLay);
-          mma_bf16_ss(tD1, smem_desc(a, 16, 1024, kSw128), bd, id1, kk > 0);
+          const uint32_t a = st + (kk >> 2) * 16384 + (2 * C * c + C) * 128 + (kk & 3) * 32;
+          mma_bf16_ss(tY, smem_desc(a, 16, 1024, kSw128),
+                      smem_desc(sop + kk * 16 * kRowBytes, 0, 8 * kRowBytes, kMnLay), id_y, kk > 0);
         }
-        mma_commit(bar_mma);
+        mma_commit(bar(kBY));
       }
-      if (!mbar_wait(bar_mma, mma_phase)) { abort_sh = 1; }
-      mma_phase ^= 1;
+      // Every MMA retires before the tensor memory is released.
+      mma_commit(bar(kBFin));
+      mbar_wait(bar(kBFin), 0);
+    }
+    __syncwarp();
+  } else if (warp < 6) {
+    // ---------------------------- state group ----------------------------
+    const int L = ((warp & 3) << 5) | lane;  // TMEM lane = key column of S
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const size_t sidx = ((size_t)bh * kD + r0) * kD + L;
+    float s[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) s[r] = state_in ? state_in[sidx + (size_t)r * kD] : 0.f;
+    auto write_op = [&](int x) {
+#pragma unroll
+      for (int ch = 0; ch < R / 8; ++ch)
+        st_shared_v4(sS(x) + mn_row_chunk<R>(L, ch), pack8(s + 8 * ch));
+      fence_proxy_async();
+      mbar_arrive(bar(kBSop));
+    };
+    write_op(0);
+    for (int j = 0; j < NC; ++j) {
+      const int c = j % kCt;
+      const uint32_t st = stage_addr(j);
+      if (c == 0 && !(ok = wait_tile(j))) break;
+      const float Gc = ld_shared_f32(st + SM::kOffGC + 4 * c);
+      if (!(ok = mbar_wait(bar(kBDs), j & 1))) break;
       tc_fence_after();
       float d[R];
 #pragma unroll
-      for (int j = 0; j < R; j += 16) tmem_ld16(tD1 + lane_base + j, d + j);
+      for (int q = 0; q < R; q += 16) tmem_ld16(tMN(j & 1) + nt_col + lane_base + q, d + q);
       tmem_wait_ld();
-      if (L < C) {
-        // W = Ut - S Pt^T for this chunk's token L.
-        float w[R];
-#pragma unroll
-        for (int ch = 0; ch < R / 8; ++ch) {
-          float u8[8];
-          unpack8(addend[ch], u8);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) w[ch * 8 + e] = u8[e] - d[ch * 8 + e];
-        }
-        write_rows(sW, L, w);
-      } else if (L < 2 * C) {
-        const int tl = L - C;
-        if (tok0 + tl < T) {
-          bf16* yp = y + (((size_t)b * T + tok0 + tl) * Hv + hv) * kD + r0;
-#pragma unroll
-          for (int ch = 0; ch < R / 8; ++ch) {
-            float y8[8];
-            unpack8(addend[ch], y8);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) y8[e] = (y8[e] + d[ch * 8 + e]) * scale;
-            *reinterpret_cast<uint4*>(yp + ch * 8) = pack8(y8);
-          }
-        }
-      }
       tc_fence_before();
-      fence_proxy_async();
-      named_bar_sync(1, 128);
-      if (abort_sh) { ok = false; break; }
-      if (issuer) {
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < C / 16; ++kk) {
-          const uint32_t a = stK + (c * C + 16 * kk) * 128;
-          const uint64_t bd = smem_desc(sW + kk * 16 * kRowBytes, 0, 8 * kRowBytes, kMnLay);
-          mma_bf16_ss(tD2, smem_desc(a, 8192, 1024, kSw128), bd, id2, kk > 0);
-        }
-        mma_commit(bar_mma);
-      }
-      if (!mbar_wait(bar_mma, mma_phase)) { abort_sh = 1; }
-      mma_phase ^= 1;
-      tc_fence_after();
-#pragma unroll
-      for (int j = 0; j < R; j += 16) tmem_ld16(tD2 + lane_base + j, d + j);
-      tmem_wait_ld();
+      mbar_arrive(bar(kBDsFree));
+      if (last_of_tile(j)) mbar_arrive(bar(kBEmpty + (j / kCt) % kStages));
 #pragma unroll
       for (int r = 0; r < R; ++r) s[r] = fmaf(Gc, s[r], d[r]);
-      write_rows(sS, L, s);
-      tc_fence_before();
-      fence_proxy_async();
-      named_bar_sync(1, 128);
-      if (abort_sh) { ok = false; break; }
+      if (j + 1 < NC) write_op((j + 1) & 1);
     }
-    if (issuer) mma_commit(empty_bar(st_i));  // stage free once its MMAs finish
+    if (ok) {
+#pragma unroll
+      for (int r = 0; r < R; ++r) state_out[sidx + (size_t)r * kD] = s[r];
+    }
+  } else {
+    // ----------------------------- aux group -----------------------------
+    const int qd = warp & 3;
+    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+    // M^T (fp32, cols 0-127) -> -M^T as bf16 pairs in cols 0-63 of the same
+    // buffer (each thread rewrites only its own lane, after reading it).
+    auto convert = [&](int j) {
+      if (!mbar_wait(bar(kBM + (j & 1)), (j >> 1) & 1)) return false;
+      tc_fence_after();
+      const uint32_t tb = tMN(j & 1) + lane_base;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float v[64];
+        tmem_ld32(tb + 64 * h, v);
+        tmem_ld32(tb + 64 * h + 32, v + 32);
+        tmem_wait_ld();
+        uint32_t p[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) p[i] = pack_bf16x2(-v[2 * i], -v[2 * i + 1]);
+        tmem_st32(tb + 32 * h, p);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(kBMt + (j & 1)));
+      return true;
+    };
+    if (NC > 0) ok = convert(0);
+    for (int j = 0; j < NC && ok; ++j) {
+      const int c = j % kCt;
+      const uint32_t st = stage_addr(j);
+      if (j + 1 < NC && !(ok = convert(j + 1))) break;
+      if (c == 0 && !(ok = wait_tile(j))) break;
+      if (!(ok = mbar_wait(bar(kBY), j & 1))) break;
+      tc_fence_after();
+      float d[R];
+#pragma unroll
+      for (int q = 0; q < R; q += 16) tmem_ld16(tY + lane_base + q, d + q);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(kBYFree));
+      // M = 64 result: row 16*qd + i sits in lane 32*qd + i, i < 16.
+      const int t = 16 * qd + lane;
+      const int tok = j * C + t;
+      if (lane < 16 && t < C && tok < T) {
+        bf16* yp = y + (((size_t)b * T + tok) * Hv + hv) * kD + r0;
+        const uint32_t yrow = st + SM::kOffY;
+#pragma unroll
+        for (int ch = 0; ch < R / 8; ++ch) {
+          float y8[8];
+          unpack8(ld_shared_v4(yrow + mn_row_chunk<R>(c * C + t, ch)), y8);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) y8[e] = (y8[e] + d[ch * 8 + e]) * scale;
+          *reinterpret_cast<uint4*>(yp + ch * 8) = pack8(y8);
+        }
+      }
+      // Y(j) complete implies every earlier MMA reading this tile is too.
+      if (last_of_tile(j)) mbar_arrive(bar(kBEmpty + (j / kCt) % kStages));
+    }
   }
 
-  if (ok) {
-#pragma unroll
-    for (int r = 0; r < R; ++r) state_out[sidx + (size_t)r * kD] = s[r];
-  }
   tc_fence_before();
-  named_bar_sync(1, 128);
-  if (warp == 1) tmem_dealloc(tmem, 2 * R < 32 ? 32 : 2 * R);
+  named_bar_sync(1, kScanThreads - 32);
+  if (warp == 1) tmem_dealloc(tmem, kScanTmemCols);
 }
 
 // ============================================================================
@@ -866,16 +970,20 @@ bool make_bthd_map(CUtensorMap* m, const void* base, int B, int T, int H) {
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-// [rows, 128] bf16 2-D view of a workspace region.
+// [rows, 128] bf16 2-D view of a workspace region.  Swizzled boxes use the
+// swizzle whose span equals the box row (box_cols * 2 bytes: 32, 64 or 128).
 bool make_rows_map(CUtensorMap* m, const void* base, size_t rows, int box_cols, int box_rows,
                    bool swizzle) {
   const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
   const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   const cuuint32_t es[2] = {1, 1};
+  CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (swizzle)
+    sw = box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
+                        : (box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
   return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -893,11 +1001,12 @@ cudaError_t launch_c(const PrefillArgs& a) {
   float* wsGC = reinterpret_cast<float*>(ws + w.gc);
 
   if (!encode_fn()) return cudaErrorNotSupported;
-  CUtensorMap tk, tq, tv, ta1, tuy, ta1s, tuys;
+  CUtensorMap tk, tq, tv, ta1, tuy, tuc, ta1s, tuys;
   if (!make_bthd_map(&tk, a.k, a.B, a.T, a.Hk) || !make_bthd_map(&tq, a.q, a.B, a.T, a.Hk) ||
       !make_bthd_map(&tv, a.v, a.B, a.T, a.Hv) ||
       !make_rows_map(&ta1, wsA1, (size_t)BH * NT * 128, 64, 128, true) ||
-      !make_rows_map(&tuy, wsUY, (size_t)BH * NT * 128, kScanRows, 64, false) ||
+      !make_rows_map(&tuy, wsUY, (size_t)BH * NT * 128, kScanRows, 64, true) ||
+      !make_rows_map(&tuc, wsUY, (size_t)BH * NT * 128, 64, C, true) ||
       !make_rows_map(&ta1s, wsA1, (size_t)BH * NT * 128, 64, C, true) ||
       !make_rows_map(&tuys, wsUY, (size_t)BH * NT * 128, 64, 64, true))
     return cudaErrorInvalidValue;
@@ -917,7 +1026,7 @@ cudaError_t launch_c(const PrefillArgs& a) {
   if (e != cudaSuccess) return e;
   const float scale = 1.0f / sqrtf((float)kD);
   scan_tc_kernel<C, kScanRows><<<dim3(kD / kScanRows, BH), kScanThreads, SM::kTotal, a.stream>>>(
-      ta1, tk, tuy, wsGC, a.state_in, a.state_out, static_cast<bf16*>(a.y), a.T, a.Hk, a.Hv, NT,
+      ta1, tk, tuc, tuy, wsGC, a.state_in, a.state_out, static_cast<bf16*>(a.y), a.T, a.Hk, a.Hv, NT,
       scale);
   return cudaGetLastError();
 }
