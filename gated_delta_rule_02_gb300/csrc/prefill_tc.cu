@@ -32,6 +32,7 @@
 #include "gdn_internal.cuh"
 #include "sm100_ptx.cuh"
 
+#include <algorithm>
 #include <mutex>
 
 namespace gdn {
@@ -45,7 +46,7 @@ constexpr int kD = kHeadDim;
 
 // ------------------------------- workspace --------------------------------
 struct WsLayout {
-  size_t a1, uy, gc, total;
+  size_t a1, uy, gc, flags, total;
 };
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 inline WsLayout ws_layout(int BH, int NT) {
@@ -54,7 +55,8 @@ inline WsLayout ws_layout(int BH, int NT) {
   w.a1 = 0;
   w.uy = align256(tiles * 128 * kD * sizeof(bf16));
   w.gc = w.uy + align256(tiles * 128 * kD * sizeof(bf16));
-  w.total = w.gc + align256(tiles * 4 * sizeof(float));
+  w.flags = w.gc + align256(tiles * 4 * sizeof(float));
+  w.total = w.flags + align256(tiles * sizeof(int));
   return w;
 }
 
@@ -130,8 +132,13 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
 // ============================================================================
 // prep kernel
 // ============================================================================
-constexpr int kPrepThreads = 256;
-// Shared-memory map (bytes from the 1024-aligned base); two CTAs fit per SM.
+// The prep kernel is persistent: one CTA per SM holds two independent groups
+// of eight warps, each with its own shared-memory map, 256 TMEM columns and
+// mbarriers, each looping over tiles.
+constexpr int kPrepGroups = 2;
+constexpr int kPrepGroupThreads = 256;
+constexpr int kPrepThreads = kPrepGroups * kPrepGroupThreads;
+// Shared-memory map of one group (bytes from its 1024-aligned base).
 constexpr uint32_t kOffKQ = 0;        // [K;Q]: 2 halves x (64 K rows + 64 Q rows) x 128 B
 constexpr uint32_t kOffV = 32768;     // V: 2 halves x 64 rows x 128 B
 constexpr uint32_t kOffA3 = 49152;    // A3 (128 rows x 64 K-cols, one 128B half)
@@ -142,7 +149,8 @@ constexpr uint32_t kOffTL = kOffB + 64 * kLdX * 4;
 constexpr uint32_t kOffZ = kOffTL + 64 * kLdX * 4;       // 32 x 32 fp32
 constexpr uint32_t kOffSmall = kOffZ + 32 * 32 * 4;      // per-token scalars
 constexpr int kLdGd = 20;                                 // row stride of the in-block ratios
-constexpr uint32_t kPrepSmem = kOffSmall + (64 * 6 + 256 + 4 + 64 * kLdGd) * 4 + 1024;
+constexpr uint32_t kPrepGroupSmem = (kOffSmall + (64 * 6 + 256 + 4 + 64 * kLdGd) * 4 + 1023) & ~1023u;
+constexpr uint32_t kPrepSmem = kPrepGroups * kPrepGroupSmem + 1024;
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -203,10 +211,11 @@ __device__ __forceinline__ void warp_store_16x8(float* D, int ldd, const float* 
 //   16 x 16 diagonal blocks   T_ii = (I + X_ii)^-1       (one column per thread)
 //   32 x 32 blocks (C >= 32)  T_10 = -T_11 X_10 T_00      (per 16-block pair)
 //   64 x 64 (C = 64)          T_BA = -T_BB X_BA T_AA      (32-block halves)
-// The block products run on warp-level tf32 MMAs; all 256 threads call this.
-template <int C>
-__device__ void invert_unit_lower(const float* X, float* Tm, float* Zs, int u) {
-  for (int idx = u; idx < 64 * 64; idx += kPrepThreads) {
+// The block products run on warp-level tf32 MMAs; the group's 256 threads call
+// this (u = thread index in the group, sync = the group's barrier).
+template <int C, typename Sync>
+__device__ void invert_unit_lower(const float* X, float* Tm, float* Zs, int u, Sync sync) {
+  for (int idx = u; idx < 64 * 64; idx += kPrepGroupThreads) {
     const int r = idx >> 6, c = idx & 63;
     if ((c >> 4) > (r >> 4) || (c / C) != (r / C)) Tm[r * kLdX + c] = 0.f;
   }
@@ -228,7 +237,7 @@ __device__ void invert_unit_lower(const float* X, float* Tm, float* Zs, int u) {
 #pragma unroll
     for (int r = 0; r < 16; ++r) Tm[(base + r) * kLdX + base + jj] = x[r];
   }
-  __syncthreads();
+  sync();
   const int w = u >> 5, lane = u & 31;
   if constexpr (C >= 32) {
     // Pairs (0,1) and (2,3): warp w < 4 handles pair w/2, columns 8*(w%2)..
@@ -239,12 +248,12 @@ __device__ void invert_unit_lower(const float* X, float* Tm, float* Zs, int u) {
       warp_gemm_16x8<16>(d, X + r0 * kLdX + c0, kLdX, Tm + c0 * kLdX + c0 + nt * 8, kLdX, lane);
       warp_store_16x8(Zs + p * 256 + nt * 8, 16, d, lane, 1.f);
     }
-    __syncthreads();
+    sync();
     if (w < 4) {
       warp_gemm_16x8<16>(d, Tm + r0 * kLdX + r0, kLdX, Zs + p * 256 + nt * 8, 16, lane);
       warp_store_16x8(Tm + r0 * kLdX + c0 + nt * 8, kLdX, d, lane, -1.f);
     }
-    __syncthreads();
+    sync();
   }
   if constexpr (C == 64) {
     // M = X[32:64][0:32] T[0:32][0:32], then T[32:64][0:32] = -T[32:64][32:64] M;
@@ -253,28 +262,52 @@ __device__ void invert_unit_lower(const float* X, float* Tm, float* Zs, int u) {
     const int mt = w >> 2, nt = w & 3;
     warp_gemm_16x8<32>(d, X + (32 + mt * 16) * kLdX, kLdX, Tm + nt * 8, kLdX, lane);
     warp_store_16x8(Zs + mt * 16 * 32 + nt * 8, 32, d, lane, 1.f);
-    __syncthreads();
+    sync();
     warp_gemm_16x8<32>(d, Tm + (32 + mt * 16) * kLdX + 32, kLdX, Zs + nt * 8, 32, lane);
     warp_store_16x8(Tm + (32 + mt * 16) * kLdX + nt * 8, kLdX, d, lane, -1.f);
-    __syncthreads();
+    sync();
   }
 }
 
+// Everything the prep work needs (the tensor maps are kernel parameters).
+struct PrepParams {
+  const CUtensorMap* tm_k;
+  const CUtensorMap* tm_q;
+  const CUtensorMap* tm_v;
+  const CUtensorMap* tm_a1s;
+  const CUtensorMap* tm_uys;
+  const bf16* g;
+  const bf16* beta;
+  float* wsGC;
+  int T, Hk, Hv, NT, BH;
+  // When set, y_loc / sqrt(Dk) goes straight to y ([B, T, Hv, 128], 64-token
+  // boxes) instead of the workspace; the scan then adds Qh S^T / sqrt(Dk) to it.
+  const CUtensorMap* tm_y;
+  float yscale;
+};
+
+// The prep work of one CTA (both groups): CTA `cta_rank` of `n_ctas` doing prep.
+// With `flags`, each finished tile (b*Hv + hv, n) is published by setting
+// flags[(b*Hv + hv) * NT + n] to 1 once its workspace rows are in memory.
 template <int C>
-__global__ void __launch_bounds__(kPrepThreads, 2)
-prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
-               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_a1s,
-               const __grid_constant__ CUtensorMap tm_uys, const bf16* __restrict__ g,
-               const bf16* __restrict__ beta, float* __restrict__ wsGC, int T, int Hk, int Hv,
-               int NT) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~(uintptr_t)1023);
-  __shared__ uint64_t bars[2];
+__device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw, int cta_rank,
+                                          int n_ctas, int* flags) {
+  const int T = P.T, Hk = P.Hk, Hv = P.Hv, NT = P.NT, BH = P.BH;
+  const bf16* __restrict__ g = P.g;
+  const bf16* __restrict__ beta = P.beta;
+  float* __restrict__ wsGC = P.wsGC;
+  __shared__ uint64_t bars[kPrepGroups][2];
   __shared__ uint32_t tmem_base_sh;
-  __shared__ float carry_sh;
+  __shared__ float carry_sh[kPrepGroups];
+  __shared__ int abort_sh[kPrepGroups];
+  const int grp = threadIdx.x / kPrepGroupThreads;
+  const int tid = threadIdx.x % kPrepGroupThreads, warp = tid >> 5;  // within the group
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~(uintptr_t)1023) +
+                grp * kPrepGroupSmem;
   const uint32_t sbase = smem_u32(sm);
-  const uint32_t bar_tma = smem_u32(&bars[0]), bar_mma = smem_u32(&bars[1]);
+  const uint32_t bar_tma = smem_u32(&bars[grp][0]), bar_mma = smem_u32(&bars[grp][1]);
+  const int sync_id = 1 + 2 * grp, gates_id = 2 + 2 * grp;  // named barriers of the group
   float* X = reinterpret_cast<float*>(sm + kOffB);               // 64 x 68 fp32
   float* TL = reinterpret_cast<float*>(sm + kOffTL);             // 64 x 68 fp32
   float* Zs = reinterpret_cast<float*>(sm + kOffZ);              // 32 x 32 fp32
@@ -287,39 +320,101 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   float* gc = rfac + 256;   // G at each chunk's end
   float* graw = gc + 4;     // g_t
   float* gdiag = graw + 64; // [64][17]: Gam[t][j] for j in t's 16-block, j <= t (products)
+  auto gsync = [&]() { named_bar_sync(sync_id, kPrepGroupThreads); };
+  // Group-wide AND of ok (sticky: a group that failed a wait stops).
+  auto gsync_and = [&](bool v) {
+    if (!v) abort_sh[grp] = 1;
+    gsync();
+    return abort_sh[grp] == 0;
+  };
 
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int tile = blockIdx.x, bh = blockIdx.y;
-  const int b = bh / Hv, hv = bh - b * Hv, hk = hv / (Hv / Hk);
-  const int t0 = tile * kTile;
-  const size_t tile_id = (size_t)bh * NT + tile;
-
-  if (tid == 0) {
-    mbar_init(bar_tma, 1);
-    mbar_init(bar_mma, 1);
+  if (threadIdx.x == 0) {
+    for (int q = 0; q < kPrepGroups; ++q) {
+      mbar_init(smem_u32(&bars[q][0]), 1);
+      mbar_init(smem_u32(&bars[q][1]), 1);
+      abort_sh[q] = 0;
+    }
     fence_mbar_init();
   }
-  if (warp == 0) {
-    tmem_alloc(smem_u32(&tmem_base_sh), 256);
+  if (threadIdx.x < 32) {
+    tmem_alloc(smem_u32(&tmem_base_sh), 256 * kPrepGroups);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = tmem_base_sh;
+  const uint32_t tmem = tmem_base_sh + 256 * grp;
 
-  if (tid == 0) {
-    prefetch_tmap(&tm_k);
-    prefetch_tmap(&tm_q);
-    prefetch_tmap(&tm_v);
+  // Tiles in chunk-major order (every head's tile n before any head's n+1);
+  // group gid takes gid, gid + ngroups, ...
+  const int total = BH * NT;
+  const int ngroups = n_ctas * kPrepGroups;
+  const int gid = cta_rank * kPrepGroups + grp;
+  auto head_of = [&](int lin) { return lin % BH; };
+  auto tile_of = [&](int lin) { return lin / BH; };
+  // TMA loads of a tile's K and V (with the byte count of K, Q and V) and of its Q.
+  auto load_kv = [&](int lin) {
+    const int bh = head_of(lin), n = tile_of(lin);
+    const int b = bh / Hv, hv = bh - b * Hv, hk = hv / (Hv / Hk), t0 = n * kTile;
     mbar_expect_tx(bar_tma, 6 * 8192);
-    tma_load_4d(sbase + kOffKQ, &tm_k, bar_tma, 0, hk, t0, b);
-    tma_load_4d(sbase + kOffKQ + 16384, &tm_k, bar_tma, 64, hk, t0, b);
-    tma_load_4d(sbase + kOffKQ + 8192, &tm_q, bar_tma, 0, hk, t0, b);
-    tma_load_4d(sbase + kOffKQ + 24576, &tm_q, bar_tma, 64, hk, t0, b);
-    tma_load_4d(sbase + kOffV, &tm_v, bar_tma, 0, hv, t0, b);
-    tma_load_4d(sbase + kOffV + 8192, &tm_v, bar_tma, 64, hv, t0, b);
+    tma_load_4d(sbase + kOffKQ, P.tm_k, bar_tma, 0, hk, t0, b);
+    tma_load_4d(sbase + kOffKQ + 16384, P.tm_k, bar_tma, 64, hk, t0, b);
+    tma_load_4d(sbase + kOffV, P.tm_v, bar_tma, 0, hv, t0, b);
+    tma_load_4d(sbase + kOffV + 8192, P.tm_v, bar_tma, 64, hv, t0, b);
+  };
+  auto load_q = [&](int lin) {
+    const int bh = head_of(lin), n = tile_of(lin);
+    const int b = bh / Hv, hv = bh - b * Hv, hk = hv / (Hv / Hk), t0 = n * kTile;
+    tma_load_4d(sbase + kOffKQ + 8192, P.tm_q, bar_tma, 0, hk, t0, b);
+    tma_load_4d(sbase + kOffKQ + 24576, P.tm_q, bar_tma, 64, hk, t0, b);
+  };
+  // Gate and beta of token `tid` of a tile, read one tile ahead into registers
+  // as raw bf16 bits (converted when used, so the load is not waited for here).
+  uint16_t g_next = 0x3f80, b_next = 0;  // 1.0 and 0.0
+  auto load_gates = [&](int lin) {
+    g_next = 0x3f80;
+    b_next = 0;
+    if (tid < 64 && lin < total) {
+      const int bh = head_of(lin), n = tile_of(lin);
+      const int b = bh / Hv, hv = bh - b * Hv, tok = n * kTile + tid;
+      if (tok < T) {
+        const size_t gi = ((size_t)b * T + tok) * Hv + hv;
+        b_next = reinterpret_cast<const uint16_t*>(beta)[gi];
+        g_next = reinterpret_cast<const uint16_t*>(g)[gi];
+      }
+    }
+  };
+  auto bits_to_f32 = [](uint16_t x) { return __uint_as_float((uint32_t)x << 16); };
+  if (gid < total && tid == 0) {
+    prefetch_tmap(P.tm_k);
+    prefetch_tmap(P.tm_q);
+    prefetch_tmap(P.tm_v);
+    load_kv(gid);
+    load_q(gid);
   }
+  load_gates(gid);
+
+  bool ok = true;
+  bool tma_pending = gid < total;  // a load phase was issued and not yet waited for
+  size_t unpublished = ~(size_t)0;  // tile whose stores are issued but whose flag is not set
+  // Thread 0: once this thread's stores of the finished tile have completed,
+  // release its flag.
+  auto publish = [&]() {
+    if (flags && unpublished != ~(size_t)0) {
+      bulk_wait_all();
+      fence_proxy_async_global();
+      __threadfence();
+      st_release_gpu(flags + unpublished, 1);
+    }
+    unpublished = ~(size_t)0;
+  };
+  uint32_t mma_phase = 0;          // completions of bar_mma so far
+  int it = 0;
+  for (int lin = gid; lin < total && ok; lin += ngroups, ++it) {
+  const size_t tile_id = (size_t)head_of(lin) * NT + tile_of(lin);
+  const int next = lin + ngroups;
+  const float gv_cur = bits_to_f32(g_next), bt_cur = bits_to_f32(b_next);
+  load_gates(next);
 
   // Gates (step 2).  Padded tokens take g = 1, beta = 0.  Decay products are
   // carried as chunk-local prefix sums lam of log2 g: G_t = 2^lam_t and
@@ -330,11 +425,8 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   // inside a block it is 2^(lam_t - lam_j) directly.
   if (tid < 64) {
     const int t = tid, lane = tid & 31;
-    const int tok = t0 + t;
-    const bool valid = tok < T;
-    const size_t gi = ((size_t)b * T + tok) * Hv + hv;
-    bta[t] = valid ? __bfloat162float(beta[gi]) : 0.f;
-    const float gv = valid ? __bfloat162float(g[gi]) : 1.f;
+    bta[t] = bt_cur;  // padded tokens: g = 1, beta = 0
+    const float gv = gv_cur;
     graw[t] = gv;
     float l = fmaxf(lg2(gv), -1000.f);
     constexpr int kSeg = C < 32 ? C : 32;
@@ -344,12 +436,12 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       if ((lane % kSeg) >= off) l += y;
     }
     if constexpr (C == 64) {
-      if (tid == 31) carry_sh = l;
-      named_bar_sync(1, 64);
-      if (tid >= 32) l += carry_sh;
+      if (tid == 31) carry_sh[grp] = l;
+      named_bar_sync(gates_id, 64);
+      if (tid >= 32) l += carry_sh[grp];
     }
     lam[t] = l;
-    named_bar_sync(1, 64);
+    named_bar_sync(gates_id, 64);
     {  // in-block ratios as products of decays (ferrox-core "The algebra")
       float r = 1.f;
       float* gd = gdiag + t * kLdGd;
@@ -370,7 +462,9 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     if (t == ce) gc[t / C] = ex2(lend);
   }
 
-  bool ok = mbar_wait(bar_tma, 0);
+  ok = mbar_wait(bar_tma, it & 1);
+  tma_pending = false;
+  if (tid == 0 && ok) publish();
   // G1: D[128 x 64] = [K; Q] K^T  (TMEM columns 0..63).
   if (ok && tid == 0) {
     tc_fence_after();
@@ -383,8 +477,9 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     }
     mma_commit(bar_mma);
   }
-  ok = __syncthreads_and(ok);  // also publishes the gate scalars
-  ok = ok && mbar_wait(bar_mma, 0);
+  ok = gsync_and(ok);  // also publishes the gate scalars
+  ok = ok && mbar_wait(bar_mma, mma_phase & 1);
+  ++mma_phase;
   tc_fence_after();
   if (ok) {
     // Row t of KK^T (TMEM lanes 0..63) -> row t of X = L (step 4):
@@ -439,16 +534,16 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       }
     }
   }
-  ok = __syncthreads_and(ok);
+  ok = gsync_and(ok);
 
   // Step 4: T_L = (I + L)^-1.  Step 5 needs no second inverse:
   // (I + A)^-1 diag(beta) = diag(beta) (Gam . T_L) for A[t][j] = beta_t Gam[t][j] KK^T[t][j].
-  if (ok) invert_unit_lower<C>(X, TL, Zs, tid);
-  else __syncthreads();
+  if (ok) invert_unit_lower<C>(X, TL, Zs, tid, gsync);
+  else gsync();
 
   // A2 = [T_L; diag(beta) (Gam . T_L)]: 128 rows x 64 K-cols, K-major 128B swizzle.
   if (ok) {
-    for (int idx = tid; idx < 128 * 8; idx += kPrepThreads) {
+    for (int idx = tid; idx < 128 * 8; idx += kPrepGroupThreads) {
       const int row = idx >> 3, col0 = (idx & 7) * 8;
       const int t = row & 63;
       const float4 a = *reinterpret_cast<const float4*>(TL + t * kLdX + col0);
@@ -481,7 +576,7 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     }
     fence_proxy_async();
   }
-  ok = __syncthreads_and(ok);
+  ok = gsync_and(ok);
 
   // G2: D2a = A2 K (cols 0..127; rows 0..63 = P = T_L K) and
   //     D2b = A2 V (cols 128..255; rows 64..127 = U = T_A (beta V)).
@@ -502,7 +597,8 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     }
     mma_commit(bar_mma);
   }
-  ok = ok && mbar_wait(bar_mma, 1);
+  ok = ok && mbar_wait(bar_mma, mma_phase & 1);
+  ++mma_phase;
   tc_fence_after();
 
   if (ok) {
@@ -537,23 +633,20 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     }
   }
   if (ok) fence_proxy_async();
-  ok = __syncthreads_and(ok);
+  ok = gsync_and(ok);
   if (ok && tid == 0) {
     const int row0 = (int)(tile_id * 128);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
 #pragma unroll
       for (int c = 0; c < 64 / C; ++c)  // Pt rows of chunk c
-        tma_store_2d(&tm_a1s, sbase + kOffKQ + h * 16384 + c * C * 128, 64 * h,
+        tma_store_2d(P.tm_a1s, sbase + kOffKQ + h * 16384 + c * C * 128, 64 * h,
                      row0 + 2 * C * c);
-      tma_store_2d(&tm_uys, sbase + kOffV + h * 8192, 64 * h, row0);  // Ut rows
+      tma_store_2d(P.tm_uys, sbase + kOffV + h * 8192, 64 * h, row0);  // Ut rows
     }
     bulk_commit();
-  }
-
-  // G3: D3a = A3 P (cols 0..127; rows 0..63 = G M P),
-  //     D3b = A3 U (cols 128..255; rows 64..127 = y_loc).
-  if (ok && tid == 0) {
+    // G3: D3a = A3 P (cols 0..127; rows 0..63 = G M P),
+    //     D3b = A3 U (cols 128..255; rows 64..127 = y_loc).
     tc_fence_after();
     const uint32_t id3 = idesc_bf16(128, 128, false, true);
 #pragma unroll
@@ -571,7 +664,8 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     }
     mma_commit(bar_mma);
   }
-  ok = ok && mbar_wait(bar_mma, 0);
+  ok = ok && mbar_wait(bar_mma, mma_phase & 1);
+  ++mma_phase;
   tc_fence_after();
 
   if (ok) {
@@ -596,6 +690,9 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         unpack8(*reinterpret_cast<const uint4*>(qa + sw128(t, (col & 63) + 8)), q + 8);
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] = gt * q[j] - v[j];
+      } else if (P.tm_y) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] *= P.yscale;
       }
       const uint32_t hs = stage + (col >> 6) * 8192;
       st_sm16(sm, hs + sw128(t, col & 63), pack8(v));
@@ -604,24 +701,59 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   }
   if (ok && tid < 64 / C) wsGC[tile_id * 4 + tid] = gc[tid];
   if (ok) fence_proxy_async();
-  ok = __syncthreads_and(ok);
+  ok = gsync_and(ok);
   if (ok && tid == 0) {
     const int row0 = (int)(tile_id * 128);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
 #pragma unroll
       for (int c = 0; c < 64 / C; ++c)  // Qh rows of chunk c
-        tma_store_2d(&tm_a1s, sbase + kOffA3 + h * 8192 + c * C * 128, 64 * h,
+        tma_store_2d(P.tm_a1s, sbase + kOffA3 + h * 8192 + c * C * 128, 64 * h,
                      row0 + 2 * C * c + C);
-      tma_store_2d(&tm_uys, sbase + kOffB + h * 8192, 64 * h, row0 + 64);  // y_loc rows
+      if (P.tm_y) {  // y_loc / sqrt(Dk) into y (rows past T are clipped)
+        const int bh = head_of(lin), b = bh / Hv;
+        tma_store_4d(P.tm_y, sbase + kOffB + h * 8192, 64 * h, bh - b * Hv, tile_of(lin) * kTile,
+                     b);
+      } else {
+        tma_store_2d(P.tm_uys, sbase + kOffB + h * 8192, 64 * h, row0 + 64);  // y_loc rows
+      }
     }
     bulk_commit();
-    bulk_wait_read_all();  // the staging must stay valid until the stores have read it
+    unpublished = tile_id;
   }
+  if (tid == 0) {
+    // Every staging region must be read by the stores before the next tile
+    // reuses it; then the next tile's K, Q and V are loaded (Q was last read
+    // by the epilogue above, K and V by G2).
+    bulk_wait_read_all();
+    if (ok && next < total) {
+      load_kv(next);
+      load_q(next);
+      tma_pending = true;
+    }
+  }
+  ok = gsync_and(ok);
+  }  // tile loop
 
+  if (tid == 0 && ok) publish();
+  // A group that stopped early lets its last prefetch land before the CTA exits.
+  if (tid == 0 && tma_pending) mbar_wait(bar_tma, it & 1);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  if (threadIdx.x < 32) tmem_dealloc(tmem_base_sh, 256 * kPrepGroups);
+}
+
+template <int C>
+__global__ void __launch_bounds__(kPrepThreads, 1)
+prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_a1s,
+               const __grid_constant__ CUtensorMap tm_uys, const bf16* __restrict__ g,
+               const bf16* __restrict__ beta, float* __restrict__ wsGC, int T, int Hk, int Hv,
+               int NT, int BH) {
+  extern __shared__ uint8_t smem_raw[];
+  const PrepParams P{&tm_k, &tm_q, &tm_v, &tm_a1s, &tm_uys, g, beta, wsGC, T, Hk, Hv, NT, BH,
+                     nullptr, 0.f};
+  prep_role<C>(P, smem_raw, blockIdx.x, gridDim.x, nullptr);
 }
 
 // ============================================================================
@@ -937,6 +1069,379 @@ scan_tc_kernel(const __grid_constant__ CUtensorMap tm_a1, const __grid_constant_
 }
 
 // ============================================================================
+// fused prefill: prep and scan in one cooperative launch
+// ============================================================================
+// One CTA per SM.  CTAs 0 .. BH-1 each run the scan of one (b, hv) head over
+// all 128 value rows; the others run prep_role in both of their groups and
+// publish every finished tile through a flag in the workspace.  A scan CTA
+// waits for a tile's flag before loading it, so the scan of chunk n overlaps
+// the prep of later chunks.  Prep never waits for the scan and the launch is
+// cooperative (every CTA resident), so each wait ends.
+//
+// The scan role is the chunk update of scan_tc_kernel at R = 128:
+//   D = K^T Ut;  D += (-M^T) S^T;  Y = Qh S^T;  S <- G_C S + D^T,
+// with M^T = K^T Pt of chunk j+1 and D = K^T Ut of chunk j issued while the
+// state group finishes chunk j-1.  One S operand buffer: the state group
+// overwrites it only after Y of the chunk has completed.
+constexpr int kFusedThreads = kPrepThreads;  // 16 warps
+
+// Two rings of tile buffers: the MN ring (Pt, K, Ut: read by K^T [Pt | Ut],
+// released as soon as those products finish) and the Q ring (Qh, later the
+// staging of y; released after the y reduction has read it).
+struct Scan128Smem {
+  static constexpr uint32_t kOffP = 0;              // Pt, 2 x 64 rows x 128 B
+  static constexpr uint32_t kOffK = 16384;          // K,  2 x 64 rows x 128 B
+  static constexpr uint32_t kOffU = 32768;          // Ut, 2 x 64 rows x 128 B
+  static constexpr uint32_t kMN = 49152;
+  static constexpr uint32_t kQ = 16384;             // Qh, 2 x 64 rows x 128 B
+  static constexpr int kStages = 3;                 // per ring
+  static constexpr uint32_t kOffQ = kStages * kMN;
+  static constexpr uint32_t kOffS = kOffQ + kStages * kQ;  // S operand: 2 x 128 k-rows x 128 B
+  static constexpr uint32_t kOffGC = kOffS + 32768;        // G_C per Q stage (fp32 x 4)
+  static constexpr uint32_t kTotal = kOffGC + kStages * 16 + 1024;
+};
+constexpr uint32_t kFusedSmem = Scan128Smem::kTotal > kPrepSmem ? Scan128Smem::kTotal : kPrepSmem;
+
+enum : int {
+  kQFullMN = 0,
+  kQEmptyMN = kQFullMN + Scan128Smem::kStages,  // MMA commit
+  kQFullQ = kQEmptyMN + Scan128Smem::kStages,
+  kQEmptyQ = kQFullQ + Scan128Smem::kStages,    // 257: state group + the y-reducing thread
+  kQDs = kQEmptyQ + Scan128Smem::kStages,
+  kQY,
+  kQM,                 // [2]
+  kQSop = kQM + 2,     // 256
+  kQDsFree,            // 256
+  kQMt,                // [2] 128
+  kQYFree = kQMt + 2,  // 128
+  kQYStaged,           // 128: Y of the chunk staged for the reduction
+  kQFin,
+  kNumQBars
+};
+
+template <int C>
+__device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CUtensorMap* tm_k,
+                                             const CUtensorMap* tm_uy, const CUtensorMap* tm_yred,
+                                             const float* wsGC, const int* flags,
+                                             const float* state_in, float* state_out, int T,
+                                             int Hk, int Hv, int NT, int bh, float scale,
+                                             uint8_t* smem_raw) {
+  using SM = Scan128Smem;
+  constexpr int kCt = kTile / C;
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~(uintptr_t)1023);
+  __shared__ uint64_t qbars[kNumQBars];
+  __shared__ uint32_t qtmem_sh;
+  const uint32_t sbase = smem_u32(sm);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = bh / Hv, hv = bh - b * Hv, hk = hv / (Hv / Hk);
+  const int NC = (T + C - 1) / C;
+  auto bar = [&](int i) { return smem_u32(&qbars[i]); };
+
+  if (tid == 0) {
+    for (int s = 0; s < SM::kStages; ++s) {
+      mbar_init(bar(kQFullMN + s), 1);
+      mbar_init(bar(kQEmptyMN + s), 1);
+      mbar_init(bar(kQFullQ + s), 1);
+      mbar_init(bar(kQEmptyQ + s), 257);
+    }
+    mbar_init(bar(kQDs), 1);
+    mbar_init(bar(kQY), 1);
+    mbar_init(bar(kQM), 1);
+    mbar_init(bar(kQM + 1), 1);
+    mbar_init(bar(kQSop), 256);
+    mbar_init(bar(kQDsFree), 256);
+    mbar_init(bar(kQMt), 128);
+    mbar_init(bar(kQMt + 1), 128);
+    mbar_init(bar(kQYFree), 128);
+    mbar_init(bar(kQYStaged), 128);
+    mbar_init(bar(kQFin), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&qtmem_sh), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = qtmem_sh;
+  const uint32_t tD = tmem, tY = tmem + 384;
+  auto tM = [&](int x) { return tmem + 128 + 128 * x; };  // fp32 M^T; cols 0-63 then -M^T bf16
+  const uint32_t sS = sbase + SM::kOffS;
+  auto ring_of = [&](int j) { return (j / kCt) % SM::kStages; };
+  auto mn_addr = [&](int j) { return sbase + ring_of(j) * SM::kMN; };
+  auto q_addr = [&](int j) { return sbase + SM::kOffQ + ring_of(j) * SM::kQ; };
+  auto last_of_tile = [&](int j) { return (j % kCt) == kCt - 1 || j == NC - 1; };
+  auto wait_mn = [&](int j) {
+    const int n = j / kCt;
+    return mbar_wait(bar(kQFullMN + n % SM::kStages), (n / SM::kStages) & 1);
+  };
+  auto wait_q = [&](int j) {
+    const int n = j / kCt;
+    return mbar_wait(bar(kQFullQ + n % SM::kStages), (n / SM::kStages) & 1);
+  };
+
+  if ((warp == 0 || warp == 14) && lane == 0) {
+    // ---------------------- producers (MN ring, Q ring) ----------------------
+    const bool mn = warp == 0;
+    const int full0 = mn ? kQFullMN : kQFullQ, empty0 = mn ? kQEmptyMN : kQEmptyQ;
+    prefetch_tmap(tm_a1c);
+    if (mn) {
+      prefetch_tmap(tm_k);
+      prefetch_tmap(tm_uy);
+    }
+    int n = 0;
+    for (; n < NT; ++n) {
+      const int s = n % SM::kStages;
+      if (n >= SM::kStages && !mbar_wait(bar(empty0 + s), ((n / SM::kStages) - 1) & 1)) break;
+      const size_t tid_ws = (size_t)bh * NT + n;
+      if (flags) {
+        if (!wait_flag(flags + tid_ws)) break;
+        fence_proxy_async_global();
+      }
+      const uint32_t fb = bar(full0 + s);
+      const int row = (int)(tid_ws * 128);
+      if (mn) {
+        const uint32_t st = sbase + s * SM::kMN;
+        mbar_expect_tx(fb, SM::kMN);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int c = 0; c < kCt; ++c)  // Pt rows of chunk c
+            tma_load_2d(st + SM::kOffP + h * 8192 + c * C * 128, tm_a1c, fb, 64 * h,
+                        row + 2 * C * c);
+          tma_load_4d(st + SM::kOffK + h * 8192, tm_k, fb, 64 * h, hk, n * kTile, b);
+          tma_load_2d(st + SM::kOffU + h * 8192, tm_uy, fb, 64 * h, row);
+        }
+      } else {
+        const uint32_t st = sbase + SM::kOffQ + s * SM::kQ;
+        mbar_expect_tx(fb, SM::kQ + 16);
+        bulk_load(sbase + SM::kOffGC + 16 * s, wsGC + tid_ws * 4, 16, fb);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int c = 0; c < kCt; ++c)  // Qh rows of chunk c
+            tma_load_2d(st + h * 8192 + c * C * 128, tm_a1c, fb, 64 * h, row + 2 * C * c + C);
+        }
+      }
+    }
+    for (int m = (n > SM::kStages ? n - SM::kStages : 0); m < n; ++m)
+      mbar_wait(bar(full0 + m % SM::kStages), (m / SM::kStages) & 1);
+  } else if (warp == 1) {
+    // ---------------------------- MMA issuer -----------------------------
+    if (lane == 0) {
+      const uint32_t id_kt = idesc_bf16(128, 128, true, true);   // K^T x (Pt | Ut)
+      const uint32_t id_s = idesc_bf16(128, 128, false, true);   // (-M^T) x S^T
+      const uint32_t id_y = idesc_bf16(64, 128, false, true);    // Qh x S^T
+      bool ok = true;
+      // M^T of chunk j into tM(j & 1), once its tile's MN buffers have landed.
+      auto issue_mt = [&](int j) {
+        if (j % kCt == 0) {
+          if (!wait_mn(j)) return false;
+          tc_fence_after();
+        }
+        const uint32_t st = mn_addr(j);
+        const int c = j % kCt;
+#pragma unroll
+        for (int kk = 0; kk < C / 16; ++kk)
+          mma_bf16_ss(tM(j & 1),
+                      smem_desc(st + SM::kOffK + (c * C + 16 * kk) * 128, 8192, 1024, kSw128),
+                      smem_desc(st + SM::kOffP + (c * C + 16 * kk) * 128, 8192, 1024, kSw128),
+                      id_kt, kk > 0);
+        mma_commit(bar(kQM + (j & 1)));
+        return true;
+      };
+      if (NC > 0) ok = issue_mt(0);
+      for (int j = 0; j < NC && ok; ++j) {
+        const int c = j % kCt;
+        const uint32_t st = mn_addr(j);
+        // D = K^T Ut once chunk j-1's D has been read; then M^T of chunk j+1.
+        if (j > 0 && !(ok = mbar_wait(bar(kQDsFree), (j - 1) & 1))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < C / 16; ++kk)
+          mma_bf16_ss(tD,
+                      smem_desc(st + SM::kOffK + (c * C + 16 * kk) * 128, 8192, 1024, kSw128),
+                      smem_desc(st + SM::kOffU + (c * C + 16 * kk) * 128, 8192, 1024, kSw128),
+                      id_kt, kk > 0);
+        // The tile's MN buffers are free once its last products finish.
+        if (last_of_tile(j)) mma_commit(bar(kQEmptyMN + ring_of(j)));
+        if (j + 1 < NC && !(ok = issue_mt(j + 1))) break;
+        // D += (-M^T) S^T   (the serial step)
+        if (!(ok = mbar_wait(bar(kQSop), j & 1))) break;
+        if (!(ok = mbar_wait(bar(kQMt + (j & 1)), (j >> 1) & 1))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ts(tD, tM(j & 1) + 8 * kk, smem_desc(sS + kk * 2048, 16384, 1024, kSw128),
+                      id_s, 1);
+        mma_commit(bar(kQDs));
+        // Y = Qh S^T
+        if (c == 0 && !(ok = wait_q(j))) break;
+        if (j > 0 && !(ok = mbar_wait(bar(kQYFree), (j - 1) & 1))) break;
+        tc_fence_after();
+        const uint32_t qa = q_addr(j) + c * C * 128;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ss(tY, smem_desc(qa + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024, kSw128),
+                      smem_desc(sS + kk * 2048, 16384, 1024, kSw128), id_y, kk > 0);
+        mma_commit(bar(kQY));
+      }
+      mma_commit(bar(kQFin));
+      mbar_wait(bar(kQFin), 0);
+    }
+    __syncwarp();
+  } else if (warp >= 2 && warp < 10) {
+    // ----------------------------- state group ----------------------------
+    // Thread = TMEM lane k (key column); value rows 64h .. 64h+63.
+    const int q = warp & 3, h = (warp - 2) >> 2;
+    const int L = q * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    const size_t sidx = ((size_t)bh * kD + 64 * h) * kD + L;
+    bool ok = true;
+    float s[64];
+#pragma unroll
+    for (int r = 0; r < 64; ++r) s[r] = state_in ? state_in[sidx + (size_t)r * kD] : 0.f;
+    auto write_op = [&]() {
+      uint8_t* row = sm + SM::kOffS + h * 16384;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) st_sm16(row, sw128(L, 8 * ch), pack8(s + 8 * ch));
+      fence_proxy_async();
+      mbar_arrive(bar(kQSop));
+    };
+    write_op();
+    for (int j = 0; j < NC; ++j) {
+      const int c = j % kCt;
+      if (c == 0 && !(ok = wait_q(j))) break;
+      const float Gc = ld_shared_f32(sbase + SM::kOffGC + 16 * ring_of(j) + 4 * c);
+      if (last_of_tile(j)) mbar_arrive(bar(kQEmptyQ + ring_of(j)));
+      if (!(ok = mbar_wait(bar(kQDs), j & 1))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float d[32];
+        tmem_ld32(tD + lane_base + 64 * h + 32 * half, d);
+        tmem_wait_ld();
+#pragma unroll
+        for (int r = 0; r < 32; ++r) s[32 * half + r] = fmaf(Gc, s[32 * half + r], d[r]);
+      }
+      tc_fence_before();
+      mbar_arrive(bar(kQDsFree));
+      if (j + 1 < NC) {
+        // Y of chunk j still reads the S operand.
+        if (!(ok = mbar_wait(bar(kQY), j & 1))) break;
+        write_op();
+      }
+    }
+    if (ok) {
+#pragma unroll
+      for (int r = 0; r < 64; ++r) state_out[sidx + (size_t)r * kD] = s[r];
+    }
+  } else if (warp >= 10 && warp < 14) {
+    // ------------------------------ aux group -----------------------------
+    const int qd = warp & 3;
+    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+    bool ok = true;
+    auto convert = [&](int j) {
+      if (!mbar_wait(bar(kQM + (j & 1)), (j >> 1) & 1)) return false;
+      tc_fence_after();
+      const uint32_t tb = tM(j & 1) + lane_base;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float v[64];
+        tmem_ld32(tb + 64 * hh, v);
+        tmem_ld32(tb + 64 * hh + 32, v + 32);
+        tmem_wait_ld();
+        uint32_t p[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) p[i] = pack_bf16x2(-v[2 * i], -v[2 * i + 1]);
+        tmem_st32(tb + 32 * hh, p);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(kQMt + (j & 1)));
+      return true;
+    };
+    if (NC > 0) ok = convert(0);
+    for (int j = 0; j < NC && ok; ++j) {
+      const int c = j % kCt;
+      if (j + 1 < NC && !(ok = convert(j + 1))) break;
+      // M = 64 result: row 16*qd + i in lane 32*qd + i, i < 16; 128 value columns.
+      // Y / sqrt(Dk) goes, as bf16, into this chunk's Qh rows (dead once Y is
+      // complete) and is added to y (which holds y_loc / sqrt(Dk)) by a TMA
+      // reduction.
+      const int t = 16 * qd + lane;
+      const bool live = lane < 16 && t < C;
+      const uint32_t qst = q_addr(j);
+      const int qrow = c * C + t;
+      if (!(ok = mbar_wait(bar(kQY), j & 1))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {  // 32 value columns at a time
+        float d[32];
+        tmem_ld32(tY + lane_base + 32 * qq, d);
+        tmem_wait_ld();
+        if (qq == 3) {
+          tc_fence_before();
+          mbar_arrive(bar(kQYFree));
+        }
+        if (live) {
+          uint8_t* hbase = sm + (qst - sbase) + (qq >> 1) * 8192;
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            float y8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y8[e] = d[8 * ch + e] * scale;
+            st_sm16(hbase, sw128(qrow, (qq & 1) * 32 + 8 * ch), pack8(y8));
+          }
+        }
+      }
+      fence_proxy_async();
+      mbar_arrive(bar(kQYStaged));
+      if (warp == 10 && lane == 0) {
+        if (!(ok = mbar_wait(bar(kQYStaged), j & 1))) break;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+          tma_reduce_add_4d(tm_yred, qst + hh * 8192 + c * C * 128, 64 * hh, hv, j * C, b);
+        bulk_commit();
+        bulk_wait_read_all();  // the Q buffers may be refilled once the reduction has read them
+        if (last_of_tile(j)) mbar_arrive(bar(kQEmptyQ + ring_of(j)));
+      }
+    }
+    if (warp == 10 && lane == 0) bulk_wait_all();
+  }
+  // warp 15 and the idle lanes of warps 0 and 14 have no scan work
+  tc_fence_before();
+  if (warp != 0 && warp != 14) named_bar_sync(1, kFusedThreads - 64);
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+template <int C>
+__global__ void __launch_bounds__(kFusedThreads, 1)
+fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_a1s,
+                     const __grid_constant__ CUtensorMap tm_uys,
+                     const __grid_constant__ CUtensorMap tm_a1,
+                     const __grid_constant__ CUtensorMap tm_y,
+                     const __grid_constant__ CUtensorMap tm_yred, const bf16* __restrict__ g,
+                     const bf16* __restrict__ beta, float* __restrict__ wsGC, int* flags,
+                     const float* state_in, float* state_out, int T, int Hk, int Hv, int NT,
+                     int BH, float scale) {
+  extern __shared__ uint8_t smem_raw[];
+  if ((int)blockIdx.x < BH) {
+    scan_role128<C>(&tm_a1s, &tm_k, &tm_uys, &tm_yred, wsGC, flags, state_in, state_out, T, Hk,
+                    Hv, NT, blockIdx.x, scale, smem_raw);
+  } else {
+    const PrepParams P{&tm_k, &tm_q, &tm_v, &tm_a1s, &tm_uys, g, beta, wsGC, T, Hk, Hv, NT, BH,
+                       &tm_y, scale};
+    prep_role<C>(P, smem_raw, blockIdx.x - BH, gridDim.x - BH, flags);
+  }
+}
+
+// ============================================================================
 // host side
 // ============================================================================
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -959,11 +1464,11 @@ EncodeTiledFn encode_fn() {
 }
 
 // [B, T, H, 128] bf16 -> box {64 cols, 1 head, 64 tokens, 1 batch}, 128B swizzle.
-bool make_bthd_map(CUtensorMap* m, const void* base, int B, int T, int H) {
+bool make_bthd_map(CUtensorMap* m, const void* base, int B, int T, int H, int box_t = kTile) {
   const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
   const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2,
                                  (cuuint64_t)T * H * kD * 2};
-  const cuuint32_t box[4] = {64, 1, kTile, 1};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)box_t, 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
                      strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -990,6 +1495,19 @@ bool make_rows_map(CUtensorMap* m, const void* base, size_t rows, int box_cols, 
 
 constexpr int kScanRows = 32;
 
+// Streaming multiprocessors of the current device (cached per device).
+int num_sms() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 1;
+  }
+  return cache[dev];
+}
+
 template <int C>
 cudaError_t launch_c(const PrefillArgs& a) {
   const int NT = (a.T + kTile - 1) / kTile;
@@ -1011,23 +1529,53 @@ cudaError_t launch_c(const PrefillArgs& a) {
       !make_rows_map(&tuys, wsUY, (size_t)BH * NT * 128, 64, 64, true))
     return cudaErrorInvalidValue;
 
-  cudaError_t e = cudaFuncSetAttribute(prep_tc_kernel<C>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
+  const float scale = 1.0f / sqrtf((float)kD);
+  const int sms = num_sms();
+  cudaError_t e;
+  // Fused path: one scan CTA per head next to at least two thirds of the SMs
+  // doing prep, in one cooperative launch.
+  if (3 * BH <= sms) {
+    int* flags = reinterpret_cast<int*>(ws + w.flags);
+    CUtensorMap ty, tyred;
+    if (!make_bthd_map(&ty, a.y, a.B, a.T, a.Hv) || !make_bthd_map(&tyred, a.y, a.B, a.T, a.Hv, C))
+      return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(fused_prefill_kernel<C>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kFusedSmem);
+    if (e == cudaSuccess) e = cudaMemsetAsync(flags, 0, (size_t)BH * NT * sizeof(int), a.stream);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sms);
+    cfg.blockDim = dim3(kFusedThreads);
+    cfg.dynamicSmemBytes = kFusedSmem;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fused_prefill_kernel<C>, tk, tq, tv, ta1s, tuys, ta1, ty,
+                              tyred, static_cast<const bf16*>(a.g),
+                              static_cast<const bf16*>(a.beta), wsGC, flags, a.state_in,
+                              a.state_out, a.T, a.Hk, a.Hv, NT, BH, scale);
+  }
+
+  // Split path: the persistent prep kernel, then the scan (R value rows per CTA).
+  e = cudaFuncSetAttribute(prep_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kPrepSmem);
   if (e != cudaSuccess) return e;
   using SM = ScanSmem<kScanRows>;
   e = cudaFuncSetAttribute(scan_tc_kernel<C, kScanRows>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kTotal);
   if (e != cudaSuccess) return e;
-
-  prep_tc_kernel<C><<<dim3(NT, BH), kPrepThreads, kPrepSmem, a.stream>>>(
+  const int prep_ctas = std::min(sms, (BH * NT + kPrepGroups - 1) / kPrepGroups);
+  prep_tc_kernel<C><<<prep_ctas, kPrepThreads, kPrepSmem, a.stream>>>(
       tk, tq, tv, ta1s, tuys, static_cast<const bf16*>(a.g), static_cast<const bf16*>(a.beta),
-      wsGC, a.T, a.Hk, a.Hv, NT);
+      wsGC, a.T, a.Hk, a.Hv, NT, BH);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const float scale = 1.0f / sqrtf((float)kD);
   scan_tc_kernel<C, kScanRows><<<dim3(kD / kScanRows, BH), kScanThreads, SM::kTotal, a.stream>>>(
-      ta1, tk, tuc, tuy, wsGC, a.state_in, a.state_out, static_cast<bf16*>(a.y), a.T, a.Hk, a.Hv, NT,
-      scale);
+      ta1, tk, tuc, tuy, wsGC, a.state_in, a.state_out, static_cast<bf16*>(a.y), a.T, a.Hk, a.Hv,
+      NT, scale);
   return cudaGetLastError();
 }
 

@@ -114,6 +114,23 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src,
       "r"(src), "r"(c0), "r"(c1)
       : "memory");
 }
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* m, uint32_t src, int c0, int c1,
+                                             int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+// Element-wise add of a shared-memory tile into global memory (in L2).
+__device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap* m, uint32_t src, int c0,
+                                                  int c1, int c2, int c3) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4, %5}], [%1];" ::"l"(reinterpret_cast<uint64_t>(m)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -126,6 +143,39 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 // Generic-proxy shared-memory writes -> visible to the async proxy (MMA/TMA).
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Orders this thread's generic-proxy accesses to global memory against its
+// async-proxy (TMA) accesses, in both directions.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// Waits until every bulk async-group of this thread has completed (writes
+// performed, not only source reads).
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Bounded wait for a flag another CTA sets with st_release_gpu; on timeout it
+// records kErrWaitTimeout and returns false.
+__device__ __forceinline__ bool wait_flag(const int* p) {
+  if (ld_acquire_gpu(p) != 0) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    __nanosleep(128);
+    if (ld_acquire_gpu(p) != 0) return true;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      atomicExch(&g_device_error, kErrWaitTimeout);
+      return false;
+    }
+  }
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int count) {

@@ -28,6 +28,8 @@ SMALL = [
     (1, 200, 2, 2, 64, F32, 0.5),
     (3, 70, 1, 3, 32, F32, 1.0),
     (1, 64, 1, 2, 64, BF16, 5.0),    # fast decay: G underflows inside a chunk
+    (2, 100, 16, 32, 64, BF16, 0.3), # B*Hv = 64 heads: the split prep + scan launches
+    (1, 150, 8, 48, 32, BF16, 0.3),  # 48 heads, GQA 6:1: the fused launch at its widest
 ]
 
 
