@@ -271,6 +271,9 @@ __device__ void invert_unit_lower(const float* X, float* Tm, float* Zs, int u, S
 
 // Everything the prep work needs (the tensor maps are kernel parameters).
 struct PrepParams {
+  const bf16* k;  // the raw inputs, for L2 prefetches
+  const bf16* q;
+  const bf16* v;
   const CUtensorMap* tm_k;
   const CUtensorMap* tm_q;
   const CUtensorMap* tm_v;
@@ -352,21 +355,26 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
   const int gid = cta_rank * kPrepGroups + grp;
   auto head_of = [&](int lin) { return lin % BH; };
   auto tile_of = [&](int lin) { return lin / BH; };
-  // TMA loads of a tile's K and V (with the byte count of K, Q and V) and of its Q.
+  // The group's TMA traffic is spread over four threads (lane 0 of warps 4-7),
+  // since one thread issues these instructions slowly.  I/O thread `io`
+  // owns one 64-column half: io 0/1 load K and Q half io and store the Pt and
+  // Qh halves staged over K; io 2/3 load V half io-2 and store the Ut and y_loc
+  // halves staged over V.  Each waits for its own stores before reloading the
+  // region they read.  io 0 posts the byte count of the whole tile.
+  const int io = (warp >= 4 && (tid & 31) == 0) ? warp - 4 : -1;
+  // K and V of tile `lin` (io 0 also posts the byte count of K, Q and V) ...
   auto load_kv = [&](int lin) {
     const int bh = head_of(lin), n = tile_of(lin);
     const int b = bh / Hv, hv = bh - b * Hv, hk = hv / (Hv / Hk), t0 = n * kTile;
-    mbar_expect_tx(bar_tma, 6 * 8192);
-    tma_load_4d(sbase + kOffKQ, P.tm_k, bar_tma, 0, hk, t0, b);
-    tma_load_4d(sbase + kOffKQ + 16384, P.tm_k, bar_tma, 64, hk, t0, b);
-    tma_load_4d(sbase + kOffV, P.tm_v, bar_tma, 0, hv, t0, b);
-    tma_load_4d(sbase + kOffV + 8192, P.tm_v, bar_tma, 64, hv, t0, b);
+    if (io == 0) mbar_expect_tx(bar_tma, 6 * 8192);
+    if (io < 2) tma_load_4d(sbase + kOffKQ + io * 16384, P.tm_k, bar_tma, 64 * io, hk, t0, b);
+    else tma_load_4d(sbase + kOffV + (io - 2) * 8192, P.tm_v, bar_tma, 64 * (io - 2), hv, t0, b);
   };
+  // ... and its Q (io 0 and 1).
   auto load_q = [&](int lin) {
     const int bh = head_of(lin), n = tile_of(lin);
     const int b = bh / Hv, hv = bh - b * Hv, hk = hv / (Hv / Hk), t0 = n * kTile;
-    tma_load_4d(sbase + kOffKQ + 8192, P.tm_q, bar_tma, 0, hk, t0, b);
-    tma_load_4d(sbase + kOffKQ + 24576, P.tm_q, bar_tma, 64, hk, t0, b);
+    if (io < 2) tma_load_4d(sbase + kOffKQ + io * 16384 + 8192, P.tm_q, bar_tma, 64 * io, hk, t0, b);
   };
   // Gate and beta of token `tid` of a tile, read one tile ahead into registers
   // as raw bf16 bits (converted when used, so the load is not waited for here).
@@ -385,10 +393,9 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
     }
   };
   auto bits_to_f32 = [](uint16_t x) { return __uint_as_float((uint32_t)x << 16); };
-  if (gid < total && tid == 0) {
-    prefetch_tmap(P.tm_k);
-    prefetch_tmap(P.tm_q);
-    prefetch_tmap(P.tm_v);
+  if (gid < total && io >= 0) {
+    prefetch_tmap(io < 2 ? P.tm_k : P.tm_v);
+    if (io < 2) prefetch_tmap(P.tm_q);
     load_kv(gid);
     load_q(gid);
   }
@@ -396,13 +403,17 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
 
   bool ok = true;
   bool tma_pending = gid < total;  // a load phase was issued and not yet waited for
-  size_t unpublished = ~(size_t)0;  // tile whose stores are issued but whose flag is not set
-  // Thread 0: once this thread's stores of the finished tile have completed,
-  // release its flag.
-  auto publish = [&]() {
-    if (flags && unpublished != ~(size_t)0) {
+  size_t unpublished = ~(size_t)0;  // io 0: tile whose flag is not yet set
+  // The I/O threads make their stores of the finished tile complete; after a
+  // group barrier io 0 releases the tile's flag.
+  auto stores_complete = [&]() {
+    if (flags && io >= 0) {
       bulk_wait_all();
       fence_proxy_async_global();
+    }
+  };
+  auto publish = [&]() {
+    if (flags && io == 0 && unpublished != ~(size_t)0) {
       __threadfence();
       st_release_gpu(flags + unpublished, 1);
     }
@@ -415,6 +426,20 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
   const int next = lin + ngroups;
   const float gv_cur = bits_to_f32(g_next), bt_cur = bits_to_f32(b_next);
   load_gates(next);
+  if (next < total && tid < 3 * kTile) {
+    // Warm L2 with the next tile's K, Q and V rows (one 256-byte token row of
+    // one tensor per thread, as plain prefetches that leave the TMA unit free).
+    const int nbh = head_of(next), nb = nbh / Hv, nhv = nbh - nb * Hv;
+    const int nhk = nhv / (Hv / Hk), tok = tile_of(next) * kTile + (tid & (kTile - 1));
+    if (tok < T) {
+      const int which = tid / kTile;  // 0: K, 1: Q, 2: V
+      const bf16* base = which == 0 ? P.k : (which == 1 ? P.q : P.v);
+      const int heads = which == 2 ? Hv : Hk, hh = which == 2 ? nhv : nhk;
+      const char* row = reinterpret_cast<const char*>(base + (((size_t)nb * T + tok) * heads + hh) * kD);
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(row) : "memory");
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(row + 128) : "memory");
+    }
+  }
 
   // Gates (step 2).  Padded tokens take g = 1, beta = 0.  Decay products are
   // carried as chunk-local prefix sums lam of log2 g: G_t = 2^lam_t and
@@ -464,9 +489,11 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
 
   ok = mbar_wait(bar_tma, it & 1);
   tma_pending = false;
-  if (tid == 0 && ok) publish();
-  // G1: D[128 x 64] = [K; Q] K^T  (TMEM columns 0..63).
-  if (ok && tid == 0) {
+  // G1: D[128 x 64] = [K; Q] K^T  (TMEM columns 0..63), issued outside the gate
+  // warps.  The previous tile's last stores must have read A3 and X, which
+  // this tile rewrites after G1.
+  if (io >= 0) bulk_wait_read_all();
+  if (ok && tid == 64) {
     tc_fence_after();
     const uint32_t id1 = idesc_bf16(128, 64, false, false);
 #pragma unroll
@@ -534,7 +561,9 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
       }
     }
   }
+  stores_complete();  // the previous tile's stores (long done by now)
   ok = gsync_and(ok);
+  if (ok) publish();
 
   // Step 4: T_L = (I + L)^-1.  Step 5 needs no second inverse:
   // (I + A)^-1 diag(beta) = diag(beta) (Gam . T_L) for A[t][j] = beta_t Gam[t][j] KK^T[t][j].
@@ -634,17 +663,19 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
   }
   if (ok) fence_proxy_async();
   ok = gsync_and(ok);
-  if (ok && tid == 0) {
+  if (ok && io >= 0) {
     const int row0 = (int)(tile_id * 128);
+    if (io < 2) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-#pragma unroll
-      for (int c = 0; c < 64 / C; ++c)  // Pt rows of chunk c
-        tma_store_2d(P.tm_a1s, sbase + kOffKQ + h * 16384 + c * C * 128, 64 * h,
+      for (int c = 0; c < 64 / C; ++c)  // Pt rows of chunk c, half io
+        tma_store_2d(P.tm_a1s, sbase + kOffKQ + io * 16384 + c * C * 128, 64 * io,
                      row0 + 2 * C * c);
-      tma_store_2d(P.tm_uys, sbase + kOffV + h * 8192, 64 * h, row0);  // Ut rows
+    } else {
+      tma_store_2d(P.tm_uys, sbase + kOffV + (io - 2) * 8192, 64 * (io - 2), row0);  // Ut rows
     }
     bulk_commit();
+  }
+  if (ok && tid == 0) {
     // G3: D3a = A3 P (cols 0..127; rows 0..63 = G M P),
     //     D3b = A3 U (cols 128..255; rows 64..127 = y_loc).
     tc_fence_after();
@@ -702,14 +733,15 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
   if (ok && tid < 64 / C) wsGC[tile_id * 4 + tid] = gc[tid];
   if (ok) fence_proxy_async();
   ok = gsync_and(ok);
-  if (ok && tid == 0) {
+  if (ok && io >= 0) {
     const int row0 = (int)(tile_id * 128);
+    if (io < 2) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-#pragma unroll
-      for (int c = 0; c < 64 / C; ++c)  // Qh rows of chunk c
-        tma_store_2d(P.tm_a1s, sbase + kOffA3 + h * 8192 + c * C * 128, 64 * h,
+      for (int c = 0; c < 64 / C; ++c)  // Qh rows of chunk c, half io
+        tma_store_2d(P.tm_a1s, sbase + kOffA3 + io * 8192 + c * C * 128, 64 * io,
                      row0 + 2 * C * c + C);
+    } else {
+      const int h = io - 2;
       if (P.tm_y) {  // y_loc / sqrt(Dk) into y (rows past T are clipped)
         const int bh = head_of(lin), b = bh / Hv;
         tma_store_4d(P.tm_y, sbase + kOffB + h * 8192, 64 * h, bh - b * Hv, tile_of(lin) * kTile,
@@ -719,13 +751,13 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
       }
     }
     bulk_commit();
-    unpublished = tile_id;
+    if (io == 0) unpublished = tile_id;
   }
-  if (tid == 0) {
-    // Every staging region must be read by the stores before the next tile
-    // reuses it; then the next tile's K, Q and V are loaded (Q was last read
-    // by the epilogue above, K and V by G2).
-    bulk_wait_read_all();
+  if (io >= 0) {
+    // The next tile's K, Q and V are loaded once this thread's stores of Pt
+    // or Ut (staged in K and V) have read them; Q was last read by the
+    // epilogue above.  The Qh / y_loc staging is waited for before the next G1.
+    bulk_wait_read<1>();
     if (ok && next < total) {
       load_kv(next);
       load_q(next);
@@ -735,9 +767,12 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
   ok = gsync_and(ok);
   }  // tile loop
 
-  if (tid == 0 && ok) publish();
+  if (io >= 0) bulk_wait_read_all();  // shared memory must outlive the last stores' reads
+  stores_complete();
+  gsync();
+  if (ok) publish();
   // A group that stopped early lets its last prefetch land before the CTA exits.
-  if (tid == 0 && tma_pending) mbar_wait(bar_tma, it & 1);
+  if (io == 0 && tma_pending) mbar_wait(bar_tma, it & 1);
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x < 32) tmem_dealloc(tmem_base_sh, 256 * kPrepGroups);
@@ -747,12 +782,12 @@ template <int C>
 __global__ void __launch_bounds__(kPrepThreads, 1)
 prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_a1s,
-               const __grid_constant__ CUtensorMap tm_uys, const bf16* __restrict__ g,
-               const bf16* __restrict__ beta, float* __restrict__ wsGC, int T, int Hk, int Hv,
-               int NT, int BH) {
+               const __grid_constant__ CUtensorMap tm_uys, const bf16* kin, const bf16* qin,
+               const bf16* vin, const bf16* __restrict__ g, const bf16* __restrict__ beta,
+               float* __restrict__ wsGC, int T, int Hk, int Hv, int NT, int BH) {
   extern __shared__ uint8_t smem_raw[];
-  const PrepParams P{&tm_k, &tm_q, &tm_v, &tm_a1s, &tm_uys, g, beta, wsGC, T, Hk, Hv, NT, BH,
-                     nullptr, 0.f};
+  const PrepParams P{kin, qin, vin, &tm_k, &tm_q, &tm_v, &tm_a1s, &tm_uys, g, beta, wsGC,
+                     T, Hk, Hv, NT, BH, nullptr, 0.f};
   prep_role<C>(P, smem_raw, blockIdx.x, gridDim.x, nullptr);
 }
 
@@ -1233,7 +1268,11 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
     if (lane == 0) {
       const uint32_t id_kt = idesc_bf16(128, 128, true, true);   // K^T x (Pt | Ut)
       const uint32_t id_s = idesc_bf16(128, 128, false, true);   // (-M^T) x S^T
-      const uint32_t id_y = idesc_bf16(64, 128, false, true);    // Qh x S^T
+      const uint32_t id_y = idesc_bf16(128, C, true, false);     // S x Qh^T (rows v, cols t)
+      // Descriptor bases (per ring stage via a byte offset; see SmemDesc).
+      const SmemDesc d_mn_mn = smem_desc_base(sbase, 8192, 1024, kSw128);   // MN-major, 64-row halves
+      const SmemDesc d_s = smem_desc_base(sS, 16384, 1024, kSw128);         // S operand
+      const SmemDesc d_q = smem_desc_base(sbase + SM::kOffQ, 16, 1024, kSw128);  // Qh, K-major
       bool ok = true;
       // M^T of chunk j into tM(j & 1), once its tile's MN buffers have landed.
       auto issue_mt = [&](int j) {
@@ -1241,52 +1280,49 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
           if (!wait_mn(j)) return false;
           tc_fence_after();
         }
-        const uint32_t st = mn_addr(j);
-        const int c = j % kCt;
+        const uint32_t off = ring_of(j) * SM::kMN + (j % kCt) * C * 128;
 #pragma unroll
         for (int kk = 0; kk < C / 16; ++kk)
-          mma_bf16_ss(tM(j & 1),
-                      smem_desc(st + SM::kOffK + (c * C + 16 * kk) * 128, 8192, 1024, kSw128),
-                      smem_desc(st + SM::kOffP + (c * C + 16 * kk) * 128, 8192, 1024, kSw128),
-                      id_kt, kk > 0);
+          mma_bf16_ss(tM(j & 1), smem_desc_at(d_mn_mn, off + SM::kOffK + kk * 2048),
+                      smem_desc_at(d_mn_mn, off + SM::kOffP + kk * 2048), id_kt, kk > 0);
         mma_commit(bar(kQM + (j & 1)));
         return true;
       };
       if (NC > 0) ok = issue_mt(0);
       for (int j = 0; j < NC && ok; ++j) {
         const int c = j % kCt;
-        const uint32_t st = mn_addr(j);
-        // D = K^T Ut once chunk j-1's D has been read; then M^T of chunk j+1.
+        const uint32_t off = ring_of(j) * SM::kMN + c * C * 128;
+        // D = K^T Ut once chunk j-1's D has been read.
         if (j > 0 && !(ok = mbar_wait(bar(kQDsFree), (j - 1) & 1))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < C / 16; ++kk)
-          mma_bf16_ss(tD,
-                      smem_desc(st + SM::kOffK + (c * C + 16 * kk) * 128, 8192, 1024, kSw128),
-                      smem_desc(st + SM::kOffU + (c * C + 16 * kk) * 128, 8192, 1024, kSw128),
-                      id_kt, kk > 0);
+          mma_bf16_ss(tD, smem_desc_at(d_mn_mn, off + SM::kOffK + kk * 2048),
+                      smem_desc_at(d_mn_mn, off + SM::kOffU + kk * 2048), id_kt, kk > 0);
         // The tile's MN buffers are free once its last products finish.
         if (last_of_tile(j)) mma_commit(bar(kQEmptyMN + ring_of(j)));
-        if (j + 1 < NC && !(ok = issue_mt(j + 1))) break;
         // D += (-M^T) S^T   (the serial step)
         if (!(ok = mbar_wait(bar(kQSop), j & 1))) break;
         if (!(ok = mbar_wait(bar(kQMt + (j & 1)), (j >> 1) & 1))) break;
         tc_fence_after();
+        const uint32_t ta = tM(j & 1);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts(tD, tM(j & 1) + 8 * kk, smem_desc(sS + kk * 2048, 16384, 1024, kSw128),
-                      id_s, 1);
+          mma_bf16_ts(tD, ta + 8 * kk, smem_desc_at(d_s, kk * 2048), id_s, 1);
         mma_commit(bar(kQDs));
-        // Y = Qh S^T
+        // Y^T = S Qh^T (A = the S operand read MN-major, B = Qh rows): the state
+        // group rewrites S once it completes.
         if (c == 0 && !(ok = wait_q(j))) break;
         if (j > 0 && !(ok = mbar_wait(bar(kQYFree), (j - 1) & 1))) break;
         tc_fence_after();
-        const uint32_t qa = q_addr(j) + c * C * 128;
+        const uint32_t qoff = ring_of(j) * SM::kQ + c * C * 128;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ss(tY, smem_desc(qa + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024, kSw128),
-                      smem_desc(sS + kk * 2048, 16384, 1024, kSw128), id_y, kk > 0);
+          mma_bf16_ss(tY, smem_desc_at(d_s, kk * 2048),
+                      smem_desc_at(d_q, qoff + (kk >> 2) * 8192 + (kk & 3) * 32), id_y, kk > 0);
         mma_commit(bar(kQY));
+        // M^T of chunk j+1, converted by the aux group while chunk j finishes.
+        if (j + 1 < NC && !(ok = issue_mt(j + 1))) break;
       }
       mma_commit(bar(kQFin));
       mbar_wait(bar(kQFin), 0);
@@ -1367,34 +1403,33 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
     for (int j = 0; j < NC && ok; ++j) {
       const int c = j % kCt;
       if (j + 1 < NC && !(ok = convert(j + 1))) break;
-      // M = 64 result: row 16*qd + i in lane 32*qd + i, i < 16; 128 value columns.
-      // Y / sqrt(Dk) goes, as bf16, into this chunk's Qh rows (dead once Y is
-      // complete) and is added to y (which holds y_loc / sqrt(Dk)) by a TMA
-      // reduction.
-      const int t = 16 * qd + lane;
-      const bool live = lane < 16 && t < C;
+      // Y^T: lane v (value row), columns t < C.  Y / sqrt(Dk) goes, as bf16 and
+      // transposed, into this chunk's Qh rows (dead once Y is complete) and is
+      // added to y (which holds y_loc / sqrt(Dk)) by a TMA reduction.
+      const int v = 32 * qd + lane;
       const uint32_t qst = q_addr(j);
-      const int qrow = c * C + t;
+      uint8_t* hbase = sm + (qst - sbase) + (v >> 6) * 8192;
+      const int vv = v & 63;
       if (!(ok = mbar_wait(bar(kQY), j & 1))) break;
       tc_fence_after();
 #pragma unroll
-      for (int qq = 0; qq < 4; ++qq) {  // 32 value columns at a time
+      for (int t0 = 0; t0 < C; t0 += 32) {
         float d[32];
-        tmem_ld32(tY + lane_base + 32 * qq, d);
+        if constexpr (C >= 32) {
+          tmem_ld32(tY + lane_base + t0, d);
+        } else {
+          tmem_ld16(tY + lane_base + t0, d);
+        }
         tmem_wait_ld();
-        if (qq == 3) {
+        if (t0 + 32 >= C) {
           tc_fence_before();
           mbar_arrive(bar(kQYFree));
         }
-        if (live) {
-          uint8_t* hbase = sm + (qst - sbase) + (qq >> 1) * 8192;
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            float y8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) y8[e] = d[8 * ch + e] * scale;
-            st_sm16(hbase, sw128(qrow, (qq & 1) * 32 + 8 * ch), pack8(y8));
-          }
+        for (int i = 0; i < (C < 32 ? C : 32); ++i) {
+          const int row = c * C + t0 + i;
+          const uint32_t off = row * 128 + ((((vv >> 3) ^ (row & 7))) << 4) + (vv & 7) * 2;
+          *reinterpret_cast<bf16*>(hbase + off) = __float2bfloat16_rn(d[i] * scale);
         }
       }
       fence_proxy_async();
@@ -1426,7 +1461,8 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_uys,
                      const __grid_constant__ CUtensorMap tm_a1,
                      const __grid_constant__ CUtensorMap tm_y,
-                     const __grid_constant__ CUtensorMap tm_yred, const bf16* __restrict__ g,
+                     const __grid_constant__ CUtensorMap tm_yred, const bf16* kin,
+                     const bf16* qin, const bf16* vin, const bf16* __restrict__ g,
                      const bf16* __restrict__ beta, float* __restrict__ wsGC, int* flags,
                      const float* state_in, float* state_out, int T, int Hk, int Hv, int NT,
                      int BH, float scale) {
@@ -1435,8 +1471,8 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_k,
     scan_role128<C>(&tm_a1s, &tm_k, &tm_uys, &tm_yred, wsGC, flags, state_in, state_out, T, Hk,
                     Hv, NT, blockIdx.x, scale, smem_raw);
   } else {
-    const PrepParams P{&tm_k, &tm_q, &tm_v, &tm_a1s, &tm_uys, g, beta, wsGC, T, Hk, Hv, NT, BH,
-                       &tm_y, scale};
+    const PrepParams P{kin, qin, vin, &tm_k, &tm_q, &tm_v, &tm_a1s, &tm_uys, g, beta, wsGC,
+                       T, Hk, Hv, NT, BH, &tm_y, scale};
     prep_role<C>(P, smem_raw, blockIdx.x - BH, gridDim.x - BH, flags);
   }
 }
@@ -1554,7 +1590,8 @@ cudaError_t launch_c(const PrefillArgs& a) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, fused_prefill_kernel<C>, tk, tq, tv, ta1s, tuys, ta1, ty,
-                              tyred, static_cast<const bf16*>(a.g),
+                              tyred, static_cast<const bf16*>(a.k), static_cast<const bf16*>(a.q),
+                              static_cast<const bf16*>(a.v), static_cast<const bf16*>(a.g),
                               static_cast<const bf16*>(a.beta), wsGC, flags, a.state_in,
                               a.state_out, a.T, a.Hk, a.Hv, NT, BH, scale);
   }
@@ -1569,8 +1606,9 @@ cudaError_t launch_c(const PrefillArgs& a) {
   if (e != cudaSuccess) return e;
   const int prep_ctas = std::min(sms, (BH * NT + kPrepGroups - 1) / kPrepGroups);
   prep_tc_kernel<C><<<prep_ctas, kPrepThreads, kPrepSmem, a.stream>>>(
-      tk, tq, tv, ta1s, tuys, static_cast<const bf16*>(a.g), static_cast<const bf16*>(a.beta),
-      wsGC, a.T, a.Hk, a.Hv, NT, BH);
+      tk, tq, tv, ta1s, tuys, static_cast<const bf16*>(a.k), static_cast<const bf16*>(a.q),
+      static_cast<const bf16*>(a.v), static_cast<const bf16*>(a.g),
+      static_cast<const bf16*>(a.beta), wsGC, a.T, a.Hk, a.Hv, NT, BH);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   scan_tc_kernel<C, kScanRows><<<dim3(kD / kScanRows, BH), kScanThreads, SM::kTotal, a.stream>>>(

@@ -97,6 +97,15 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, 
 }
 
 // Non-tensor bulk copy global -> shared (16-byte aligned, size a multiple of 16).
+// Prefetch a tensor box into L2 (no shared-memory destination, no barrier).
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* m, int c0, int c1, int c2,
+                                                int c3) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint32_t bar) {
   asm volatile(
@@ -138,6 +147,11 @@ __device__ __forceinline__ void bulk_commit() {
 // (the global writes complete on their own before the grid does).
 __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Same, but the most recent `N` committed groups may still be reading.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
 // Generic-proxy shared-memory writes -> visible to the async proxy (MMA/TMA).
@@ -294,6 +308,21 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
   d |= (uint64_t)1 << 46;
   d |= (uint64_t)(layout & 7) << 61;
   return d;
+}
+
+// A shared-memory descriptor split in 32-bit halves, so that a descriptor at
+// a byte offset from its base costs one add (the start address field, bits
+// 0-13, holds addr >> 4 and smem addresses stay below 256 KB: no carry).
+struct SmemDesc {
+  uint32_t lo, hi;
+};
+__device__ __forceinline__ SmemDesc smem_desc_base(uint32_t addr, uint32_t lbo, uint32_t sbo,
+                                                   uint32_t layout) {
+  const uint64_t d = smem_desc(addr, lbo, sbo, layout);
+  return SmemDesc{(uint32_t)d, (uint32_t)(d >> 32)};
+}
+__device__ __forceinline__ uint64_t smem_desc_at(SmemDesc d, uint32_t byte_off) {
+  return ((uint64_t)d.hi << 32) | (uint64_t)(d.lo + (byte_off >> 4));
 }
 
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 D:
