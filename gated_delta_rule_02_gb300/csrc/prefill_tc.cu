@@ -46,15 +46,15 @@ constexpr int kD = kHeadDim;
 
 // ------------------------------- workspace --------------------------------
 struct WsLayout {
-  size_t a1, uy, gc, flags, total;
+  size_t a1, u, gc, flags, total;
 };
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 inline WsLayout ws_layout(int BH, int NT) {
   WsLayout w;
   const size_t tiles = (size_t)BH * NT;
   w.a1 = 0;
-  w.uy = align256(tiles * 128 * kD * sizeof(bf16));
-  w.gc = w.uy + align256(tiles * 128 * kD * sizeof(bf16));
+  w.u = align256(tiles * 128 * kD * sizeof(bf16));
+  w.gc = w.u + align256(tiles * kTile * kD * sizeof(bf16));
   w.flags = w.gc + align256(tiles * 4 * sizeof(float));
   w.total = w.flags + align256(tiles * sizeof(int));
   return w;
@@ -66,27 +66,9 @@ inline WsLayout ws_layout(int BH, int NT) {
 __device__ __forceinline__ uint32_t sw128(int row, int col) {
   return row * 128 + ((((col >> 3) ^ (row & 7))) << 4) + (col & 7) * 2;
 }
-// Row `row` of an MN-major operand whose rows are 2*R bytes (R bf16), with the
-// matching swizzle (R = 16: 32B, 32: 64B, 64: 128B); 16-byte chunk `ch`.
-template <int R>
-__device__ __forceinline__ uint32_t mn_row_chunk(int row, int ch) {
-  constexpr int kRowBytes = 2 * R;
-  constexpr int kMask = kRowBytes / 16 - 1;
-  return row * kRowBytes + ((ch ^ ((row * kRowBytes >> 7) & kMask)) << 4);
-}
-template <int R>
-__host__ __device__ constexpr uint32_t mn_layout() {
-  return R == 16 ? kSw32 : (R == 32 ? kSw64 : kSw128);
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
-}
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
-  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
 }
 // 16 consecutive floats from a 16-byte-aligned shared address.
 __device__ __forceinline__ void ld16f(const float* p, float* o) {
@@ -100,14 +82,6 @@ __device__ __forceinline__ void ld16f(const float* p, float* o) {
 // form it lets the compiler schedule the surrounding shared loads freely.
 __device__ __forceinline__ void st_sm16(uint8_t* base, uint32_t off, uint4 v) {
   *reinterpret_cast<uint4*>(base + off) = v;
-}
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
 }
 __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
   float v;
@@ -278,13 +252,13 @@ struct PrepParams {
   const CUtensorMap* tm_q;
   const CUtensorMap* tm_v;
   const CUtensorMap* tm_a1s;
-  const CUtensorMap* tm_uys;
+  const CUtensorMap* tm_us;
   const bf16* g;
   const bf16* beta;
   float* wsGC;
   int T, Hk, Hv, NT, BH;
-  // When set, y_loc / sqrt(Dk) goes straight to y ([B, T, Hv, 128], 64-token
-  // boxes) instead of the workspace; the scan then adds Qh S^T / sqrt(Dk) to it.
+  // y_loc / sqrt(Dk) goes straight to y ([B, T, Hv, 128], 64-token boxes); the
+  // scan then adds Qh S^T / sqrt(Dk) to it.
   const CUtensorMap* tm_y;
   float yscale;
 };
@@ -671,7 +645,8 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
         tma_store_2d(P.tm_a1s, sbase + kOffKQ + io * 16384 + c * C * 128, 64 * io,
                      row0 + 2 * C * c);
     } else {
-      tma_store_2d(P.tm_uys, sbase + kOffV + (io - 2) * 8192, 64 * (io - 2), row0);  // Ut rows
+      tma_store_2d(P.tm_us, sbase + kOffV + (io - 2) * 8192, 64 * (io - 2),
+                   (int)(tile_id * kTile));  // Ut rows
     }
     bulk_commit();
   }
@@ -721,7 +696,7 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
         unpack8(*reinterpret_cast<const uint4*>(qa + sw128(t, (col & 63) + 8)), q + 8);
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] = gt * q[j] - v[j];
-      } else if (P.tm_y) {
+      } else {
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] *= P.yscale;
       }
@@ -740,15 +715,9 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
       for (int c = 0; c < 64 / C; ++c)  // Qh rows of chunk c, half io
         tma_store_2d(P.tm_a1s, sbase + kOffA3 + io * 8192 + c * C * 128, 64 * io,
                      row0 + 2 * C * c + C);
-    } else {
-      const int h = io - 2;
-      if (P.tm_y) {  // y_loc / sqrt(Dk) into y (rows past T are clipped)
-        const int bh = head_of(lin), b = bh / Hv;
-        tma_store_4d(P.tm_y, sbase + kOffB + h * 8192, 64 * h, bh - b * Hv, tile_of(lin) * kTile,
-                     b);
-      } else {
-        tma_store_2d(P.tm_uys, sbase + kOffB + h * 8192, 64 * h, row0 + 64);  // y_loc rows
-      }
+    } else {  // y_loc / sqrt(Dk) into y (rows past T are clipped)
+      const int h = io - 2, bh = head_of(lin), b = bh / Hv;
+      tma_store_4d(P.tm_y, sbase + kOffB + h * 8192, 64 * h, bh - b * Hv, tile_of(lin) * kTile, b);
     }
     bulk_commit();
     if (io == 0) unpublished = tile_id;
@@ -782,325 +751,14 @@ template <int C>
 __global__ void __launch_bounds__(kPrepThreads, 1)
 prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_a1s,
-               const __grid_constant__ CUtensorMap tm_uys, const bf16* kin, const bf16* qin,
-               const bf16* vin, const bf16* __restrict__ g, const bf16* __restrict__ beta,
-               float* __restrict__ wsGC, int T, int Hk, int Hv, int NT, int BH) {
+               const __grid_constant__ CUtensorMap tm_us, const __grid_constant__ CUtensorMap tm_y,
+               const bf16* kin, const bf16* qin, const bf16* vin, const bf16* __restrict__ g,
+               const bf16* __restrict__ beta, float* __restrict__ wsGC, int T, int Hk, int Hv,
+               int NT, int BH, float scale) {
   extern __shared__ uint8_t smem_raw[];
-  const PrepParams P{kin, qin, vin, &tm_k, &tm_q, &tm_v, &tm_a1s, &tm_uys, g, beta, wsGC,
-                     T, Hk, Hv, NT, BH, nullptr, 0.f};
+  const PrepParams P{kin, qin, vin, &tm_k, &tm_q, &tm_v, &tm_a1s, &tm_us, g, beta, wsGC,
+                     T, Hk, Hv, NT, BH, &tm_y, scale};
   prep_role<C>(P, smem_raw, blockIdx.x, gridDim.x, nullptr);
-}
-
-// ============================================================================
-// scan kernel
-// ============================================================================
-// With M = Pt^T K (Dk x Dk) and N = Ut^T K, the state update of a chunk is
-//   S <- G_C S - S M + N,
-// so the only product that needs the state is S M; M, N and the output
-// product y = Yloc + Qh S^T are off the serial path.  Per chunk j:
-//   issuer  [M^T | N^T] = K^T [Pt | Ut]   (C/16 MMAs, N = 192; one chunk ahead)
-//           N^T += (-M^T) S_op^T           (8 MMAs, A = -M^T as bf16 in TMEM)
-//           Y    = Qh S_op^T               (8 MMAs, M = 64)
-//   state   S = G_C S + (N^T)^T; write S (bf16) as the next MMA operand
-//   aux     M^T (fp32) -> -M^T (bf16) in place; y = (Yloc + Y) / sqrt(Dk)
-// N^T is formed for the 64-wide value block holding this CTA's R rows.
-// Warp 0 is the TMA producer (three tile stages), warp 1 issues the MMAs and
-// owns the tensor memory, warps 2-5 hold S (thread = TMEM lane = key column k),
-// warps 6-9 are the auxiliary group.
-constexpr int kScanThreads = 320;
-constexpr int kStages = 3;
-constexpr uint32_t kScanTmemCols = 512;
-
-template <int R>
-struct ScanSmem {
-  // Pt (two 64-column halves of the [Pt; Qh] tile) and the 64-wide Ut block
-  // form three 128-row MN-major atoms 16 KB apart: the B operand of K^T [Pt | Ut].
-  // Chunk c's Ut rows sit at rows 2*C*c.., level with its Pt rows.
-  static constexpr uint32_t kA1 = 32 * 1024;  // [Pt; Qh]: 2 x 128 rows x 128 B
-  static constexpr uint32_t kOffU = kA1;      // Ut block, 128 rows x 128 B
-  static constexpr uint32_t kOffK = kOffU + 16384;  // K tile: 2 x 64 rows x 128 B
-  static constexpr uint32_t kOffY = kOffK + 16384;  // Yloc slice: 64 rows x R (MN-major)
-  static constexpr uint32_t kY = 64 * 2 * R;
-  static constexpr uint32_t kOffGC = kOffY + kY;    // G_C of the tile's chunks (fp32 x 4)
-  static constexpr uint32_t kGC = 16;
-  static constexpr uint32_t kStage = (kOffGC + kGC + 1023) & ~1023u;
-  static constexpr uint32_t kS = 128 * 2 * R;  // one S operand: 128 K-rows x R
-  static constexpr uint32_t kOffS = kStages * kStage;
-  static constexpr uint32_t kTotal = kOffS + 2 * ((kS + 1023) & ~1023u) + 1024;
-};
-
-// mbarrier slots
-enum : int {
-  kBFull = 0,                 // [kStages] tile landed (TMA)
-  kBEmpty = kBFull + kStages, // [kStages] tile consumed (256 thread arrivals)
-  kBDs = kBEmpty + kStages,   // serial product complete
-  kBY,                        // Y complete
-  kBM,                        // [2] [M^T | N^T] complete
-  kBSop = kBM + 2,            // S operand written (128 arrivals)
-  kBDsFree,                   // N^T read by the state group (128)
-  kBMt,                       // [2] -M^T operand written (128)
-  kBYFree = kBMt + 2,         // Y read by the aux group (128)
-  kBFin,                      // every MMA retired
-  kNumScanBars
-};
-
-template <int C, int R>
-__global__ void __launch_bounds__(kScanThreads, 1)
-scan_tc_kernel(const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_y,
-               const float* __restrict__ wsGC, const float* state_in, float* state_out,
-               bf16* __restrict__ y, int T, int Hk, int Hv, int NT, float scale) {
-  static_assert(R == 32 || R == 64, "value rows per CTA");
-  using SM = ScanSmem<R>;
-  constexpr int kCt = kTile / C;  // chunks per tile
-  constexpr uint32_t kRowBytes = 2 * R;
-  constexpr uint32_t kMnLay = mn_layout<R>();
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~(uintptr_t)1023);
-  __shared__ uint64_t bars[kNumScanBars];
-  __shared__ uint32_t tmem_base_sh;
-  const uint32_t sbase = smem_u32(sm);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int tile = blockIdx.x, bh = blockIdx.y;
-  const int b = bh / Hv, hv = bh - b * Hv, hk = hv / (Hv / Hk);
-  const int r0 = tile * R;
-  const int NC = (T + C - 1) / C;  // chunks holding at least one token
-  auto bar = [&](int i) { return smem_u32(&bars[i]); };
-
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(kBFull + s), 1);
-      mbar_init(bar(kBEmpty + s), 256);
-    }
-    mbar_init(bar(kBDs), 1);
-    mbar_init(bar(kBY), 1);
-    mbar_init(bar(kBM), 1);
-    mbar_init(bar(kBM + 1), 1);
-    mbar_init(bar(kBSop), 128);
-    mbar_init(bar(kBDsFree), 128);
-    mbar_init(bar(kBMt), 128);
-    mbar_init(bar(kBMt + 1), 128);
-    mbar_init(bar(kBYFree), 128);
-    mbar_init(bar(kBFin), 1);
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(&tmem_base_sh), kScanTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = tmem_base_sh;
-  // Two 192-column buffers: cols 0-127 M^T (fp32; cols 0-63 then hold -M^T as
-  // bf16 pairs), cols 128-191 N^T of the 64-wide value block; then Y.
-  auto tMN = [&](int x) { return tmem + 192 * x; };
-  const uint32_t tY = tmem + 384;
-  const uint32_t nt_col = 128 + (r0 & 63);  // this CTA's R columns inside N^T
-  auto stage_addr = [&](int j) { return sbase + ((j / kCt) % kStages) * SM::kStage; };
-  auto sS = [&](int x) { return sbase + SM::kOffS + x * ((SM::kS + 1023) & ~1023u); };
-  auto last_of_tile = [&](int j) { return (j % kCt) == kCt - 1 || j == NC - 1; };
-  // Wait for the tile holding chunk j (used once per tile per role).
-  auto wait_tile = [&](int j) {
-    const int n = j / kCt;
-    return mbar_wait(bar(kBFull + n % kStages), (n / kStages) & 1);
-  };
-
-  if (warp == 0) {
-    // ------------------------------ producer ------------------------------
-    if (lane == 0) {
-      prefetch_tmap(&tm_a1);
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_u);
-      prefetch_tmap(&tm_y);
-      int n = 0;
-      for (; n < NT; ++n) {
-        const int s = n % kStages;
-        if (n >= kStages && !mbar_wait(bar(kBEmpty + s), ((n / kStages) - 1) & 1)) break;
-        const uint32_t st = sbase + s * SM::kStage;
-        const uint32_t fb = bar(kBFull + s);
-        const int row = (int)(((size_t)bh * NT + n) * 128);
-        mbar_expect_tx(fb, SM::kA1 + kTile * 128 + 16384 + SM::kY + SM::kGC);
-        bulk_load(st + SM::kOffGC, wsGC + ((size_t)bh * NT + n) * 4, SM::kGC, fb);
-        tma_load_2d(st, &tm_a1, fb, 0, row);
-        tma_load_2d(st + 16384, &tm_a1, fb, 64, row);
-#pragma unroll
-        for (int c = 0; c < kCt; ++c)
-          tma_load_2d(st + SM::kOffU + 2 * C * c * 128, &tm_u, fb, r0 & ~63, row + c * C);
-        tma_load_4d(st + SM::kOffK, &tm_k, fb, 0, hk, n * kTile, b);
-        tma_load_4d(st + SM::kOffK + 8192, &tm_k, fb, 64, hk, n * kTile, b);
-        tma_load_2d(st + SM::kOffY, &tm_y, fb, r0, row + 64);
-      }
-      // Let the last copies land before the CTA can exit (they have, unless a
-      // consumer gave up early).
-      for (int m = (n > kStages ? n - kStages : 0); m < n; ++m)
-        mbar_wait(bar(kBFull + m % kStages), (m / kStages) & 1);
-    }
-    return;
-  }
-
-  bool ok = true;
-  if (warp == 1) {
-    // ---------------------------- MMA issuer -----------------------------
-    if (lane == 0) {
-      const uint32_t id_mn = idesc_bf16(128, 192, true, true);
-      const uint32_t id_s = idesc_bf16(128, R, false, true);
-      const uint32_t id_y = idesc_bf16(64, R, false, true);
-      // [M^T | N^T] of chunk j = K^T [Pt | Ut]: A = K^T, B = three MN-major atoms.
-      auto issue_mn = [&](int j) {
-        const uint32_t st = stage_addr(j);
-        const int c = j % kCt;
-#pragma unroll
-        for (int kk = 0; kk < C / 16; ++kk) {
-          const uint64_t a = smem_desc(st + SM::kOffK + (c * C + 16 * kk) * 128, 8192, 1024, kSw128);
-          const uint64_t bd = smem_desc(st + (2 * C * c + 16 * kk) * 128, 16384, 1024, kSw128);
-          mma_bf16_ss(tMN(j & 1), a, bd, id_mn, kk > 0);
-        }
-        mma_commit(bar(kBM + (j & 1)));
-      };
-      if (NC > 0) {
-        ok = wait_tile(0);
-        tc_fence_after();
-        if (ok) issue_mn(0);
-      }
-      for (int j = 0; j < NC && ok; ++j) {
-        const int c = j % kCt;
-        const uint32_t st = stage_addr(j);
-        const uint32_t sop = sS(j & 1);
-        // N^T += (-M^T) S^T   (the serial step)
-        if (!(ok = mbar_wait(bar(kBSop), j & 1))) break;
-        if (!(ok = mbar_wait(bar(kBMt + (j & 1)), (j >> 1) & 1))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts(tMN(j & 1) + nt_col, tMN(j & 1) + 8 * kk,
-                      smem_desc(sop + kk * 16 * kRowBytes, 0, 8 * kRowBytes, kMnLay), id_s, 1);
-        mma_commit(bar(kBDs));
-        // [M^T | N^T] of the next chunk, once the state group has read chunk j-1's.
-        if (j + 1 < NC) {
-          if (j > 0 && !(ok = mbar_wait(bar(kBDsFree), (j - 1) & 1))) break;
-          if ((j + 1) % kCt == 0 && !(ok = wait_tile(j + 1))) break;
-          tc_fence_after();
-          issue_mn(j + 1);
-        }
-        // Y = Qh S^T (M = 64: the chunk's Qh rows)
-        if (j > 0 && !(ok = mbar_wait(bar(kBYFree), (j - 1) & 1))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t a = st + (kk >> 2) * 16384 + (2 * C * c + C) * 128 + (kk & 3) * 32;
-          mma_bf16_ss(tY, smem_desc(a, 16, 1024, kSw128),
-                      smem_desc(sop + kk * 16 * kRowBytes, 0, 8 * kRowBytes, kMnLay), id_y, kk > 0);
-        }
-        mma_commit(bar(kBY));
-      }
-      // Every MMA retires before the tensor memory is released.
-      mma_commit(bar(kBFin));
-      mbar_wait(bar(kBFin), 0);
-    }
-    __syncwarp();
-  } else if (warp < 6) {
-    // ---------------------------- state group ----------------------------
-    const int L = ((warp & 3) << 5) | lane;  // TMEM lane = key column of S
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const size_t sidx = ((size_t)bh * kD + r0) * kD + L;
-    float s[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) s[r] = state_in ? state_in[sidx + (size_t)r * kD] : 0.f;
-    auto write_op = [&](int x) {
-#pragma unroll
-      for (int ch = 0; ch < R / 8; ++ch)
-        st_shared_v4(sS(x) + mn_row_chunk<R>(L, ch), pack8(s + 8 * ch));
-      fence_proxy_async();
-      mbar_arrive(bar(kBSop));
-    };
-    write_op(0);
-    for (int j = 0; j < NC; ++j) {
-      const int c = j % kCt;
-      const uint32_t st = stage_addr(j);
-      if (c == 0 && !(ok = wait_tile(j))) break;
-      const float Gc = ld_shared_f32(st + SM::kOffGC + 4 * c);
-      if (!(ok = mbar_wait(bar(kBDs), j & 1))) break;
-      tc_fence_after();
-      float d[R];
-#pragma unroll
-      for (int q = 0; q < R; q += 16) tmem_ld16(tMN(j & 1) + nt_col + lane_base + q, d + q);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar(kBDsFree));
-      if (last_of_tile(j)) mbar_arrive(bar(kBEmpty + (j / kCt) % kStages));
-#pragma unroll
-      for (int r = 0; r < R; ++r) s[r] = fmaf(Gc, s[r], d[r]);
-      if (j + 1 < NC) write_op((j + 1) & 1);
-    }
-    if (ok) {
-#pragma unroll
-      for (int r = 0; r < R; ++r) state_out[sidx + (size_t)r * kD] = s[r];
-    }
-  } else {
-    // ----------------------------- aux group -----------------------------
-    const int qd = warp & 3;
-    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
-    // M^T (fp32, cols 0-127) -> -M^T as bf16 pairs in cols 0-63 of the same
-    // buffer (each thread rewrites only its own lane, after reading it).
-    auto convert = [&](int j) {
-      if (!mbar_wait(bar(kBM + (j & 1)), (j >> 1) & 1)) return false;
-      tc_fence_after();
-      const uint32_t tb = tMN(j & 1) + lane_base;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float v[64];
-        tmem_ld32(tb + 64 * h, v);
-        tmem_ld32(tb + 64 * h + 32, v + 32);
-        tmem_wait_ld();
-        uint32_t p[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) p[i] = pack_bf16x2(-v[2 * i], -v[2 * i + 1]);
-        tmem_st32(tb + 32 * h, p);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(kBMt + (j & 1)));
-      return true;
-    };
-    if (NC > 0) ok = convert(0);
-    for (int j = 0; j < NC && ok; ++j) {
-      const int c = j % kCt;
-      const uint32_t st = stage_addr(j);
-      if (j + 1 < NC && !(ok = convert(j + 1))) break;
-      if (c == 0 && !(ok = wait_tile(j))) break;
-      if (!(ok = mbar_wait(bar(kBY), j & 1))) break;
-      tc_fence_after();
-      float d[R];
-#pragma unroll
-      for (int q = 0; q < R; q += 16) tmem_ld16(tY + lane_base + q, d + q);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar(kBYFree));
-      // M = 64 result: row 16*qd + i sits in lane 32*qd + i, i < 16.
-      const int t = 16 * qd + lane;
-      const int tok = j * C + t;
-      if (lane < 16 && t < C && tok < T) {
-        bf16* yp = y + (((size_t)b * T + tok) * Hv + hv) * kD + r0;
-        const uint32_t yrow = st + SM::kOffY;
-#pragma unroll
-        for (int ch = 0; ch < R / 8; ++ch) {
-          float y8[8];
-          unpack8(ld_shared_v4(yrow + mn_row_chunk<R>(c * C + t, ch)), y8);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) y8[e] = (y8[e] + d[ch * 8 + e]) * scale;
-          *reinterpret_cast<uint4*>(yp + ch * 8) = pack8(y8);
-        }
-      }
-      // Y(j) complete implies every earlier MMA reading this tile is too.
-      if (last_of_tile(j)) mbar_arrive(bar(kBEmpty + (j / kCt) % kStages));
-    }
-  }
-
-  tc_fence_before();
-  named_bar_sync(1, kScanThreads - 32);
-  if (warp == 1) tmem_dealloc(tmem, kScanTmemCols);
 }
 
 // ============================================================================
@@ -1247,7 +905,7 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
             tma_load_2d(st + SM::kOffP + h * 8192 + c * C * 128, tm_a1c, fb, 64 * h,
                         row + 2 * C * c);
           tma_load_4d(st + SM::kOffK + h * 8192, tm_k, fb, 64 * h, hk, n * kTile, b);
-          tma_load_2d(st + SM::kOffU + h * 8192, tm_uy, fb, 64 * h, row);
+          tma_load_2d(st + SM::kOffU + h * 8192, tm_uy, fb, 64 * h, (int)(tid_ws * kTile));
         }
       } else {
         const uint32_t st = sbase + SM::kOffQ + s * SM::kQ;
@@ -1458,8 +1116,7 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_a1s,
-                     const __grid_constant__ CUtensorMap tm_uys,
-                     const __grid_constant__ CUtensorMap tm_a1,
+                     const __grid_constant__ CUtensorMap tm_us,
                      const __grid_constant__ CUtensorMap tm_y,
                      const __grid_constant__ CUtensorMap tm_yred, const bf16* kin,
                      const bf16* qin, const bf16* vin, const bf16* __restrict__ g,
@@ -1468,13 +1125,26 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_k,
                      int BH, float scale) {
   extern __shared__ uint8_t smem_raw[];
   if ((int)blockIdx.x < BH) {
-    scan_role128<C>(&tm_a1s, &tm_k, &tm_uys, &tm_yred, wsGC, flags, state_in, state_out, T, Hk,
+    scan_role128<C>(&tm_a1s, &tm_k, &tm_us, &tm_yred, wsGC, flags, state_in, state_out, T, Hk,
                     Hv, NT, blockIdx.x, scale, smem_raw);
   } else {
-    const PrepParams P{kin, qin, vin, &tm_k, &tm_q, &tm_v, &tm_a1s, &tm_uys, g, beta, wsGC,
+    const PrepParams P{kin, qin, vin, &tm_k, &tm_q, &tm_v, &tm_a1s, &tm_us, g, beta, wsGC,
                        T, Hk, Hv, NT, BH, &tm_y, scale};
     prep_role<C>(P, smem_raw, blockIdx.x - BH, gridDim.x - BH, flags);
   }
+}
+
+// The scan alone (after prep_tc_kernel in stream order): one CTA per head.
+template <int C>
+__global__ void __launch_bounds__(kFusedThreads, 1)
+scan_head_kernel(const __grid_constant__ CUtensorMap tm_a1s, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_us,
+                 const __grid_constant__ CUtensorMap tm_yred, const float* __restrict__ wsGC,
+                 const float* state_in, float* state_out, int T, int Hk, int Hv, int NT,
+                 float scale) {
+  extern __shared__ uint8_t smem_raw[];
+  scan_role128<C>(&tm_a1s, &tm_k, &tm_us, &tm_yred, wsGC, nullptr, state_in, state_out, T, Hk,
+                  Hv, NT, blockIdx.x, scale, smem_raw);
 }
 
 // ============================================================================
@@ -1529,7 +1199,6 @@ bool make_rows_map(CUtensorMap* m, const void* base, size_t rows, int box_cols, 
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr int kScanRows = 32;
 
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms() {
@@ -1551,30 +1220,30 @@ cudaError_t launch_c(const PrefillArgs& a) {
   const WsLayout w = ws_layout(BH, NT);
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   bf16* wsA1 = reinterpret_cast<bf16*>(ws + w.a1);
-  bf16* wsUY = reinterpret_cast<bf16*>(ws + w.uy);
+  bf16* wsU = reinterpret_cast<bf16*>(ws + w.u);
   float* wsGC = reinterpret_cast<float*>(ws + w.gc);
 
   if (!encode_fn()) return cudaErrorNotSupported;
-  CUtensorMap tk, tq, tv, ta1, tuy, tuc, ta1s, tuys;
+  CUtensorMap tk, tq, tv, ta1s, tus, ty, tyred;
   if (!make_bthd_map(&tk, a.k, a.B, a.T, a.Hk) || !make_bthd_map(&tq, a.q, a.B, a.T, a.Hk) ||
       !make_bthd_map(&tv, a.v, a.B, a.T, a.Hv) ||
-      !make_rows_map(&ta1, wsA1, (size_t)BH * NT * 128, 64, 128, true) ||
-      !make_rows_map(&tuy, wsUY, (size_t)BH * NT * 128, kScanRows, 64, true) ||
-      !make_rows_map(&tuc, wsUY, (size_t)BH * NT * 128, 64, C, true) ||
       !make_rows_map(&ta1s, wsA1, (size_t)BH * NT * 128, 64, C, true) ||
-      !make_rows_map(&tuys, wsUY, (size_t)BH * NT * 128, 64, 64, true))
+      !make_rows_map(&tus, wsU, (size_t)BH * NT * kTile, 64, 64, true) ||
+      !make_bthd_map(&ty, a.y, a.B, a.T, a.Hv) || !make_bthd_map(&tyred, a.y, a.B, a.T, a.Hv, C))
     return cudaErrorInvalidValue;
 
   const float scale = 1.0f / sqrtf((float)kD);
   const int sms = num_sms();
+  const bf16* k = static_cast<const bf16*>(a.k);
+  const bf16* q = static_cast<const bf16*>(a.q);
+  const bf16* v = static_cast<const bf16*>(a.v);
+  const bf16* g = static_cast<const bf16*>(a.g);
+  const bf16* beta = static_cast<const bf16*>(a.beta);
   cudaError_t e;
   // Fused path: one scan CTA per head next to at least two thirds of the SMs
   // doing prep, in one cooperative launch.
   if (3 * BH <= sms) {
     int* flags = reinterpret_cast<int*>(ws + w.flags);
-    CUtensorMap ty, tyred;
-    if (!make_bthd_map(&ty, a.y, a.B, a.T, a.Hv) || !make_bthd_map(&tyred, a.y, a.B, a.T, a.Hv, C))
-      return cudaErrorInvalidValue;
     e = cudaFuncSetAttribute(fused_prefill_kernel<C>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kFusedSmem);
     if (e == cudaSuccess) e = cudaMemsetAsync(flags, 0, (size_t)BH * NT * sizeof(int), a.stream);
@@ -1589,31 +1258,25 @@ cudaError_t launch_c(const PrefillArgs& a) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fused_prefill_kernel<C>, tk, tq, tv, ta1s, tuys, ta1, ty,
-                              tyred, static_cast<const bf16*>(a.k), static_cast<const bf16*>(a.q),
-                              static_cast<const bf16*>(a.v), static_cast<const bf16*>(a.g),
-                              static_cast<const bf16*>(a.beta), wsGC, flags, a.state_in,
-                              a.state_out, a.T, a.Hk, a.Hv, NT, BH, scale);
+    return cudaLaunchKernelEx(&cfg, fused_prefill_kernel<C>, tk, tq, tv, ta1s, tus, ty, tyred, k,
+                              q, v, g, beta, wsGC, flags, a.state_in, a.state_out, a.T, a.Hk,
+                              a.Hv, NT, BH, scale);
   }
 
-  // Split path: the persistent prep kernel, then the scan (R value rows per CTA).
+  // Split path: the persistent prep kernel on every SM, then one scan CTA per head.
   e = cudaFuncSetAttribute(prep_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kPrepSmem);
-  if (e != cudaSuccess) return e;
-  using SM = ScanSmem<kScanRows>;
-  e = cudaFuncSetAttribute(scan_tc_kernel<C, kScanRows>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kTotal);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(scan_head_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Scan128Smem::kTotal);
   if (e != cudaSuccess) return e;
   const int prep_ctas = std::min(sms, (BH * NT + kPrepGroups - 1) / kPrepGroups);
   prep_tc_kernel<C><<<prep_ctas, kPrepThreads, kPrepSmem, a.stream>>>(
-      tk, tq, tv, ta1s, tuys, static_cast<const bf16*>(a.k), static_cast<const bf16*>(a.q),
-      static_cast<const bf16*>(a.v), static_cast<const bf16*>(a.g),
-      static_cast<const bf16*>(a.beta), wsGC, a.T, a.Hk, a.Hv, NT, BH);
+      tk, tq, tv, ta1s, tus, ty, k, q, v, g, beta, wsGC, a.T, a.Hk, a.Hv, NT, BH, scale);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  scan_tc_kernel<C, kScanRows><<<dim3(kD / kScanRows, BH), kScanThreads, SM::kTotal, a.stream>>>(
-      ta1, tk, tuc, tuy, wsGC, a.state_in, a.state_out, static_cast<bf16*>(a.y), a.T, a.Hk, a.Hv,
-      NT, scale);
+  scan_head_kernel<C><<<BH, kFusedThreads, Scan128Smem::kTotal, a.stream>>>(
+      ta1s, tk, tus, tyred, wsGC, a.state_in, a.state_out, a.T, a.Hk, a.Hv, NT, scale);
   return cudaGetLastError();
 }
 

@@ -124,7 +124,7 @@ GDN_API int gdn_decode_step(const void *q, const void *k, const void *v, const v
  *
  *   Limit: the problem's gdn_prefill_workspace_bytes(...) must not exceed
  *   GDN_NOALLOC_SCRATCH_BYTES (32 MiB: for bf16 inputs, B*Hv*ceil(T/64) up to
- *   511 tiles, e.g. T = 4096 with B*Hv = 7, or T = 1024 with B*Hv = 31);
+ *   682 tiles, e.g. T = 4096 with B*Hv = 10, or T = 1024 with B*Hv = 42);
  *   larger problems return GDN_ERR_NOALLOC_LIMIT with nothing enqueued.
  *   Set-up: the first call on each device (with that device current) looks
  *   up the array's device address once; make that first call before any
