@@ -45,8 +45,8 @@ FLUSH_BYTES = 256 << 20
 # it was taken on (sha256 prefix of those files); otherwise reported as null.
 _KDIR = os.path.join(ROOT, "gated_delta_rule_02_gb300", "csrc")
 MEASURED_TRAFFIC = {
-    "prefill": {"sources": ["prefill_tc.cu", "sm100_ptx.cuh"], "sha": "42ab9df1c488e0c3",
-                "bytes": 320.1e6},
+    "prefill": {"sources": ["prefill_tc.cu", "sm100_ptx.cuh"], "sha": "521805415adfb180",
+                "bytes": 154.4e6},
     "decode": {"sources": ["decode.cu"], "sha": "76396f3fe1bee68d", "bytes": 211.9e6},
 }
 
@@ -186,6 +186,16 @@ def roofline(alg_bytes, seconds, hbm_gbs, kind, traffic=None):
             "unit": "GB/s", "frac": round(achieved / hbm_gbs, 4),
             "traffic": None if traffic is None else round(traffic),
             "algorithmic_bytes": alg_bytes, "peak_kind": kind}
+
+
+def prefill_launches(w, dev):
+    """Kernels one gdn_prefill call launches: bf16 runs prep and scan as one
+    cooperative kernel when B*Hv is at most a third of the SMs, else as two;
+    fp32 always as two."""
+    if w.torch_dtype != torch.bfloat16:
+        return 2
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    return 1 if 3 * w.B * w.Hv <= sms else 2
 
 
 def median_ms(pairs):
@@ -444,7 +454,7 @@ def main():
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline(prefill_alg_bytes(w), ms / 1e3, hbm, peak_kind,
                              measured_traffic("prefill") if w.name == "prefill_t4096" else None),
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": prefill_launches(w, dev) * args.steps,
         "clocks": clocks,
     }
     line["roofline"]["scope"] = "whole gdn_prefill call (all its kernels)"

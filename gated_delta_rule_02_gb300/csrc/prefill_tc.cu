@@ -2,33 +2,33 @@
 //
 // The method is the chunked Woodbury-Young form of metaltile-std
 // `gated_delta_wy.rs` (module docs, "Algorithm", steps 1-9), with the decay
-// ratios formed as products (ferrox-core `gdn_chunk.rs`, "The algebra").  It is
-// split in two launches:
+// ratios formed as products (ferrox-core `gdn_chunk.rs`, "The algebra").  Two
+// roles share a workspace:
 //
-// prep_tc_kernel, one CTA per (b, hv, 64-token tile), every tile in parallel.
-// A tile holds 64/C chunks; all C x C matrices are block diagonal by chunk.
+// prep (prep_role): the state-free work of one 64-token tile of one (b, hv)
+// head; every tile independent.  A tile holds 64/C chunks; all C x C matrices
+// are block diagonal by chunk.
 //   G1  [K;Q] K^T                      -> KK^T, QK^T          (steps 3, 6-prep)
 //   gates: G_t (chunk-local prefix products), Gam[t][j] = g_{j+1}..g_t
-//   T_L = (I + L)^-1,  L[t][j] = beta_j KK^T[t][j]          (step 4)
-//   T_A = (I + A)^-1,  A[t][j] = beta_t Gam[t][j] KK^T[t][j] (step 5)
-//       both by blocked forward substitution (16 x 16 diagonal blocks).
-//   G2  [T_L 0; 0 T_A diag(beta)] [K; V]  -> P = T_L K, U = T_A (beta V)
+//   T_L = (I + L)^-1,  L[t][j] = beta_j KK^T[t][j]          (step 4), by blocked
+//       forward substitution; step 5 needs no second inverse:
+//       (I + A)^-1 diag(beta) = diag(beta) (Gam . T_L),  A[t][j] = beta_t Gam[t][j] KK^T[t][j]
+//   G2  [T_L; diag(beta)(Gam . T_L)] [K | V]  -> P = T_L K, U = (I + A)^-1 (beta V)
 //   G3  [diag(G) M 0; 0 Gam.QK^T] [P; U]  -> the state-free part of step 7
 //       (M[t][i] = beta_i QK^T[t][i], i <= t) and y_local (step 6)
-//   and writes to the workspace, per tile, in bf16:
-//     A1 = per chunk [Pt; Qh], Pt = G_C beta P  (step 9),  Qh = G Q - G M P (step 7)
-//     UY = [Ut; Yloc],         Ut = Gam[C-1][.] U          (step 9)
-//   plus G_C (fp32) per chunk.
-// scan_tc_kernel, one CTA per (b, hv, tile of R value rows); S (R x 128, fp32)
-// lives in registers, one column per thread, and as a bf16 MMA operand in
-// shared memory.  Step 9 is regrouped as S <- G_C S - S M + N with
-// M = Pt^T K and N = Ut^T K, so per chunk only the product with M waits for
-// the state:
+//   and writes, per tile, in bf16: to the workspace A1 = per chunk [Pt; Qh] with
+//   Pt = G_C beta P (step 9), Qh = G Q - G M P (step 7), and Ut = Gam[C-1][.] U
+//   (step 9), plus G_C (fp32) per chunk; y_local / sqrt(Dk) straight into y.
+// scan (scan_role128): one CTA per (b, hv) carries S (128 x 128, fp32) through
+// the chunks.  Step 9 is regrouped as S <- G_C S - S M + N with M = Pt^T K and
+// N = Ut^T K, so per chunk only the product with M waits for the state:
 //   D  = K^T Ut + (-M^T) S^T;  S <- G_C S + D^T                       (step 9)
-//   Y  = Qh S^T;               y = (Y + Yloc) / sqrt(Dk)              (steps 7-8)
-// M^T = K^T Pt is formed one chunk ahead on the tensor cores.  Warp-specialised:
-// a TMA producer (three tile stages), an MMA issuer, the state group and an
-// auxiliary group (M^T to a bf16 operand, the y epilogue).
+//   Y^T = S Qh^T;  y += Y / sqrt(Dk)  (TMA reduction)                 (steps 7-8)
+// M^T = K^T Pt is formed a chunk ahead on the tensor cores.
+//
+// Launches: fused_prefill_kernel runs both roles in one cooperative launch
+// (prep publishes each tile through a flag, the scan waits for it); for many
+// heads, prep_tc_kernel then scan_head_kernel in stream order.
 #include "gdn_internal.cuh"
 #include "sm100_ptx.cuh"
 
