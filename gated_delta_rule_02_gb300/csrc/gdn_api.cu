@@ -31,6 +31,7 @@ size_t gdn_prefill_workspace_bytes(int B, int T, int Hk, int Hv, int Dk, int Dv,
                                    int chunk, int dtype) {
   if (check_common(B, T, Hk, Hv, Dk, Dv, dtype) != GDN_OK) return 0;
   if (chunk != 16 && chunk != 32 && chunk != 64) return 0;
+  if (T <= gdn::kShortT) return 0;  // the short-T sequential kernel needs none
   if (dtype == GDN_DTYPE_BF16) return gdn::prefill_tc_workspace_bytes(B, T, Hv);
   return gdn::prefill_simt_workspace_bytes(B, T, Hv, chunk);
 }
@@ -54,8 +55,9 @@ int gdn_prefill(const void* q, const void* k, const void* v, const void* g,
   gdn::PrefillArgs a{q, k, v, g, beta, state_in, state_out, y, B, T, Hk, Hv, chunk,
                      dtype, workspace, workspace_bytes,
                      static_cast<cudaStream_t>(stream)};
-  cudaError_t e = dtype == GDN_DTYPE_BF16 ? gdn::launch_prefill_tc(a)
-                                           : gdn::launch_prefill_simt(a);
+  cudaError_t e = T <= gdn::kShortT       ? gdn::launch_prefill_short(a)
+                  : dtype == GDN_DTYPE_BF16 ? gdn::launch_prefill_tc(a)
+                                            : gdn::launch_prefill_simt(a);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

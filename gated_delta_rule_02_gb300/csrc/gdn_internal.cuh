@@ -50,6 +50,11 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a);
 // -1 if it cannot be read.
 int prefill_tc_device_error(bool clear);
 
+// Short sequences (T <= kShortT): the sequential rule with the state on chip,
+// no workspace.
+constexpr int kShortT = 32;
+cudaError_t launch_prefill_short(const PrefillArgs& a);
+
 // Streaming single-step decode.
 cudaError_t launch_decode(const DecodeArgs& a);
 

@@ -1,0 +1,180 @@
+// Short-T prefill: T <= kShortT tokens of every (b, hv) through the sequential
+// rule with the state held on chip, read once and written once.
+//
+// The pages route short sequences to the row-packed sequential kernel rather
+// than the chunked form (MLX PR "Pack gated_delta_seq: 8 value rows per
+// SIMD-group", Performance, the short-T rows; ferrox-core `gdn_chunk.rs`,
+// `DEVICE_ROWS`): below about a chunk of tokens the chunk machinery costs more
+// than it saves.  Per value row r of S and token t (every row evolves on its
+// own; ferrox-core "The algebra", one row):
+//     x = S[r]·k_t,  z = S[r]·q_t
+//     d = beta_t (v_t[r] - g_t x)
+//     S[r] <- g_t S[r] + d k_t
+//     y_t[r] = (g_t z + d (k_t·q_t)) / sqrt(Dk)      (= S_t[r]·q_t / sqrt(Dk))
+//
+// Layout: one CTA of four warps per (b, hv) head, each warp owning 32 rows,
+// eight lanes per 512-byte row as in the decode kernel.  The CTA first stages
+// the T tokens' k, q, v (as fp32), g, beta and k·q in shared memory; each warp
+// then takes G row groups (4 rows each) at a time through all T tokens with
+// their state in registers.
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kShortThreads = 128;
+
+__device__ __forceinline__ float4 ld_state(const float* p) {
+  return __ldcg(reinterpret_cast<const float4*>(p));
+}
+__device__ __forceinline__ void st_state(float* p, float4 v) {
+  __stcg(reinterpret_cast<float4*>(p), v);
+}
+
+template <typename T, int G>
+__global__ void __launch_bounds__(kShortThreads)
+short_prefill_kernel(const T* __restrict__ q, const T* __restrict__ k,
+                     const T* __restrict__ v, const T* __restrict__ g,
+                     const T* __restrict__ beta, const float* state_in,
+                     float* state_out, T* __restrict__ y, int Tlen, int Hk, int Hv,
+                     float scale) {
+  constexpr int D = kHeadDim;
+  extern __shared__ float4 smem_f4[];
+  float* ks = reinterpret_cast<float*>(smem_f4);  // [Tlen][D]
+  float* qs = ks + Tlen * D;                      // [Tlen][D]
+  float* vs = qs + Tlen * D;                      // [Tlen][D]
+  float* gs = vs + Tlen * D;                      // [Tlen]
+  float* bs = gs + Tlen;                          // [Tlen]
+  float* kqs = bs + Tlen;                         // [Tlen]
+
+  const int bh = blockIdx.x;
+  const int b = bh / Hv;
+  const int hv = bh - b * Hv;
+  const int hk = hv / (Hv / Hk);
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int rg = lane >> 3;   // row within a group of four
+  const int sub = lane & 7;   // lane within the row
+
+  // Stage the tokens: thread tid loads elements 4*(tid%32)..+3 of rows t with
+  // t = tid/32 (mod 4) stepping by 4.
+  for (int t = warp; t < Tlen; t += kShortThreads / 32) {
+    const size_t kq_off = (((size_t)b * Tlen + t) * Hk + hk) * D + 4 * lane;
+    const size_t v_off = (((size_t)b * Tlen + t) * Hv + hv) * D + 4 * lane;
+    float kk[4], qq[4], vv[4];
+    load4(k + kq_off, kk);
+    load4(q + kq_off, qq);
+    load4(v + v_off, vv);
+    *reinterpret_cast<float4*>(ks + t * D + 4 * lane) = make_float4(kk[0], kk[1], kk[2], kk[3]);
+    *reinterpret_cast<float4*>(qs + t * D + 4 * lane) = make_float4(qq[0], qq[1], qq[2], qq[3]);
+    *reinterpret_cast<float4*>(vs + t * D + 4 * lane) = make_float4(vv[0], vv[1], vv[2], vv[3]);
+    float kq = kk[0] * qq[0] + kk[1] * qq[1] + kk[2] * qq[2] + kk[3] * qq[3];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+    if (lane == 0) {
+      const size_t gi = ((size_t)b * Tlen + t) * Hv + hv;
+      kqs[t] = kq;
+      gs[t] = to_f32(g[gi]);
+      bs[t] = to_f32(beta[gi]);
+    }
+  }
+  __syncthreads();
+
+  const float* Sin = state_in ? state_in + (size_t)bh * D * D : nullptr;
+  float* Sout = state_out + (size_t)bh * D * D;
+
+#pragma unroll 1
+  for (int it = 0; it < 32 / (4 * G); ++it) {
+    const int row0 = warp * 32 + it * 4 * G + rg;  // this lane's row in group gi: row0 + 4*gi
+    float4 s[G][4];
+#pragma unroll
+    for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        s[gi][j] = Sin ? ld_state(Sin + (size_t)(row0 + 4 * gi) * D + 4 * (sub + 8 * j))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+
+#pragma unroll 1
+    for (int t = 0; t < Tlen; ++t) {
+      float kr[16], qr[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 a = *reinterpret_cast<const float4*>(ks + t * D + 4 * (sub + 8 * j));
+        const float4 c = *reinterpret_cast<const float4*>(qs + t * D + 4 * (sub + 8 * j));
+        kr[4 * j] = a.x; kr[4 * j + 1] = a.y; kr[4 * j + 2] = a.z; kr[4 * j + 3] = a.w;
+        qr[4 * j] = c.x; qr[4 * j + 1] = c.y; qr[4 * j + 2] = c.z; qr[4 * j + 3] = c.w;
+      }
+      const float gt = gs[t], bt = bs[t], kq = kqs[t];
+      float x[G], z[G];
+#pragma unroll
+      for (int gi = 0; gi < G; ++gi) {
+        float xa = 0.f, za = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          xa = fmaf(s[gi][j].x, kr[4 * j + 0], xa);
+          xa = fmaf(s[gi][j].y, kr[4 * j + 1], xa);
+          xa = fmaf(s[gi][j].z, kr[4 * j + 2], xa);
+          xa = fmaf(s[gi][j].w, kr[4 * j + 3], xa);
+          za = fmaf(s[gi][j].x, qr[4 * j + 0], za);
+          za = fmaf(s[gi][j].y, qr[4 * j + 1], za);
+          za = fmaf(s[gi][j].z, qr[4 * j + 2], za);
+          za = fmaf(s[gi][j].w, qr[4 * j + 3], za);
+        }
+        x[gi] = xa;
+        z[gi] = za;
+      }
+#pragma unroll
+      for (int off = 1; off < 8; off <<= 1)
+#pragma unroll
+        for (int gi = 0; gi < G; ++gi) {
+          x[gi] += __shfl_xor_sync(0xffffffffu, x[gi], off);
+          z[gi] += __shfl_xor_sync(0xffffffffu, z[gi], off);
+        }
+      T* yt = y + (((size_t)b * Tlen + t) * Hv + hv) * D;
+#pragma unroll
+      for (int gi = 0; gi < G; ++gi) {
+        const int row = row0 + 4 * gi;
+        const float d = bt * (vs[t * D + row] - gt * x[gi]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          s[gi][j].x = fmaf(gt, s[gi][j].x, d * kr[4 * j + 0]);
+          s[gi][j].y = fmaf(gt, s[gi][j].y, d * kr[4 * j + 1]);
+          s[gi][j].z = fmaf(gt, s[gi][j].z, d * kr[4 * j + 2]);
+          s[gi][j].w = fmaf(gt, s[gi][j].w, d * kr[4 * j + 3]);
+        }
+        if (sub == 0) yt[row] = from_f32<T>(fmaf(gt, z[gi], d * kq) * scale);
+      }
+    }
+#pragma unroll
+    for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        st_state(Sout + (size_t)(row0 + 4 * gi) * D + 4 * (sub + 8 * j), s[gi][j]);
+  }
+}
+
+size_t short_smem_bytes(int T) { return (size_t)T * (3 * kHeadDim + 3) * sizeof(float); }
+
+template <typename T>
+cudaError_t launch_short_t(const PrefillArgs& a) {
+  const float scale = 1.0f / sqrtf((float)kHeadDim);
+  const size_t smem = short_smem_bytes(a.T);
+  cudaError_t e = cudaFuncSetAttribute(short_prefill_kernel<T, 2>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  short_prefill_kernel<T, 2><<<a.B * a.Hv, kShortThreads, smem, a.stream>>>(
+      static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v),
+      static_cast<const T*>(a.g), static_cast<const T*>(a.beta), a.state_in, a.state_out,
+      static_cast<T*>(a.y), a.T, a.Hk, a.Hv, scale);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_short(const PrefillArgs& a) {
+  if (a.dtype == 0) return launch_short_t<float>(a);
+  return launch_short_t<__nv_bfloat16>(a);
+}
+
+}  // namespace gdn

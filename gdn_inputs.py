@@ -64,6 +64,11 @@ WORKLOADS = {
                                Dk=128, Dv=128, dtype="bf16", chunk=64, u_max=0.1,
                                s0_std=0.0, seed=1004, heavy_frac=0.1,
                                heavy_umax=5.0),
+    # A short multi-token call (the short-T sequential path): 16 tokens for
+    # each of 64 sequences, the decode shape; the state (134 MB) dominates.
+    "prefill_b64_t16": Workload("prefill_b64_t16", B=64, T=16, Hk=16, Hv=32, Dk=128,
+                                Dv=128, dtype="bf16", chunk=64, u_max=0.1,
+                                s0_std=0.1, seed=1005),
 }
 
 

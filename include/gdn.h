@@ -82,6 +82,9 @@ GDN_API size_t gdn_prefill_workspace_bytes(int B, int T, int Hk, int Hv, int Dk,
  *   chunk      tokens per chunk: 16, 32 or 64.  Any T >= 1 is accepted; a
  *              last chunk shorter than `chunk` behaves as if padded with
  *              g = 1, beta = 0 tokens (metaltile-std kernel, chunk loop).
+ *              Sequences of T <= 32 run the sequential rule instead (state on
+ *              chip, fp32 arithmetic, no workspace; the short-T routing of
+ *              the MLX PR "Pack gated_delta_seq", Performance).
  *   workspace  device scratch of at least gdn_prefill_workspace_bytes(...)
  *              bytes, 256-byte aligned, owned by the caller; its contents on
  *              entry do not matter and on return are unspecified.  It must

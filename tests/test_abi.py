@@ -61,6 +61,10 @@ def test_workspace_bytes(L):
     assert w(1, 100, 3, 32, 128, 128, 64, 1) == 0        # Hv % Hk != 0
     # grows with the sequence
     assert w(1, 8192, 16, 32, 128, 128, 64, 1) > w(1, 4096, 16, 32, 128, 128, 64, 1)
+    # short sequences run the sequential kernel, which needs no workspace
+    assert w(4, 32, 16, 32, 128, 128, 64, 1) == 0
+    assert w(4, 32, 16, 32, 128, 128, 64, 0) == 0
+    assert w(4, 33, 16, 32, 128, 128, 64, 1) > 0
 
 
 FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call is rejected first

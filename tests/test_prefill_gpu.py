@@ -99,6 +99,54 @@ def test_prefill_vanishing_gate_is_finite(cuda_device):
     assert rel_err(s, so) <= TOL[BF16]
 
 
+SHORT = [
+    # (B, T, Hk, Hv, dtype): T <= 32 runs the short-T sequential kernel
+    (1, 1, 1, 1, BF16),
+    (2, 7, 2, 6, BF16),     # GQA 3:1
+    (3, 16, 4, 8, F32),
+    (1, 31, 16, 32, BF16),
+    (2, 32, 8, 16, F32),
+]
+
+
+@pytest.mark.parametrize("B,T,Hk,Hv,dtype", SHORT)
+def test_prefill_short_t_matches_oracle(cuda_device, B, T, Hk, Hv, dtype):
+    ins = gdn_inputs.make_inputs(B, T, Hk, Hv, 128, 128, dtype, seed=300 + T + Hv,
+                                 u_max=0.5, s0_std=0.1)
+    y, s = gpu_prefill(ins, 64, cuda_device)
+    yo, so = oracle_prefill(ins)
+    # the sequential kernel computes in fp32 throughout: fp32 inputs meet 1e-4
+    tol = TOL[dtype]
+    assert rel_err(y, yo) <= tol, rel_err(y, yo)
+    assert rel_err(s, so) <= tol, rel_err(s, so)
+
+
+@pytest.mark.parametrize("mode", ["null", "inplace"])
+def test_prefill_short_t_state_modes(cuda_device, mode):
+    ins = gdn_inputs.make_inputs(1, 20, 2, 4, 128, 128, BF16, seed=8, s0_std=0.1)
+    y, s = gpu_prefill(ins, 32, cuda_device, state_mode=mode)
+    yo, so = oracle_prefill(ins, zero_state=(mode == "null"))
+    assert rel_err(y, yo) <= TOL[BF16]
+    assert rel_err(s, so) <= TOL[BF16]
+
+
+def test_prefill_short_and_chunked_paths_agree(cuda_device):
+    """T = 32 (sequential kernel) then one more token, against T = 33 in one
+    call (chunked tensor-core path): the same rule on both sides of the switch."""
+    ins = gdn_inputs.make_inputs(1, 33, 2, 4, 128, 128, BF16, seed=33, s0_std=0.1)
+    y, s = gpu_prefill(ins, 32, cuda_device)
+    a = {n: t[:, :32] if n != "s0" else t for n, t in ins.items()}
+    ya, sa = gpu_prefill(a, 32, cuda_device)
+    b = {n: t[:, 32:].contiguous() if n != "s0" else torch.from_numpy(sa)
+         for n, t in ins.items()}
+    yb, sb = gpu_prefill(b, 32, cuda_device)
+    yo, so = oracle_prefill(ins)
+    assert rel_err(np.concatenate([ya, yb], axis=1), yo) <= TOL[BF16]
+    assert rel_err(sb, so) <= TOL[BF16]
+    assert rel_err(y, yo) <= TOL[BF16]
+    assert rel_err(s, so) <= TOL[BF16]
+
+
 FULL = ["prefill_t4096", "prefill_b4_t2048", "prefill_t65536"]
 
 
