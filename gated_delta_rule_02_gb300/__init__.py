@@ -37,6 +37,8 @@ GDN_ERR_NOALLOC_LIMIT = -7
 GDN_NOALLOC_SCRATCH_BYTES = 32 << 20
 GDN_DTYPE_F32 = 0
 GDN_DTYPE_BF16 = 1
+GDN_OPT_TILED_HEADS = 1
+GDN_OPT_LOG_GATE = 2
 
 _DTYPES = {torch.float32: GDN_DTYPE_F32, torch.bfloat16: GDN_DTYPE_BF16}
 _lock = threading.Lock()
@@ -72,6 +74,10 @@ def lib() -> ctypes.CDLL:
             L.gdn_device_status.restype = i
             L.gdn_prefill_noalloc.argtypes = [vp] * 8 + [i] * 8 + [vp]
             L.gdn_prefill_noalloc.restype = i
+            L.gdn_prefill_ex.argtypes = [vp] * 8 + [i] * 8 + [vp, sz, vp, i]
+            L.gdn_prefill_ex.restype = i
+            L.gdn_decode_step_ex.argtypes = [vp] * 8 + [i] * 6 + [vp, i]
+            L.gdn_decode_step_ex.restype = i
             _lib = L
     return _lib
 
@@ -115,8 +121,9 @@ def _check(tensors, dtype, device):
 
 
 def gdn_prefill(q, k, v, g, beta, state_in, state_out, y, chunk, workspace=None,
-                stream=None):
-    """Enqueue ``gdn_prefill`` (include/gdn.h) on ``stream`` (default: current)."""
+                stream=None, options=0):
+    """Enqueue ``gdn_prefill`` (include/gdn.h) on ``stream`` (default: current);
+    with ``options`` (GDN_OPT_* bits) ``gdn_prefill_ex``."""
     dt = q.dtype
     if dt not in _DTYPES:
         raise ValueError(f"unsupported dtype {dt}")
@@ -129,12 +136,15 @@ def gdn_prefill(q, k, v, g, beta, state_in, state_out, y, chunk, workspace=None,
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib().gdn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
-                           _ptr(state_in), _ptr(state_out), _ptr(y),
-                           B, T, Hk, Hv, Dk, Dv, int(chunk), _DTYPES[dt],
-                           _ptr(workspace), ws_bytes, _stream_handle(stream, dev))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in), _ptr(state_out),
+            _ptr(y), B, T, Hk, Hv, Dk, Dv, int(chunk), _DTYPES[dt], _ptr(workspace), ws_bytes,
+            _stream_handle(stream, dev))
+    if options:
+        st = lib().gdn_prefill_ex(*args, int(options))
+    else:
+        st = lib().gdn_prefill(*args)
     if st != GDN_OK:
-        raise GdnError(st, "gdn_prefill")
+        raise GdnError(st, "gdn_prefill_ex" if options else "gdn_prefill")
 
 
 def gdn_prefill_noalloc(q, k, v, g, beta, state_in, state_out, y, chunk, stream=None):
@@ -156,8 +166,9 @@ def gdn_prefill_noalloc(q, k, v, g, beta, state_in, state_out, y, chunk, stream=
         raise GdnError(st, "gdn_prefill_noalloc")
 
 
-def gdn_decode_step(q, k, v, g, beta, state_in, state_out, y, stream=None):
-    """Enqueue ``gdn_decode_step`` (include/gdn.h) on ``stream`` (default: current)."""
+def gdn_decode_step(q, k, v, g, beta, state_in, state_out, y, stream=None, options=0):
+    """Enqueue ``gdn_decode_step`` (include/gdn.h) on ``stream`` (default: current);
+    with ``options`` (GDN_OPT_* bits) ``gdn_decode_step_ex``."""
     dt = q.dtype
     if dt not in _DTYPES:
         raise ValueError(f"unsupported dtype {dt}")
@@ -166,28 +177,30 @@ def gdn_decode_step(q, k, v, g, beta, state_in, state_out, y, stream=None):
     _check([("state_in", state_in), ("state_out", state_out)], torch.float32, dev)
     B, _, Hk, Dk = q.shape
     Hv, Dv = v.shape[2], v.shape[3]
-    st = lib().gdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
-                               _ptr(state_in), _ptr(state_out), _ptr(y),
-                               B, Hk, Hv, Dk, Dv, _DTYPES[dt],
-                               _stream_handle(stream, dev))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in), _ptr(state_out),
+            _ptr(y), B, Hk, Hv, Dk, Dv, _DTYPES[dt], _stream_handle(stream, dev))
+    if options:
+        st = lib().gdn_decode_step_ex(*args, int(options))
+    else:
+        st = lib().gdn_decode_step(*args)
     if st != GDN_OK:
-        raise GdnError(st, "gdn_decode_step")
+        raise GdnError(st, "gdn_decode_step_ex" if options else "gdn_decode_step")
 
 
-def prefill(q, k, v, g, beta, state_in=None, chunk=64, stream=None):
+def prefill(q, k, v, g, beta, state_in=None, chunk=64, stream=None, options=0):
     """Run the prefill; returns ``(y, state_out)`` (new tensors)."""
     B, T, Hk, Dk = q.shape
     Hv, Dv = v.shape[2], v.shape[3]
     y = torch.empty((B, T, Hv, Dv), dtype=q.dtype, device=q.device)
     state_out = torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=q.device)
-    gdn_prefill(q, k, v, g, beta, state_in, state_out, y, chunk, stream=stream)
+    gdn_prefill(q, k, v, g, beta, state_in, state_out, y, chunk, stream=stream, options=options)
     return y, state_out
 
 
-def decode_step(q, k, v, g, beta, state, stream=None):
+def decode_step(q, k, v, g, beta, state, stream=None, options=0):
     """One decode step; ``state`` is updated in place, returns ``y``."""
     B = q.shape[0]
     Hv, Dv = v.shape[2], v.shape[3]
     y = torch.empty((B, 1, Hv, Dv), dtype=q.dtype, device=q.device)
-    gdn_decode_step(q, k, v, g, beta, state, state, y, stream=stream)
+    gdn_decode_step(q, k, v, g, beta, state, state, y, stream=stream, options=options)
     return y

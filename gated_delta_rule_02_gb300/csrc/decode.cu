@@ -35,12 +35,12 @@ __global__ void __launch_bounds__(kDecodeThreads)
 decode_kernel(const T* __restrict__ q, const T* __restrict__ k,
               const T* __restrict__ v, const T* __restrict__ g,
               const T* __restrict__ beta, const float* state_in,
-              float* state_out, T* __restrict__ y, int Hk, int Hv, float scale) {
+              float* state_out, T* __restrict__ y, int Hk, int Hv, int opts, float scale) {
   constexpr int D = kHeadDim;
   const int bh = blockIdx.x;
   const int b = bh / Hv;
   const int hv = bh - b * Hv;
-  const int hk = hv / (Hv / Hk);
+  const int hk = key_head(hv, Hk, Hv, opts);
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int rg = lane >> 3;   // row within a group of four
@@ -61,7 +61,7 @@ decode_kernel(const T* __restrict__ q, const T* __restrict__ k,
   kq += __shfl_xor_sync(0xffffffffu, kq, 2);
   kq += __shfl_xor_sync(0xffffffffu, kq, 4);
 
-  const float gt = to_f32(g[bh]);
+  const float gt = decay_of(to_f32(g[bh]), opts);
   const float bt = to_f32(beta[bh]);
   const float* Sin = state_in + (size_t)bh * D * D;
   float* Sout = state_out + (size_t)bh * D * D;
@@ -133,7 +133,7 @@ cudaError_t launch_decode_t(const DecodeArgs& a) {
       static_cast<const T*>(a.q), static_cast<const T*>(a.k),
       static_cast<const T*>(a.v), static_cast<const T*>(a.g),
       static_cast<const T*>(a.beta), a.state_in, a.state_out,
-      static_cast<T*>(a.y), a.Hk, a.Hv, scale);
+      static_cast<T*>(a.y), a.Hk, a.Hv, a.options, scale);
   return cudaGetLastError();
 }
 

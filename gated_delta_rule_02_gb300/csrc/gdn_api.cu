@@ -16,6 +16,11 @@ int check_common(int B, int T, int Hk, int Hv, int Dk, int Dv, int dtype) {
   return GDN_OK;
 }
 
+// Option bits this build understands (GDN_OPT_* in include/gdn.h).
+constexpr int kKnownOptions = GDN_OPT_TILED_HEADS | GDN_OPT_LOG_GATE;
+static_assert(GDN_OPT_TILED_HEADS == gdn::kOptTiledHeads && GDN_OPT_LOG_GATE == gdn::kOptLogGate,
+              "option bits");
+
 int check_pointers(const void* const* ptrs, int n) {
   for (int i = 0; i < n; ++i)
     if (ptrs[i] == nullptr) return GDN_ERR_INVALID;
@@ -36,12 +41,13 @@ size_t gdn_prefill_workspace_bytes(int B, int T, int Hk, int Hv, int Dk, int Dv,
   return gdn::prefill_simt_workspace_bytes(B, T, Hv, chunk);
 }
 
-int gdn_prefill(const void* q, const void* k, const void* v, const void* g,
-                const void* beta, const float* state_in, float* state_out, void* y,
-                int B, int T, int Hk, int Hv, int Dk, int Dv, int chunk, int dtype,
-                void* workspace, size_t workspace_bytes, void* stream) {
+int gdn_prefill_ex(const void* q, const void* k, const void* v, const void* g,
+                   const void* beta, const float* state_in, float* state_out, void* y,
+                   int B, int T, int Hk, int Hv, int Dk, int Dv, int chunk, int dtype,
+                   void* workspace, size_t workspace_bytes, void* stream, int options) {
   int st = check_common(B, T, Hk, Hv, Dk, Dv, dtype);
   if (st != GDN_OK) return st;
+  if (options & ~kKnownOptions) return GDN_ERR_UNSUPPORTED;
   if (chunk != 16 && chunk != 32 && chunk != 64) return GDN_ERR_UNSUPPORTED;
   const void* req[] = {q, k, v, g, beta, state_out, y};
   st = check_pointers(req, 7);
@@ -53,7 +59,7 @@ int gdn_prefill(const void* q, const void* k, const void* v, const void* g,
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDN_ERR_ALIGNMENT;
   }
   gdn::PrefillArgs a{q, k, v, g, beta, state_in, state_out, y, B, T, Hk, Hv, chunk,
-                     dtype, workspace, workspace_bytes,
+                     dtype, options, workspace, workspace_bytes,
                      static_cast<cudaStream_t>(stream)};
   cudaError_t e = T <= gdn::kShortT       ? gdn::launch_prefill_short(a)
                   : dtype == GDN_DTYPE_BF16 ? gdn::launch_prefill_tc(a)
@@ -61,19 +67,36 @@ int gdn_prefill(const void* q, const void* k, const void* v, const void* g,
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+int gdn_prefill(const void* q, const void* k, const void* v, const void* g,
+                const void* beta, const float* state_in, float* state_out, void* y,
+                int B, int T, int Hk, int Hv, int Dk, int Dv, int chunk, int dtype,
+                void* workspace, size_t workspace_bytes, void* stream) {
+  return gdn_prefill_ex(q, k, v, g, beta, state_in, state_out, y, B, T, Hk, Hv, Dk, Dv, chunk,
+                        dtype, workspace, workspace_bytes, stream, 0);
+}
+
+int gdn_decode_step_ex(const void* q, const void* k, const void* v, const void* g,
+                       const void* beta, const float* state_in, float* state_out,
+                       void* y, int B, int Hk, int Hv, int Dk, int Dv, int dtype,
+                       void* stream, int options) {
+  int st = check_common(B, 1, Hk, Hv, Dk, Dv, dtype);
+  if (st != GDN_OK) return st;
+  if (options & ~kKnownOptions) return GDN_ERR_UNSUPPORTED;
+  const void* req[] = {q, k, v, g, beta, state_in, state_out, y};
+  st = check_pointers(req, 8);
+  if (st != GDN_OK) return st;
+  gdn::DecodeArgs a{q, k, v, g, beta, state_in, state_out, y, B, Hk, Hv, dtype, options,
+                    static_cast<cudaStream_t>(stream)};
+  cudaError_t e = gdn::launch_decode(a);
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 int gdn_decode_step(const void* q, const void* k, const void* v, const void* g,
                     const void* beta, const float* state_in, float* state_out,
                     void* y, int B, int Hk, int Hv, int Dk, int Dv, int dtype,
                     void* stream) {
-  int st = check_common(B, 1, Hk, Hv, Dk, Dv, dtype);
-  if (st != GDN_OK) return st;
-  const void* req[] = {q, k, v, g, beta, state_in, state_out, y};
-  st = check_pointers(req, 8);
-  if (st != GDN_OK) return st;
-  gdn::DecodeArgs a{q, k, v, g, beta, state_in, state_out, y, B, Hk, Hv, dtype,
-                    static_cast<cudaStream_t>(stream)};
-  cudaError_t e = gdn::launch_decode(a);
-  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  return gdn_decode_step_ex(q, k, v, g, beta, state_in, state_out, y, B, Hk, Hv, Dk, Dv, dtype,
+                            stream, 0);
 }
 
 int gdn_device_status(int clear) {
@@ -86,7 +109,7 @@ const char* gdn_status_string(int status) {
   switch (status) {
     case GDN_OK: return "ok";
     case GDN_ERR_INVALID: return "invalid argument (null pointer, size <= 0 or Hv % Hk != 0)";
-    case GDN_ERR_UNSUPPORTED: return "unsupported shape, chunk or dtype (Dk = Dv = 128, chunk 16/32/64, f32/bf16)";
+    case GDN_ERR_UNSUPPORTED: return "unsupported shape, chunk, dtype or option (Dk = Dv = 128, chunk 16/32/64, f32/bf16)";
     case GDN_ERR_ALIGNMENT: return "pointer not 16-byte aligned (workspace: 256-byte)";
     case GDN_ERR_WORKSPACE: return "workspace missing or smaller than gdn_prefill_workspace_bytes()";
     case GDN_ERR_CUDA: return "CUDA launch error";

@@ -11,6 +11,19 @@ namespace gdn {
 
 constexpr int kHeadDim = 128;  // Dk = Dv = 128 is the compiled head size
 
+// Input conventions selected by the options word of the *_ex entry points
+// (same bits as GDN_OPT_* in include/gdn.h).
+constexpr int kOptTiledHeads = 1;  // key head of value head hv is hv % Hk (else hv / (Hv/Hk))
+constexpr int kOptLogGate = 2;     // g holds log-decays; the decay is exp(g)
+
+__host__ __device__ __forceinline__ int key_head(int hv, int Hk, int Hv, int opts) {
+  return (opts & kOptTiledHeads) ? hv % Hk : hv / (Hv / Hk);
+}
+// The multiplicative decay from a stored gate value.
+__device__ __forceinline__ float decay_of(float gate, int opts) {
+  return (opts & kOptLogGate) ? exp2f(gate * 1.4426950408889634f) : gate;
+}
+
 struct PrefillArgs {
   const void* q;
   const void* k;
@@ -21,6 +34,7 @@ struct PrefillArgs {
   float* state_out;
   void* y;
   int B, T, Hk, Hv, chunk, dtype;
+  int options;  // kOpt* bits
   void* workspace;
   size_t workspace_bytes;
   cudaStream_t stream;
@@ -36,6 +50,7 @@ struct DecodeArgs {
   float* state_out;
   void* y;
   int B, Hk, Hv, dtype;
+  int options;  // kOpt* bits
   cudaStream_t stream;
 };
 

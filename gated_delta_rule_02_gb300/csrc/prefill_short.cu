@@ -37,7 +37,7 @@ short_prefill_kernel(const T* __restrict__ q, const T* __restrict__ k,
                      const T* __restrict__ v, const T* __restrict__ g,
                      const T* __restrict__ beta, const float* state_in,
                      float* state_out, T* __restrict__ y, int Tlen, int Hk, int Hv,
-                     float scale) {
+                     int opts, float scale) {
   constexpr int D = kHeadDim;
   extern __shared__ float4 smem_f4[];
   float* ks = reinterpret_cast<float*>(smem_f4);  // [Tlen][D]
@@ -50,7 +50,7 @@ short_prefill_kernel(const T* __restrict__ q, const T* __restrict__ k,
   const int bh = blockIdx.x;
   const int b = bh / Hv;
   const int hv = bh - b * Hv;
-  const int hk = hv / (Hv / Hk);
+  const int hk = key_head(hv, Hk, Hv, opts);
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
@@ -75,7 +75,7 @@ short_prefill_kernel(const T* __restrict__ q, const T* __restrict__ k,
     if (lane == 0) {
       const size_t gi = ((size_t)b * Tlen + t) * Hv + hv;
       kqs[t] = kq;
-      gs[t] = to_f32(g[gi]);
+      gs[t] = decay_of(to_f32(g[gi]), opts);
       bs[t] = to_f32(beta[gi]);
     }
   }
@@ -166,7 +166,7 @@ cudaError_t launch_short_t(const PrefillArgs& a) {
   short_prefill_kernel<T, 2><<<a.B * a.Hv, kShortThreads, smem, a.stream>>>(
       static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v),
       static_cast<const T*>(a.g), static_cast<const T*>(a.beta), a.state_in, a.state_out,
-      static_cast<T*>(a.y), a.T, a.Hk, a.Hv, scale);
+      static_cast<T*>(a.y), a.T, a.Hk, a.Hv, a.options, scale);
   return cudaGetLastError();
 }
 

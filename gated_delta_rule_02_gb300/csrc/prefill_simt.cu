@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(kThreads)
 intra_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
                   const T* __restrict__ v, const T* __restrict__ g,
                   const T* __restrict__ beta, float* __restrict__ ws,
-                  float* __restrict__ wsG, int T_, int Hk, int Hv, int N) {
+                  float* __restrict__ wsG, int T_, int Hk, int Hv, int N, int opts) {
   constexpr int D = kHeadDim;
   constexpr int LC = C + 1;
   extern __shared__ float sm[];
@@ -62,7 +62,7 @@ intra_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
   const int bh = blockIdx.y;
   const int b = bh / Hv;
   const int hv = bh - b * Hv;
-  const int hk = hv / (Hv / Hk);
+  const int hk = key_head(hv, Hk, Hv, opts);
   const int t0 = n * C;
   const int c = min(C, T_ - t0);
   const int tid = threadIdx.x;
@@ -83,7 +83,7 @@ intra_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
   }
   for (int t = tid; t < C; t += kThreads) {
     const size_t tok = (size_t)b * T_ + t0 + t;
-    sg[t] = t < c ? to_f32(g[tok * Hv + hv]) : 1.f;
+    sg[t] = t < c ? decay_of(to_f32(g[tok * Hv + hv]), opts) : 1.f;
     sb[t] = t < c ? to_f32(beta[tok * Hv + hv]) : 0.f;
   }
   __syncthreads();
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kThreads)
 scan_simt_kernel(const T* __restrict__ k, const float* __restrict__ ws,
                  const float* __restrict__ wsG, const float* state_in,
                  float* state_out, T* __restrict__ y, int T_, int Hk, int Hv,
-                 int N, float scale) {
+                 int N, int opts, float scale) {
   constexpr int D = kHeadDim;
   constexpr int R = kRows;
   extern __shared__ float sm[];
@@ -187,7 +187,7 @@ scan_simt_kernel(const T* __restrict__ k, const float* __restrict__ ws,
   const int bh = blockIdx.y;
   const int b = bh / Hv;
   const int hv = bh - b * Hv;
-  const int hk = hv / (Hv / Hk);
+  const int hk = key_head(hv, Hk, Hv, opts);
   const int r0 = tile * R;
   const int tid = threadIdx.x;
   const size_t sbase = (size_t)bh * D * D + (size_t)r0 * D;
@@ -269,13 +269,13 @@ cudaError_t launch_t(const PrefillArgs& a) {
   intra_simt_kernel<T, C><<<dim3(N, BH), kThreads, smem_i, a.stream>>>(
       static_cast<const T*>(a.q), static_cast<const T*>(a.k),
       static_cast<const T*>(a.v), static_cast<const T*>(a.g),
-      static_cast<const T*>(a.beta), ws, wsG, a.T, a.Hk, a.Hv, N);
+      static_cast<const T*>(a.beta), ws, wsG, a.T, a.Hk, a.Hv, N, a.options);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const float scale = 1.0f / sqrtf((float)kHeadDim);
   scan_simt_kernel<T, C><<<dim3(kHeadDim / kRows, BH), kThreads, smem_s, a.stream>>>(
       static_cast<const T*>(a.k), ws, wsG, a.state_in, a.state_out,
-      static_cast<T*>(a.y), a.T, a.Hk, a.Hv, N, scale);
+      static_cast<T*>(a.y), a.T, a.Hk, a.Hv, N, a.options, scale);
   return cudaGetLastError();
 }
 

@@ -257,6 +257,7 @@ struct PrepParams {
   const bf16* beta;
   float* wsGC;
   int T, Hk, Hv, NT, BH;
+  int opts;  // kOpt* bits
   // y_loc / sqrt(Dk) goes straight to y ([B, T, Hv, 128], 64-token boxes); the
   // scan then adds Qh S^T / sqrt(Dk) to it.
   const CUtensorMap* tm_y;
@@ -269,7 +270,7 @@ struct PrepParams {
 template <int C>
 __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw, int cta_rank,
                                           int n_ctas, int* flags) {
-  const int T = P.T, Hk = P.Hk, Hv = P.Hv, NT = P.NT, BH = P.BH;
+  const int T = P.T, Hk = P.Hk, Hv = P.Hv, NT = P.NT, BH = P.BH, opts = P.opts;
   const bf16* __restrict__ g = P.g;
   const bf16* __restrict__ beta = P.beta;
   float* __restrict__ wsGC = P.wsGC;
@@ -339,7 +340,7 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
   // K and V of tile `lin` (io 0 also posts the byte count of K, Q and V) ...
   auto load_kv = [&](int lin) {
     const int bh = head_of(lin), n = tile_of(lin);
-    const int b = bh / Hv, hv = bh - b * Hv, hk = hv / (Hv / Hk), t0 = n * kTile;
+    const int b = bh / Hv, hv = bh - b * Hv, hk = key_head(hv, Hk, Hv, opts), t0 = n * kTile;
     if (io == 0) mbar_expect_tx(bar_tma, 6 * 8192);
     if (io < 2) tma_load_4d(sbase + kOffKQ + io * 16384, P.tm_k, bar_tma, 64 * io, hk, t0, b);
     else tma_load_4d(sbase + kOffV + (io - 2) * 8192, P.tm_v, bar_tma, 64 * (io - 2), hv, t0, b);
@@ -347,14 +348,16 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
   // ... and its Q (io 0 and 1).
   auto load_q = [&](int lin) {
     const int bh = head_of(lin), n = tile_of(lin);
-    const int b = bh / Hv, hv = bh - b * Hv, hk = hv / (Hv / Hk), t0 = n * kTile;
+    const int b = bh / Hv, hv = bh - b * Hv, hk = key_head(hv, Hk, Hv, opts), t0 = n * kTile;
     if (io < 2) tma_load_4d(sbase + kOffKQ + io * 16384 + 8192, P.tm_q, bar_tma, 64 * io, hk, t0, b);
   };
   // Gate and beta of token `tid` of a tile, read one tile ahead into registers
   // as raw bf16 bits (converted when used, so the load is not waited for here).
-  uint16_t g_next = 0x3f80, b_next = 0;  // 1.0 and 0.0
+  // Padded tokens: decay 1 (gate 1.0, or log-gate 0.0), beta 0.
+  const uint16_t g_pad = (opts & kOptLogGate) ? 0x0000 : 0x3f80;
+  uint16_t g_next = g_pad, b_next = 0;
   auto load_gates = [&](int lin) {
-    g_next = 0x3f80;
+    g_next = g_pad;
     b_next = 0;
     if (tid < 64 && lin < total) {
       const int bh = head_of(lin), n = tile_of(lin);
@@ -404,7 +407,7 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
     // Warm L2 with the next tile's K, Q and V rows (one 256-byte token row of
     // one tensor per thread, as plain prefetches that leave the TMA unit free).
     const int nbh = head_of(next), nb = nbh / Hv, nhv = nbh - nb * Hv;
-    const int nhk = nhv / (Hv / Hk), tok = tile_of(next) * kTile + (tid & (kTile - 1));
+    const int nhk = key_head(nhv, Hk, Hv, opts), tok = tile_of(next) * kTile + (tid & (kTile - 1));
     if (tok < T) {
       const int which = tid / kTile;  // 0: K, 1: Q, 2: V
       const bf16* base = which == 0 ? P.k : (which == 1 ? P.q : P.v);
@@ -425,9 +428,9 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
   if (tid < 64) {
     const int t = tid, lane = tid & 31;
     bta[t] = bt_cur;  // padded tokens: g = 1, beta = 0
-    const float gv = gv_cur;
-    graw[t] = gv;
-    float l = fmaxf(lg2(gv), -1000.f);
+    // log2 of the decay (clamped: a vanishing decay underflows the products to 0)
+    float l = fmaxf((opts & kOptLogGate) ? gv_cur * 1.4426950408889634f : lg2(gv_cur), -1000.f);
+    graw[t] = (opts & kOptLogGate) ? ex2(l) : gv_cur;
     constexpr int kSeg = C < 32 ? C : 32;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -754,10 +757,10 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                const __grid_constant__ CUtensorMap tm_us, const __grid_constant__ CUtensorMap tm_y,
                const bf16* kin, const bf16* qin, const bf16* vin, const bf16* __restrict__ g,
                const bf16* __restrict__ beta, float* __restrict__ wsGC, int T, int Hk, int Hv,
-               int NT, int BH, float scale) {
+               int NT, int BH, int opts, float scale) {
   extern __shared__ uint8_t smem_raw[];
   const PrepParams P{kin, qin, vin, &tm_k, &tm_q, &tm_v, &tm_a1s, &tm_us, g, beta, wsGC,
-                     T, Hk, Hv, NT, BH, &tm_y, scale};
+                     T, Hk, Hv, NT, BH, opts, &tm_y, scale};
   prep_role<C>(P, smem_raw, blockIdx.x, gridDim.x, nullptr);
 }
 
@@ -817,8 +820,8 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
                                              const CUtensorMap* tm_uy, const CUtensorMap* tm_yred,
                                              const float* wsGC, const int* flags,
                                              const float* state_in, float* state_out, int T,
-                                             int Hk, int Hv, int NT, int bh, float scale,
-                                             uint8_t* smem_raw) {
+                                             int Hk, int Hv, int NT, int bh, int opts,
+                                             float scale, uint8_t* smem_raw) {
   using SM = Scan128Smem;
   constexpr int kCt = kTile / C;
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -827,7 +830,7 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
   __shared__ uint32_t qtmem_sh;
   const uint32_t sbase = smem_u32(sm);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = bh / Hv, hv = bh - b * Hv, hk = hv / (Hv / Hk);
+  const int b = bh / Hv, hv = bh - b * Hv, hk = key_head(hv, Hk, Hv, opts);
   const int NC = (T + C - 1) / C;
   auto bar = [&](int i) { return smem_u32(&qbars[i]); };
 
@@ -1122,14 +1125,14 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_k,
                      const bf16* qin, const bf16* vin, const bf16* __restrict__ g,
                      const bf16* __restrict__ beta, float* __restrict__ wsGC, int* flags,
                      const float* state_in, float* state_out, int T, int Hk, int Hv, int NT,
-                     int BH, float scale) {
+                     int BH, int opts, float scale) {
   extern __shared__ uint8_t smem_raw[];
   if ((int)blockIdx.x < BH) {
     scan_role128<C>(&tm_a1s, &tm_k, &tm_us, &tm_yred, wsGC, flags, state_in, state_out, T, Hk,
-                    Hv, NT, blockIdx.x, scale, smem_raw);
+                    Hv, NT, blockIdx.x, opts, scale, smem_raw);
   } else {
     const PrepParams P{kin, qin, vin, &tm_k, &tm_q, &tm_v, &tm_a1s, &tm_us, g, beta, wsGC,
-                       T, Hk, Hv, NT, BH, &tm_y, scale};
+                       T, Hk, Hv, NT, BH, opts, &tm_y, scale};
     prep_role<C>(P, smem_raw, blockIdx.x - BH, gridDim.x - BH, flags);
   }
 }
@@ -1141,10 +1144,10 @@ scan_head_kernel(const __grid_constant__ CUtensorMap tm_a1s, const __grid_consta
                  const __grid_constant__ CUtensorMap tm_us,
                  const __grid_constant__ CUtensorMap tm_yred, const float* __restrict__ wsGC,
                  const float* state_in, float* state_out, int T, int Hk, int Hv, int NT,
-                 float scale) {
+                 int opts, float scale) {
   extern __shared__ uint8_t smem_raw[];
   scan_role128<C>(&tm_a1s, &tm_k, &tm_us, &tm_yred, wsGC, nullptr, state_in, state_out, T, Hk,
-                  Hv, NT, blockIdx.x, scale, smem_raw);
+                  Hv, NT, blockIdx.x, opts, scale, smem_raw);
 }
 
 // ============================================================================
@@ -1260,7 +1263,7 @@ cudaError_t launch_c(const PrefillArgs& a) {
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, fused_prefill_kernel<C>, tk, tq, tv, ta1s, tus, ty, tyred, k,
                               q, v, g, beta, wsGC, flags, a.state_in, a.state_out, a.T, a.Hk,
-                              a.Hv, NT, BH, scale);
+                              a.Hv, NT, BH, a.options, scale);
   }
 
   // Split path: the persistent prep kernel on every SM, then one scan CTA per head.
@@ -1272,11 +1275,13 @@ cudaError_t launch_c(const PrefillArgs& a) {
   if (e != cudaSuccess) return e;
   const int prep_ctas = std::min(sms, (BH * NT + kPrepGroups - 1) / kPrepGroups);
   prep_tc_kernel<C><<<prep_ctas, kPrepThreads, kPrepSmem, a.stream>>>(
-      tk, tq, tv, ta1s, tus, ty, k, q, v, g, beta, wsGC, a.T, a.Hk, a.Hv, NT, BH, scale);
+      tk, tq, tv, ta1s, tus, ty, k, q, v, g, beta, wsGC, a.T, a.Hk, a.Hv, NT, BH, a.options,
+      scale);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   scan_head_kernel<C><<<BH, kFusedThreads, Scan128Smem::kTotal, a.stream>>>(
-      ta1s, tk, tus, tyred, wsGC, a.state_in, a.state_out, a.T, a.Hk, a.Hv, NT, scale);
+      ta1s, tk, tus, tyred, wsGC, a.state_in, a.state_out, a.T, a.Hk, a.Hv, NT, a.options,
+      scale);
   return cudaGetLastError();
 }
 

@@ -65,6 +65,22 @@ extern "C" {
 #define GDN_DTYPE_BF16  1
 
 /*
+ * Input conventions for gdn_prefill_ex / gdn_decode_step_ex (bits of
+ * `options`; 0 gives gdn_prefill / gdn_decode_step exactly).
+ *   GDN_OPT_TILED_HEADS  value head hv reads key head hv % Hk ("tiled"), instead
+ *                        of hv / (Hv/Hk) ("grouped").  ferrox-core `gdn_chunk.rs`
+ *                        names both maps (HeadMap::Tiled, HeadMap::Grouped) but
+ *                        shows no body for either; these are the two usual GQA
+ *                        layouts, the grouped one matching metaltile-std "Layouts".
+ *   GDN_OPT_LOG_GATE     g holds log-decays (<= 0) and the decay is exp(g), as in
+ *                        ferrox-core `delta_chunk` (`a = exp(g)`), instead of the
+ *                        multiplicative gate of metaltile-std.
+ * Any other bit gives GDN_ERR_UNSUPPORTED.
+ */
+#define GDN_OPT_TILED_HEADS 1
+#define GDN_OPT_LOG_GATE    2
+
+/*
  * Bytes of device workspace gdn_prefill needs for this shape (0 if none).
  * Returns 0 as well for arguments gdn_prefill would reject.
  */
@@ -97,6 +113,13 @@ GDN_API int gdn_prefill(const void *q, const void *k, const void *v, const void 
                 int B, int T, int Hk, int Hv, int Dk, int Dv, int chunk,
                 int dtype, void *workspace, size_t workspace_bytes, void *stream);
 
+/* gdn_prefill with input conventions `options` (GDN_OPT_* bits above). */
+GDN_API int gdn_prefill_ex(const void *q, const void *k, const void *v, const void *g,
+                const void *beta, const float *state_in, float *state_out, void *y,
+                int B, int T, int Hk, int Hv, int Dk, int Dv, int chunk,
+                int dtype, void *workspace, size_t workspace_bytes, void *stream,
+                int options);
+
 /*
  * Decode: one token (T = 1) of every (b, hv) through the rule, streaming
  * the state once (the single-step recurrence above; row packing after the
@@ -111,6 +134,12 @@ GDN_API int gdn_decode_step(const void *q, const void *k, const void *v, const v
                     const void *beta, const float *state_in, float *state_out,
                     void *y, int B, int Hk, int Hv, int Dk, int Dv, int dtype,
                     void *stream);
+
+/* gdn_decode_step with input conventions `options` (GDN_OPT_* bits above). */
+GDN_API int gdn_decode_step_ex(const void *q, const void *k, const void *v, const void *g,
+                const void *beta, const float *state_in, float *state_out, void *y,
+                int B, int Hk, int Hv, int Dk, int Dv, int dtype, void *stream,
+                int options);
 
 /*
  * Prefill for callers that cannot allocate device memory.  This entry point

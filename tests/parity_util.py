@@ -26,9 +26,9 @@ def to_device(ins, dev):
     return {n: t.to(dev) for n, t in ins.items() if t is not None}
 
 
-def gpu_prefill(ins, chunk, dev, state_mode="given"):
+def gpu_prefill(ins, chunk, dev, state_mode="given", options=0):
     """state_mode: 'given' (s0 -> new state_out), 'null' (state_in = NULL),
-    'inplace' (state_in is state_out)."""
+    'inplace' (state_in is state_out).  options: GDN_OPT_* bits."""
     import gated_delta_rule_02_gb300 as gdn
     d = to_device(ins, dev)
     B, T, Hk, Dk = d["q"].shape
@@ -39,7 +39,8 @@ def gpu_prefill(ins, chunk, dev, state_mode="given"):
     else:
         s_in = None if state_mode == "null" else d["s0"]
         s_out = torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=dev)
-    gdn.gdn_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], s_in, s_out, y, chunk)
+    gdn.gdn_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], s_in, s_out, y, chunk,
+                    options=options)
     torch.cuda.synchronize(dev)
     return y.float().cpu().numpy(), s_out.cpu().numpy()
 

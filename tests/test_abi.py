@@ -127,3 +127,10 @@ def test_binding_fails_loudly_without_library(monkeypatch):
     monkeypatch.setattr(gdn, "LIB_PATH", os.path.join(ROOT, "no", "such", "libgdn.so"))
     with pytest.raises(RuntimeError):
         gdn.lib()
+
+
+@pytest.mark.parametrize("options", [4, 8, -1, 1 << 20])
+def test_ex_entry_points_reject_unknown_options(L, options):
+    assert L.gdn_prefill_ex(*prefill_args(), options) == gdn.GDN_ERR_UNSUPPORTED
+    dec = [FAKE] * 8 + [1, 1, 2, 128, 128, 1, None]
+    assert L.gdn_decode_step_ex(*dec, options) == gdn.GDN_ERR_UNSUPPORTED

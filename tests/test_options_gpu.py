@@ -1,0 +1,95 @@
+"""Input conventions of the *_ex entry points (GDN_OPT_*), on every path,
+against the oracle fed the equivalent inputs:
+
+- tiled head map (value head hv reads key head hv % Hk): the oracle runs the
+  same problem with q and k expanded to one key head per value head;
+- log-decay gates (the decay is exp(g)): the oracle gets exp of the stored
+  log-gates, taken in fp64.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gdn_inputs
+import oracle
+from parity_util import TOL, gpu_prefill, rel_err
+
+pytestmark = pytest.mark.gpu
+
+F32, BF16 = torch.float32, torch.bfloat16
+TILED, LOGG = 1, 2
+
+
+def _oracle_equivalent(ins, options):
+    """Inputs for the oracle (grouped heads, multiplicative gates) that define
+    the same problem as `ins` read under `options`."""
+    out = dict(ins)
+    Hk, Hv = ins["q"].shape[2], ins["v"].shape[2]
+    if options & TILED:
+        idx = torch.tensor([hv % Hk for hv in range(Hv)])
+        out["q"] = ins["q"][:, :, idx]
+        out["k"] = ins["k"][:, :, idx]
+    if options & LOGG:
+        out["g"] = torch.exp(ins["g"].double())
+    return out
+
+
+def _with_log_gates(ins):
+    out = dict(ins)
+    out["g"] = torch.log(ins["g"].double()).to(ins["g"].dtype)
+    return out
+
+
+def _run(ins, options, chunk, dev):
+    gins = _with_log_gates(ins) if options & LOGG else ins
+    y, s = gpu_prefill(gins, chunk, dev, options=options)
+    o = _oracle_equivalent(gins, options)
+    yo, so = oracle.gdn_sequential(o["q"], o["k"], o["v"], o["g"], o["beta"], o["s0"])
+    return y, s, yo, so
+
+
+CASES = [
+    # (B, T, Hk, Hv, chunk, dtype): the fused tensor-core path, the split
+    # launches (B*Hv = 64), the short-T kernel and the fp32 path
+    (1, 150, 2, 6, 32, BF16),
+    (2, 100, 16, 32, 64, BF16),
+    (2, 20, 4, 8, 64, BF16),
+    (1, 70, 2, 4, 32, F32),
+]
+
+
+@pytest.mark.parametrize("options", [TILED, LOGG, TILED | LOGG])
+@pytest.mark.parametrize("B,T,Hk,Hv,chunk,dtype", CASES)
+def test_prefill_options(cuda_device, options, B, T, Hk, Hv, chunk, dtype):
+    ins = gdn_inputs.make_inputs(B, T, Hk, Hv, 128, 128, dtype, seed=500 + T + Hv,
+                                 u_max=0.5, s0_std=0.1)
+    y, s, yo, so = _run(ins, options, chunk, cuda_device)
+    assert rel_err(y, yo) <= TOL[dtype], rel_err(y, yo)
+    assert rel_err(s, so) <= TOL[dtype], rel_err(s, so)
+
+
+def test_tiled_differs_from_grouped(cuda_device):
+    """The option changes the result (the two maps pair different heads)."""
+    ins = gdn_inputs.make_inputs(1, 40, 2, 4, 128, 128, BF16, seed=7, s0_std=0.1)
+    y1, s1 = gpu_prefill(ins, 32, cuda_device, options=0)
+    y2, s2 = gpu_prefill(ins, 32, cuda_device, options=TILED)
+    assert rel_err(y1, y2) > 0.05
+
+
+@pytest.mark.parametrize("options", [TILED, LOGG, TILED | LOGG])
+def test_decode_options(cuda_device, options):
+    import gated_delta_rule_02_gb300 as gdn
+    B, Hk, Hv = 3, 2, 6
+    ins = gdn_inputs.make_inputs(B, 1, Hk, Hv, 128, 128, BF16, seed=600 + options,
+                                 u_max=0.5, s0_std=0.1)
+    gins = _with_log_gates(ins) if options & LOGG else ins
+    d = {n: t.to(cuda_device) for n, t in gins.items()}
+    y = torch.empty((B, 1, Hv, 128), dtype=BF16, device=cuda_device)
+    s_out = torch.empty_like(d["s0"])
+    gdn.gdn_decode_step(d["q"], d["k"], d["v"], d["g"], d["beta"], d["s0"], s_out, y,
+                        options=options)
+    torch.cuda.synchronize(cuda_device)
+    o = _oracle_equivalent(gins, options)
+    yo, so = oracle.gdn_sequential(o["q"], o["k"], o["v"], o["g"], o["beta"], o["s0"])
+    assert rel_err(y.float().cpu().numpy(), yo) <= TOL[BF16]
+    assert rel_err(s_out.cpu().numpy(), so) <= TOL[BF16]
