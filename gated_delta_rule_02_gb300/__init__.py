@@ -39,6 +39,7 @@ GDN_DTYPE_F32 = 0
 GDN_DTYPE_BF16 = 1
 GDN_OPT_TILED_HEADS = 1
 GDN_OPT_LOG_GATE = 2
+GDN_OPT_L2NORM_QK = 4
 
 _DTYPES = {torch.float32: GDN_DTYPE_F32, torch.bfloat16: GDN_DTYPE_BF16}
 _lock = threading.Lock()

@@ -54,6 +54,25 @@ decode_kernel(const T* __restrict__ q, const T* __restrict__ k,
     load4(kp + 4 * sub + 32 * j, kr + 4 * j);
     load4(qp + 4 * sub + 32 * j, qr + 4 * j);
   }
+  if (opts & kOptL2NormQK) {  // the eight lanes of a row hold the whole vectors
+    float sk = 0.f, sq = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      sk = fmaf(kr[i], kr[i], sk);
+      sq = fmaf(qr[i], qr[i], sq);
+    }
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) {
+      sk += __shfl_xor_sync(0xffffffffu, sk, off);
+      sq += __shfl_xor_sync(0xffffffffu, sq, off);
+    }
+    const float fk = inv_norm(sk), fq = inv_norm(sq);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      kr[i] *= fk;
+      qr[i] *= fq;
+    }
+  }
   float kq = 0.f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) kq = fmaf(kr[i], qr[i], kq);

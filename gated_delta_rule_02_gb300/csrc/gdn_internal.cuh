@@ -15,10 +15,29 @@ constexpr int kHeadDim = 128;  // Dk = Dv = 128 is the compiled head size
 // (same bits as GDN_OPT_* in include/gdn.h).
 constexpr int kOptTiledHeads = 1;  // key head of value head hv is hv % Hk (else hv / (Hv/Hk))
 constexpr int kOptLogGate = 2;     // g holds log-decays; the decay is exp(g)
+constexpr int kOptL2NormQK = 4;    // every q and k row is used as x / |x|
 
 __host__ __device__ __forceinline__ int key_head(int hv, int Hk, int Hv, int opts) {
   return (opts & kOptTiledHeads) ? hv % Hk : hv / (Hv / Hk);
 }
+// 1/|x| from a row's sum of squares (a zero row stays zero).
+__device__ __forceinline__ float inv_norm(float sumsq) { return rsqrtf(fmaxf(sumsq, 1e-30f)); }
+
+// Normalise `rows` fp32 rows of D = 128 (row stride `ld` floats) in shared
+// memory, one warp per row; all `nthreads` threads of the block call this.
+__device__ __forceinline__ void l2norm_rows_f32(float* s, int rows, int ld, int tid, int nthreads) {
+  const int lane = tid & 31;
+  for (int r = tid >> 5; r < rows; r += nthreads >> 5) {
+    float* row = s + r * ld + 4 * lane;
+    float a = row[0], b = row[1], c = row[2], d = row[3];
+    float ss = a * a + b * b + c * c + d * d;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float f = inv_norm(ss);
+    row[0] = a * f; row[1] = b * f; row[2] = c * f; row[3] = d * f;
+  }
+}
+
 // The multiplicative decay from a stored gate value.
 __device__ __forceinline__ float decay_of(float gate, int opts) {
   return (opts & kOptLogGate) ? exp2f(gate * 1.4426950408889634f) : gate;

@@ -66,6 +66,21 @@ short_prefill_kernel(const T* __restrict__ q, const T* __restrict__ k,
     load4(k + kq_off, kk);
     load4(q + kq_off, qq);
     load4(v + v_off, vv);
+    if (opts & kOptL2NormQK) {
+      float sk = kk[0] * kk[0] + kk[1] * kk[1] + kk[2] * kk[2] + kk[3] * kk[3];
+      float sq = qq[0] * qq[0] + qq[1] * qq[1] + qq[2] * qq[2] + qq[3] * qq[3];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        sk += __shfl_xor_sync(0xffffffffu, sk, off);
+        sq += __shfl_xor_sync(0xffffffffu, sq, off);
+      }
+      const float fk = inv_norm(sk), fq = inv_norm(sq);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        kk[i] *= fk;
+        qq[i] *= fq;
+      }
+    }
     *reinterpret_cast<float4*>(ks + t * D + 4 * lane) = make_float4(kk[0], kk[1], kk[2], kk[3]);
     *reinterpret_cast<float4*>(qs + t * D + 4 * lane) = make_float4(qq[0], qq[1], qq[2], qq[3]);
     *reinterpret_cast<float4*>(vs + t * D + 4 * lane) = make_float4(vv[0], vv[1], vv[2], vv[3]);

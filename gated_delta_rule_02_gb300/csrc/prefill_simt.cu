@@ -87,6 +87,11 @@ intra_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
     sb[t] = t < c ? to_f32(beta[tok * Hv + hv]) : 0.f;
   }
   __syncthreads();
+  if (opts & kOptL2NormQK) {
+    l2norm_rows_f32(sK, c, kLd, tid, kThreads);
+    l2norm_rows_f32(sQ, c, kLd, tid, kThreads);
+    __syncthreads();
+  }
 
   // Step 2: prefix gates and decay ratios, both as products.
   if (tid < C) {
@@ -213,6 +218,10 @@ scan_simt_kernel(const T* __restrict__ k, const float* __restrict__ ws,
     }
     const float Gc = wsG[(size_t)bh * N + n];
     __syncthreads();
+    if (opts & kOptL2NormQK) {
+      l2norm_rows_f32(sK, c, D, tid, kThreads);
+      __syncthreads();
+    }
 
     // [SP | SQ][r][t'] = S[r] . PQ[t'], t' < 2C.
     for (int idx = tid; idx < R * 2 * C; idx += kThreads) {

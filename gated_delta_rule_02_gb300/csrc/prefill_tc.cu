@@ -103,6 +103,33 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
                     pack_bf16x2(f[6], f[7]));
 }
 
+// x / |x| for row `row` of a bf16 tile whose rows are split in two 128B-swizzled
+// 64-column halves `half_stride` bytes apart; the calling thread takes half
+// `half` and its lane partner (lane ^ 1) the other half.
+__device__ __forceinline__ void l2norm_row_sw128(uint8_t* base, int half_stride, int row,
+                                                 int half) {
+  uint8_t* hb = base + half * half_stride;
+  float ss = 0.f;
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    float v[8];
+    unpack8(*reinterpret_cast<const uint4*>(hb + sw128(row, 8 * ch)), v);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
+  }
+  ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+  const float f = inv_norm(ss);
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    uint4* p = reinterpret_cast<uint4*>(hb + sw128(row, 8 * ch));
+    float v[8];
+    unpack8(*p, v);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] *= f;
+    *p = pack8(v);
+  }
+}
+
 // ============================================================================
 // prep kernel
 // ============================================================================
@@ -466,6 +493,11 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
 
   ok = mbar_wait(bar_tma, it & 1);
   tma_pending = false;
+  if (opts & kOptL2NormQK) {  // rows 0-63 of each half are K, 64-127 Q
+    if (ok) l2norm_row_sw128(sm + kOffKQ, 16384, tid >> 1, tid & 1);
+    fence_proxy_async();
+    gsync();
+  }
   // G1: D[128 x 64] = [K; Q] K^T  (TMEM columns 0..63), issued outside the gate
   // warps.  The previous tile's last stores must have read A3 and X, which
   // this tile rewrites after G1.
@@ -803,7 +835,8 @@ enum : int {
   kQEmptyMN = kQFullMN + Scan128Smem::kStages,  // MMA commit
   kQFullQ = kQEmptyMN + Scan128Smem::kStages,
   kQEmptyQ = kQFullQ + Scan128Smem::kStages,    // 257: state group + the y-reducing thread
-  kQDs = kQEmptyQ + Scan128Smem::kStages,
+  kQKNorm = kQEmptyQ + Scan128Smem::kStages,    // 128: K rows of the MN stage normalised
+  kQDs = kQKNorm + Scan128Smem::kStages,
   kQY,
   kQM,                 // [2]
   kQSop = kQM + 2,     // 256
@@ -840,6 +873,7 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
       mbar_init(bar(kQEmptyMN + s), 1);
       mbar_init(bar(kQFullQ + s), 1);
       mbar_init(bar(kQEmptyQ + s), 257);
+      mbar_init(bar(kQKNorm + s), 128);
     }
     mbar_init(bar(kQDs), 1);
     mbar_init(bar(kQY), 1);
@@ -872,6 +906,12 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
   auto wait_mn = [&](int j) {
     const int n = j / kCt;
     return mbar_wait(bar(kQFullMN + n % SM::kStages), (n / SM::kStages) & 1);
+  };
+  // With L2-normalised keys the aux group rewrites each K tile first.
+  const bool knorm = (opts & kOptL2NormQK) != 0;
+  auto wait_knorm = [&](int j) {
+    const int n = j / kCt;
+    return mbar_wait(bar(kQKNorm + n % SM::kStages), (n / SM::kStages) & 1);
   };
   auto wait_q = [&](int j) {
     const int n = j / kCt;
@@ -938,7 +978,7 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
       // M^T of chunk j into tM(j & 1), once its tile's MN buffers have landed.
       auto issue_mt = [&](int j) {
         if (j % kCt == 0) {
-          if (!wait_mn(j)) return false;
+          if (!(knorm ? wait_knorm(j) : wait_mn(j))) return false;
           tc_fence_after();
         }
         const uint32_t off = ring_of(j) * SM::kMN + (j % kCt) * C * 128;
@@ -1060,9 +1100,21 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
       mbar_arrive(bar(kQMt + (j & 1)));
       return true;
     };
-    if (NC > 0) ok = convert(0);
+    // Normalise the K rows of the tile holding chunk j (64 rows, two threads
+    // per row), then release it to the issuer.
+    const int atid = tid - 320;  // 0..127 in the aux group
+    auto normalise_k = [&](int j) {
+      if (!wait_mn(j)) return false;
+      l2norm_row_sw128(sm + (mn_addr(j) - sbase) + SM::kOffK, 8192, atid >> 1, atid & 1);
+      fence_proxy_async();
+      mbar_arrive(bar(kQKNorm + ring_of(j)));
+      return true;
+    };
+    if (knorm && NC > 0) ok = normalise_k(0);
+    if (ok && NC > 0) ok = convert(0);
     for (int j = 0; j < NC && ok; ++j) {
       const int c = j % kCt;
+      if (knorm && j + 1 < NC && (j + 1) % kCt == 0 && !(ok = normalise_k(j + 1))) break;
       if (j + 1 < NC && !(ok = convert(j + 1))) break;
       // Y^T: lane v (value row), columns t < C.  Y / sqrt(Dk) goes, as bf16 and
       // transposed, into this chunk's Qh rows (dead once Y is complete) and is

@@ -75,10 +75,16 @@ extern "C" {
  *   GDN_OPT_LOG_GATE     g holds log-decays (<= 0) and the decay is exp(g), as in
  *                        ferrox-core `delta_chunk` (`a = exp(g)`), instead of the
  *                        multiplicative gate of metaltile-std.
+ *   GDN_OPT_L2NORM_QK    every q and k row (Dk values) is used as x / |x|,
+ *                        computed in fp32 from the stored values (the step
+ *                        before the recurrence in the MLX PR's test inputs); a
+ *                        zero row stays zero.  For bf16 inputs the normalised
+ *                        rows enter the tensor-core products rounded to bf16.
  * Any other bit gives GDN_ERR_UNSUPPORTED.
  */
 #define GDN_OPT_TILED_HEADS 1
 #define GDN_OPT_LOG_GATE    2
+#define GDN_OPT_L2NORM_QK   4
 
 /*
  * Bytes of device workspace gdn_prefill needs for this shape (0 if none).

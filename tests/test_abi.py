@@ -129,7 +129,7 @@ def test_binding_fails_loudly_without_library(monkeypatch):
         gdn.lib()
 
 
-@pytest.mark.parametrize("options", [4, 8, -1, 1 << 20])
+@pytest.mark.parametrize("options", [8, 16, -1, 1 << 20])
 def test_ex_entry_points_reject_unknown_options(L, options):
     assert L.gdn_prefill_ex(*prefill_args(), options) == gdn.GDN_ERR_UNSUPPORTED
     dec = [FAKE] * 8 + [1, 1, 2, 128, 128, 1, None]

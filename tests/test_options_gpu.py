@@ -4,7 +4,9 @@ against the oracle fed the equivalent inputs:
 - tiled head map (value head hv reads key head hv % Hk): the oracle runs the
   same problem with q and k expanded to one key head per value head;
 - log-decay gates (the decay is exp(g)): the oracle gets exp of the stored
-  log-gates, taken in fp64.
+  log-gates, taken in fp64;
+- L2-normalised q, k: the oracle gets the stored rows divided by their norm
+  in fp64 (a zero row stays zero).
 """
 import numpy as np
 import pytest
@@ -17,7 +19,7 @@ from parity_util import TOL, gpu_prefill, rel_err
 pytestmark = pytest.mark.gpu
 
 F32, BF16 = torch.float32, torch.bfloat16
-TILED, LOGG = 1, 2
+TILED, LOGG, L2N = 1, 2, 4
 
 
 def _oracle_equivalent(ins, options):
@@ -31,6 +33,11 @@ def _oracle_equivalent(ins, options):
         out["k"] = ins["k"][:, :, idx]
     if options & LOGG:
         out["g"] = torch.exp(ins["g"].double())
+    if options & L2N:
+        for n in ("q", "k"):
+            x = out[n].double()
+            nrm = x.norm(dim=-1, keepdim=True)
+            out[n] = x / torch.where(nrm > 0, nrm, torch.ones_like(nrm))
     return out
 
 
@@ -58,7 +65,7 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("options", [TILED, LOGG, TILED | LOGG])
+@pytest.mark.parametrize("options", [TILED, LOGG, L2N, TILED | LOGG | L2N])
 @pytest.mark.parametrize("B,T,Hk,Hv,chunk,dtype", CASES)
 def test_prefill_options(cuda_device, options, B, T, Hk, Hv, chunk, dtype):
     ins = gdn_inputs.make_inputs(B, T, Hk, Hv, 128, 128, dtype, seed=500 + T + Hv,
@@ -76,12 +83,34 @@ def test_tiled_differs_from_grouped(cuda_device):
     assert rel_err(y1, y2) > 0.05
 
 
-@pytest.mark.parametrize("options", [TILED, LOGG, TILED | LOGG])
+def _unnormalised(ins, scale=3.0):
+    """q and k rows of varied length (the stored rows are unit length)."""
+    out = dict(ins)
+    gen = torch.Generator().manual_seed(11)
+    for n in ("q", "k"):
+        f = 0.25 + scale * torch.rand(ins[n].shape[:-1] + (1,), generator=gen)
+        out[n] = (ins[n].double() * f).to(ins[n].dtype)
+    return out
+
+
+@pytest.mark.parametrize("B,T,Hk,Hv,chunk,dtype", CASES)
+def test_prefill_l2norm_of_unnormalised_rows(cuda_device, B, T, Hk, Hv, chunk, dtype):
+    """Rows of length 0.25..3.25 in, unit rows used; one key row is zero."""
+    ins = _unnormalised(gdn_inputs.make_inputs(B, T, Hk, Hv, 128, 128, dtype, seed=700 + T,
+                                               u_max=0.5, s0_std=0.1))
+    ins["k"][0, T // 2, 0] = 0
+    y, s, yo, so = _run(ins, L2N, chunk, cuda_device)
+    assert np.all(np.isfinite(y)) and np.all(np.isfinite(s))
+    assert rel_err(y, yo) <= TOL[dtype], rel_err(y, yo)
+    assert rel_err(s, so) <= TOL[dtype], rel_err(s, so)
+
+
+@pytest.mark.parametrize("options", [TILED, LOGG, L2N, TILED | LOGG | L2N])
 def test_decode_options(cuda_device, options):
     import gated_delta_rule_02_gb300 as gdn
     B, Hk, Hv = 3, 2, 6
-    ins = gdn_inputs.make_inputs(B, 1, Hk, Hv, 128, 128, BF16, seed=600 + options,
-                                 u_max=0.5, s0_std=0.1)
+    ins = _unnormalised(gdn_inputs.make_inputs(B, 1, Hk, Hv, 128, 128, BF16,
+                                               seed=600 + options, u_max=0.5, s0_std=0.1))
     gins = _with_log_gates(ins) if options & LOGG else ins
     d = {n: t.to(cuda_device) for n, t in gins.items()}
     y = torch.empty((B, 1, Hv, 128), dtype=BF16, device=cuda_device)
