@@ -37,11 +37,13 @@ GDN_ERR_NOALLOC_LIMIT = -7
 GDN_NOALLOC_SCRATCH_BYTES = 32 << 20
 GDN_DTYPE_F32 = 0
 GDN_DTYPE_BF16 = 1
+GDN_DTYPE_F16 = 2
 GDN_OPT_TILED_HEADS = 1
 GDN_OPT_LOG_GATE = 2
 GDN_OPT_L2NORM_QK = 4
 
-_DTYPES = {torch.float32: GDN_DTYPE_F32, torch.bfloat16: GDN_DTYPE_BF16}
+_DTYPES = {torch.float32: GDN_DTYPE_F32, torch.bfloat16: GDN_DTYPE_BF16,
+           torch.float16: GDN_DTYPE_F16}
 _lock = threading.Lock()
 _lib = None
 

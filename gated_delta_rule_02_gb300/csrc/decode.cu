@@ -160,6 +160,7 @@ cudaError_t launch_decode_t(const DecodeArgs& a) {
 
 cudaError_t launch_decode(const DecodeArgs& a) {
   if (a.dtype == 0) return launch_decode_t<float>(a);
+  if (a.dtype == 2) return launch_decode_t<__half>(a);
   return launch_decode_t<__nv_bfloat16>(a);
 }
 

@@ -12,7 +12,8 @@ int check_common(int B, int T, int Hk, int Hv, int Dk, int Dv, int dtype) {
   if (B <= 0 || T <= 0 || Hk <= 0 || Hv <= 0 || Dk <= 0 || Dv <= 0) return GDN_ERR_INVALID;
   if (Hv % Hk != 0) return GDN_ERR_INVALID;
   if (Dk != gdn::kHeadDim || Dv != gdn::kHeadDim) return GDN_ERR_UNSUPPORTED;
-  if (dtype != GDN_DTYPE_F32 && dtype != GDN_DTYPE_BF16) return GDN_ERR_UNSUPPORTED;
+  if (dtype != GDN_DTYPE_F32 && dtype != GDN_DTYPE_BF16 && dtype != GDN_DTYPE_F16)
+    return GDN_ERR_UNSUPPORTED;
   return GDN_OK;
 }
 
@@ -110,7 +111,7 @@ const char* gdn_status_string(int status) {
   switch (status) {
     case GDN_OK: return "ok";
     case GDN_ERR_INVALID: return "invalid argument (null pointer, size <= 0 or Hv % Hk != 0)";
-    case GDN_ERR_UNSUPPORTED: return "unsupported shape, chunk, dtype or option (Dk = Dv = 128, chunk 16/32/64, f32/bf16)";
+    case GDN_ERR_UNSUPPORTED: return "unsupported shape, chunk, dtype or option (Dk = Dv = 128, chunk 16/32/64, f32/bf16/f16)";
     case GDN_ERR_ALIGNMENT: return "pointer not 16-byte aligned (workspace: 256-byte)";
     case GDN_ERR_WORKSPACE: return "workspace missing or smaller than gdn_prefill_workspace_bytes()";
     case GDN_ERR_CUDA: return "CUDA launch error";

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -97,11 +98,16 @@ cudaError_t launch_decode(const DecodeArgs& a);
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
 
 template <typename T>
 __device__ __forceinline__ T from_f32(float x);
 template <>
 __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __half from_f32<__half>(float x) {
+  return __float2half_rn(x);
+}
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
   return __float2bfloat16_rn(x);
@@ -117,6 +123,12 @@ __device__ __forceinline__ void load4(const __nv_bfloat16* p, float* out) {
   const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&t.x);
   const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&t.y);
   const float2 a = __bfloat1622float2(lo), b = __bfloat1622float2(hi);
+  out[0] = a.x; out[1] = a.y; out[2] = b.x; out[3] = b.y;
+}
+__device__ __forceinline__ void load4(const __half* p, float* out) {
+  const uint2 t = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&t.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&t.y));
   out[0] = a.x; out[1] = a.y; out[2] = b.x; out[3] = b.y;
 }
 

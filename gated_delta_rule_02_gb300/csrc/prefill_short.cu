@@ -189,6 +189,7 @@ cudaError_t launch_short_t(const PrefillArgs& a) {
 
 cudaError_t launch_prefill_short(const PrefillArgs& a) {
   if (a.dtype == 0) return launch_short_t<float>(a);
+  if (a.dtype == 2) return launch_short_t<__half>(a);
   return launch_short_t<__nv_bfloat16>(a);
 }
 

@@ -308,6 +308,7 @@ size_t prefill_simt_workspace_bytes(int B, int T, int Hv, int chunk) {
 
 cudaError_t launch_prefill_simt(const PrefillArgs& a) {
   if (a.dtype == 0) return launch_dtype<float>(a);
+  if (a.dtype == 2) return launch_dtype<__half>(a);
   return launch_dtype<__nv_bfloat16>(a);
 }
 

@@ -63,6 +63,9 @@ extern "C" {
 /* Element types of q, k, v, g, beta and y. */
 #define GDN_DTYPE_F32   0
 #define GDN_DTYPE_BF16  1
+/* fp16: decode and T <= 32 on the row-packed kernels; longer prefills on the
+ * fp32 CUDA-core chunked path (the tensor-core path is bf16 only). */
+#define GDN_DTYPE_F16   2
 
 /*
  * Input conventions for gdn_prefill_ex / gdn_decode_step_ex (bits of

@@ -93,6 +93,7 @@ def prefill_args(**over):
     (dict(chunk=48), gdn.GDN_ERR_UNSUPPORTED),
     (dict(chunk=128), gdn.GDN_ERR_UNSUPPORTED),
     (dict(dtype=7), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(dtype=3), gdn.GDN_ERR_UNSUPPORTED),
     (dict(k=FAKE + 4), gdn.GDN_ERR_ALIGNMENT),
     (dict(state_in=FAKE + 8), gdn.GDN_ERR_ALIGNMENT),
     (dict(workspace=None), gdn.GDN_ERR_WORKSPACE),
@@ -109,7 +110,7 @@ def test_prefill_rejects_bad_arguments_on_host(L, over, expect):
     (dict(B=0), gdn.GDN_ERR_INVALID),
     (dict(Hk=2, Hv=3), gdn.GDN_ERR_INVALID),
     (dict(Dk=96), gdn.GDN_ERR_UNSUPPORTED),
-    (dict(dtype=2), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(dtype=3), gdn.GDN_ERR_UNSUPPORTED),
     (dict(y=FAKE + 2), gdn.GDN_ERR_ALIGNMENT),
 ])
 def test_decode_rejects_bad_arguments_on_host(L, over, expect):
