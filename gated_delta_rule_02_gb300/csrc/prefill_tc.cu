@@ -529,11 +529,13 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
     const int cs = (t / C) * C, bt = t >> 4;
     const float gt = gpw[t];
     const int cbeg = (warp >> 2) * 32;
+    float vv[2][16];  // both 16-column blocks, one TMEM round trip
+    tmem_ld16(tmem + lane_base + cbeg, vv[0]);
+    tmem_ld16(tmem + lane_base + cbeg + 16, vv[1]);
+    tmem_wait_ld();
 #pragma unroll
     for (int c0 = cbeg; c0 < cbeg + 32; c0 += 16) {
-      float v[16];
-      tmem_ld16(tmem + lane_base + c0, v);
-      tmem_wait_ld();
+      const float* v = vv[(c0 - cbeg) >> 4];
       // A 16-column block lies wholly inside or outside t's chunk (16 | C); it
       // is before, on or after t's own 16-block.
       const int cb = c0 >> 4, tt = t & 15;
@@ -656,18 +658,24 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
     const uint32_t half_stride = top ? 16384 : 8192;
     const int cbeg = (warp >> 2) * 64;
 #pragma unroll
-    for (int col = cbeg; col < cbeg + 64; col += 16) {
-      float v[16];
-      tmem_ld16(src + col, v);
+    for (int c2 = cbeg; c2 < cbeg + 64; c2 += 32) {
+      float vv[2][16];  // two 16-column blocks per TMEM round trip
+      tmem_ld16(src + c2, vv[0]);
+      tmem_ld16(src + c2 + 16, vv[1]);
       tmem_wait_ld();
-      const uint32_t atom = bdst + (col >> 6) * 8192;
-      st_sm16(sm, atom + sw128(t, col & 63), pack8(v));
-      st_sm16(sm, atom + sw128(t, (col & 63) + 8), pack8(v + 8));
 #pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] *= scale;
-      const uint32_t hs = stage + (col >> 6) * half_stride;
-      st_sm16(sm, hs + sw128(t, col & 63), pack8(v));
-      st_sm16(sm, hs + sw128(t, (col & 63) + 8), pack8(v + 8));
+      for (int hh = 0; hh < 2; ++hh) {
+        const int col = c2 + 16 * hh;
+        float* v = vv[hh];
+        const uint32_t atom = bdst + (col >> 6) * 8192;
+        st_sm16(sm, atom + sw128(t, col & 63), pack8(v));
+        st_sm16(sm, atom + sw128(t, (col & 63) + 8), pack8(v + 8));
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] *= scale;
+        const uint32_t hs = stage + (col >> 6) * half_stride;
+        st_sm16(sm, hs + sw128(t, col & 63), pack8(v));
+        st_sm16(sm, hs + sw128(t, (col & 63) + 8), pack8(v + 8));
+      }
     }
   }
   if (ok) fence_proxy_async();
@@ -720,24 +728,30 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
     const float gt = gpw[t];
     const int cbeg = (warp >> 2) * 64;
 #pragma unroll
-    for (int col = cbeg; col < cbeg + 64; col += 16) {
-      float v[16];
-      tmem_ld16(src + col, v);
+    for (int c2 = cbeg; c2 < cbeg + 64; c2 += 32) {
+      float vv[2][16];  // two 16-column blocks per TMEM round trip
+      tmem_ld16(src + c2, vv[0]);
+      tmem_ld16(src + c2 + 16, vv[1]);
       tmem_wait_ld();
-      if (top) {  // Qh = G q - G M P  (step 7, state-free part)
-        const uint8_t* qa = sm + kOffKQ + (col >> 6) * 16384 + 8192;
-        float q[16];
-        unpack8(*reinterpret_cast<const uint4*>(qa + sw128(t, col & 63)), q);
-        unpack8(*reinterpret_cast<const uint4*>(qa + sw128(t, (col & 63) + 8)), q + 8);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = gt * q[j] - v[j];
-      } else {
+      for (int hh = 0; hh < 2; ++hh) {
+        const int col = c2 + 16 * hh;
+        float* v = vv[hh];
+        if (top) {  // Qh = G q - G M P  (step 7, state-free part)
+          const uint8_t* qa = sm + kOffKQ + (col >> 6) * 16384 + 8192;
+          float q[16];
+          unpack8(*reinterpret_cast<const uint4*>(qa + sw128(t, col & 63)), q);
+          unpack8(*reinterpret_cast<const uint4*>(qa + sw128(t, (col & 63) + 8)), q + 8);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] *= P.yscale;
+          for (int j = 0; j < 16; ++j) v[j] = gt * q[j] - v[j];
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] *= P.yscale;
+        }
+        const uint32_t hs = stage + (col >> 6) * 8192;
+        st_sm16(sm, hs + sw128(t, col & 63), pack8(v));
+        st_sm16(sm, hs + sw128(t, (col & 63) + 8), pack8(v + 8));
       }
-      const uint32_t hs = stage + (col >> 6) * 8192;
-      st_sm16(sm, hs + sw128(t, col & 63), pack8(v));
-      st_sm16(sm, hs + sw128(t, (col & 63) + 8), pack8(v + 8));
     }
   }
   if (ok && tid < 64 / C) wsGC[tile_id * 4 + tid] = gc[tid];
