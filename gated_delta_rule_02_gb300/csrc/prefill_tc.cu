@@ -312,7 +312,9 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
                 grp * kPrepGroupSmem;
   const uint32_t sbase = smem_u32(sm);
   const uint32_t bar_tma = smem_u32(&bars[grp][0]), bar_mma = smem_u32(&bars[grp][1]);
-  const int sync_id = 1 + 2 * grp, gates_id = 2 + 2 * grp;  // named barriers of the group
+  // Named barriers of the group: the whole group, its gate warps (0-3) and the
+  // two warps of the prefix sum.
+  const int sync_id = 1 + 2 * grp, gates_id = 2 + 2 * grp, carry_id = 5 + grp;
   float* X = reinterpret_cast<float*>(sm + kOffB);               // 64 x 68 fp32
   float* TL = reinterpret_cast<float*>(sm + kOffTL);             // 64 x 68 fp32
   float* Zs = reinterpret_cast<float*>(sm + kOffZ);              // 32 x 32 fp32
@@ -323,8 +325,7 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
   float* sfac = gpw + 64;   // 2^(lam[end of t's 16-block] - lam_t)
   float* rfac = sfac + 64;  // [64][4]: 2^(lam_t - lam[end of block b]), b before t's block
   float* gc = rfac + 256;   // G at each chunk's end
-  float* graw = gc + 4;     // g_t
-  float* gdiag = graw + 64; // [64][17]: Gam[t][j] for j in t's 16-block, j <= t (products)
+  float* gdiag = gc + 4;    // [64][kLdGd]: Gam[t][j] for j in t's 16-block, j <= t
   auto gsync = [&]() { named_bar_sync(sync_id, kPrepGroupThreads); };
   // Group-wide AND of ok (sticky: a group that failed a wait stops).
   auto gsync_and = [&](bool v) {
@@ -430,34 +431,39 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
   const int next = lin + ngroups;
   const float gv_cur = bits_to_f32(g_next), bt_cur = bits_to_f32(b_next);
   load_gates(next);
-  if (next < total && tid < 3 * kTile) {
-    // Warm L2 with the next tile's K, Q and V rows (one 256-byte token row of
-    // one tensor per thread, as plain prefetches that leave the TMA unit free).
+  // Warm L2 with the next tile's K, Q and V rows: warps 2-7 (u = tid - 64), one
+  // 256-byte token row of one tensor per thread, as plain prefetches that leave
+  // the TMA unit free.  Issued while those warps wait for the inverse's first
+  // stage, which only warps 0-1 work on.
+  auto prefetch_next = [&]() {
+    const int u = tid - 64;
+    if (next >= total || u < 0 || u >= 3 * kTile) return;
     const int nbh = head_of(next), nb = nbh / Hv, nhv = nbh - nb * Hv;
-    const int nhk = key_head(nhv, Hk, Hv, opts), tok = tile_of(next) * kTile + (tid & (kTile - 1));
+    const int nhk = key_head(nhv, Hk, Hv, opts), tok = tile_of(next) * kTile + (u & (kTile - 1));
     if (tok < T) {
-      const int which = tid / kTile;  // 0: K, 1: Q, 2: V
+      const int which = u / kTile;  // 0: K, 1: Q, 2: V
       const bf16* base = which == 0 ? P.k : (which == 1 ? P.q : P.v);
       const int heads = which == 2 ? Hv : Hk, hh = which == 2 ? nhv : nhk;
       const char* row = reinterpret_cast<const char*>(base + (((size_t)nb * T + tok) * heads + hh) * kD);
       asm volatile("prefetch.global.L2 [%0];" ::"l"(row) : "memory");
       asm volatile("prefetch.global.L2 [%0];" ::"l"(row + 128) : "memory");
     }
-  }
+  };
 
   // Gates (step 2).  Padded tokens take g = 1, beta = 0.  Decay products are
   // carried as chunk-local prefix sums lam of log2 g: G_t = 2^lam_t and
   // Gam[t][j] = 2^(lam_t - lam_j) (j <= t) -- never a quotient, so a vanishing
   // product underflows to 0.  Gam is used factored per 16-token block b:
-  // Across 16-token blocks, Gam[t][j] = rfac[t][b(j)] * sfac[j] with the
+  // across 16-token blocks, Gam[t][j] = rfac[t][b(j)] * sfac[j] with the
   // block end as the split point, so both factors are products of decays (<= 1);
-  // inside a block it is 2^(lam_t - lam_j) directly.
+  // inside a block it is 2^(lam_t - lam_j) directly.  Warps 0-1 form the
+  // prefix sums (one token per thread); warps 0-3 then derive the tables (two
+  // threads per token).
   if (tid < 64) {
     const int t = tid, lane = tid & 31;
     bta[t] = bt_cur;  // padded tokens: g = 1, beta = 0
     // log2 of the decay (clamped: a vanishing decay underflows the products to 0)
     float l = fmaxf((opts & kOptLogGate) ? gv_cur * 1.4426950408889634f : lg2(gv_cur), -1000.f);
-    graw[t] = (opts & kOptLogGate) ? ex2(l) : gv_cur;
     constexpr int kSeg = C < 32 ? C : 32;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -466,29 +472,34 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
     }
     if constexpr (C == 64) {
       if (tid == 31) carry_sh[grp] = l;
-      named_bar_sync(gates_id, 64);
+      named_bar_sync(carry_id, 64);
       if (tid >= 32) l += carry_sh[grp];
     }
     lam[t] = l;
-    named_bar_sync(gates_id, 64);
-    {  // in-block ratios as products of decays (ferrox-core "The algebra")
-      float r = 1.f;
-      float* gd = gdiag + t * kLdGd;
-      gd[t & 15] = 1.f;
-      for (int j = t - 1; j >= (t & ~15); --j) {
-        r *= graw[j + 1];
-        gd[j & 15] = r;
-      }
+  }
+  if (tid < 128) {
+    named_bar_sync(gates_id, 128);
+    const int t = tid >> 1, p = tid & 1;
+    const float l = lam[t];
+    const int tb = t & ~15, tt = t & 15;
+    float* gd = gdiag + t * kLdGd + 8 * p;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int j = 8 * p + e;  // in-block ratios (entries past t are never read)
+      gd[e] = j <= tt ? ex2(l - lam[tb + j]) : 0.f;
     }
     const int ce = (t / C) * C + C - 1, cs = (t / C) * C;
     const float lend = lam[ce];
-    gsuf[t] = ex2(lend - l);
-    gpw[t] = ex2(l);
-    sfac[t] = ex2(lam[(t | 15)] - l);
+    if (p == 0) {
+      gsuf[t] = ex2(lend - l);
+      gpw[t] = ex2(l);
+      sfac[t] = ex2(lam[(t | 15)] - l);
+    } else {
 #pragma unroll
-    for (int bb = 0; bb < 4; ++bb)
-      rfac[t * 4 + bb] = (bb * 16 >= cs && bb < (t >> 4)) ? ex2(l - lam[bb * 16 + 15]) : 0.f;
-    if (t == ce) gc[t / C] = ex2(lend);
+      for (int bb = 0; bb < 4; ++bb)
+        rfac[t * 4 + bb] = (bb * 16 >= cs && bb < (t >> 4)) ? ex2(l - lam[bb * 16 + 15]) : 0.f;
+      if (t == ce) gc[t / C] = ex2(lend);
+    }
   }
 
   ok = mbar_wait(bar_tma, it & 1);
@@ -499,10 +510,10 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
     gsync();
   }
   // G1: D[128 x 64] = [K; Q] K^T  (TMEM columns 0..63), issued outside the gate
-  // warps.  The previous tile's last stores must have read A3 and X, which
+  // warps (lane 1 of warp 4).  The previous tile's last stores must have read A3 and X, which
   // this tile rewrites after G1.
   if (io >= 0) bulk_wait_read_all();
-  if (ok && tid == 64) {
+  if (ok && tid == 129) {
     tc_fence_after();
     const uint32_t id1 = idesc_bf16(128, 64, false, false);
 #pragma unroll
@@ -578,41 +589,43 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
 
   // Step 4: T_L = (I + L)^-1.  Step 5 needs no second inverse:
   // (I + A)^-1 diag(beta) = diag(beta) (Gam . T_L) for A[t][j] = beta_t Gam[t][j] KK^T[t][j].
+  prefetch_next();
   if (ok) invert_unit_lower<C>(X, TL, Zs, tid, gsync);
   else gsync();
 
   // A2 = [T_L; diag(beta) (Gam . T_L)]: 128 rows x 64 K-cols, K-major 128B swizzle.
+  // Thread: 8 columns (col0..col0+7) of T_L rows r0 and r0+32, written as rows
+  // t and 64+t of A2.
   if (ok) {
-    for (int idx = tid; idx < 128 * 8; idx += kPrepGroupThreads) {
-      const int row = idx >> 3, col0 = (idx & 7) * 8;
-      const int t = row & 63;
+    const int col0 = (tid & 7) * 8, r0 = tid >> 3, bj = col0 >> 4;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int t = r0 + 32 * i;
       const float4 a = *reinterpret_cast<const float4*>(TL + t * kLdX + col0);
       const float4 c4 = *reinterpret_cast<const float4*>(TL + t * kLdX + col0 + 4);
       float v[8] = {a.x, a.y, a.z, a.w, c4.x, c4.y, c4.z, c4.w};
-      if (row >= 64) {
-        // T_L is zero above the diagonal and across chunks (rfac is 0 there too).
-        const int bj = col0 >> 4;
-        float f[8];
-        if (bj < (t >> 4)) {
-          const float rb = bta[t] * rfac[t * 4 + bj];
-          const float4 s0 = *reinterpret_cast<const float4*>(sfac + col0);
-          const float4 s1 = *reinterpret_cast<const float4*>(sfac + col0 + 4);
-          f[0] = s0.x * rb; f[1] = s0.y * rb; f[2] = s0.z * rb; f[3] = s0.w * rb;
-          f[4] = s1.x * rb; f[5] = s1.y * rb; f[6] = s1.z * rb; f[7] = s1.w * rb;
-        } else {
-          const float bt = bta[t];
-          const float* gd = gdiag + t * kLdGd + (col0 & 15);
-          const float4 s0 = *reinterpret_cast<const float4*>(gd);
-          const float4 s1 = *reinterpret_cast<const float4*>(gd + 4);
-          f[0] = s0.x * bt; f[1] = s0.y * bt; f[2] = s0.z * bt; f[3] = s0.w * bt;
-          f[4] = s1.x * bt; f[5] = s1.y * bt; f[6] = s1.z * bt; f[7] = s1.w * bt;
+      st_sm16(sm, kOffB + sw128(t, col0), pack8(v));
+      // T_L is zero above the diagonal and across chunks (rfac is 0 there too).
+      float f[8];
+      const float bt = bta[t];
+      if (bj < (t >> 4)) {
+        const float rb = bt * rfac[t * 4 + bj];
+        const float4 s0 = *reinterpret_cast<const float4*>(sfac + col0);
+        const float4 s1 = *reinterpret_cast<const float4*>(sfac + col0 + 4);
+        f[0] = s0.x * rb; f[1] = s0.y * rb; f[2] = s0.z * rb; f[3] = s0.w * rb;
+        f[4] = s1.x * rb; f[5] = s1.y * rb; f[6] = s1.z * rb; f[7] = s1.w * rb;
+      } else {
+        const float* gd = gdiag + t * kLdGd + (col0 & 15);
+        const float4 s0 = *reinterpret_cast<const float4*>(gd);
+        const float4 s1 = *reinterpret_cast<const float4*>(gd + 4);
+        f[0] = s0.x * bt; f[1] = s0.y * bt; f[2] = s0.z * bt; f[3] = s0.w * bt;
+        f[4] = s1.x * bt; f[5] = s1.y * bt; f[6] = s1.z * bt; f[7] = s1.w * bt;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = (col0 + e <= t) ? f[e] : 0.f;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] *= f[e];
+        for (int e = 0; e < 8; ++e) f[e] = (col0 + e <= t) ? f[e] : 0.f;
       }
-      st_sm16(sm, kOffB + sw128(row, col0), pack8(v));
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] *= f[e];
+      st_sm16(sm, kOffB + sw128(64 + t, col0), pack8(v));
     }
     fence_proxy_async();
   }
@@ -782,7 +795,9 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
       tma_pending = true;
     }
   }
-  ok = gsync_and(ok);
+  // No group barrier here: ok is uniform since the last one, and the next
+  // tile's gate tables are free (their last reader was the epilogue above), so
+  // the gate warps start on the next tile while the I/O threads issue its loads.
   }  // tile loop
 
   if (io >= 0) bulk_wait_read_all();  // shared memory must outlive the last stores' reads
