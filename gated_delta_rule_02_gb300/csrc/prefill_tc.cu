@@ -213,9 +213,11 @@ __device__ __forceinline__ void warp_store_16x8(float* D, int ldd, const float* 
 //   32 x 32 blocks (C >= 32)  T_10 = -T_11 X_10 T_00      (per 16-block pair)
 //   64 x 64 (C = 64)          T_BA = -T_BB X_BA T_AA      (32-block halves)
 // The block products run on warp-level tf32 MMAs; the group's 256 threads call
-// this (u = thread index in the group, sync = the group's barrier).
-template <int C, typename Sync>
-__device__ void invert_unit_lower(const float* X, float* Tm, float* Zs, int u, Sync sync) {
+// this (u = thread index in the group, sync = the group's barrier); `first`
+// runs right after the first barrier.
+template <int C, typename Sync, typename First>
+__device__ void invert_unit_lower(const float* X, float* Tm, float* Zs, int u, Sync sync,
+                                  First first) {
   for (int idx = u; idx < 64 * 64; idx += kPrepGroupThreads) {
     const int r = idx >> 6, c = idx & 63;
     if ((c >> 4) > (r >> 4) || (c / C) != (r / C)) Tm[r * kLdX + c] = 0.f;
@@ -239,6 +241,7 @@ __device__ void invert_unit_lower(const float* X, float* Tm, float* Zs, int u, S
     for (int r = 0; r < 16; ++r) Tm[(base + r) * kLdX + base + jj] = x[r];
   }
   sync();
+  first();
   const int w = u >> 5, lane = u & 31;
   if constexpr (C >= 32) {
     // Pairs (0,1) and (2,3): warp w < 4 handles pair w/2, columns 8*(w%2)..
@@ -315,6 +318,7 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
   // Named barriers of the group: the whole group, its gate warps (0-3) and the
   // two warps of the prefix sum.
   const int sync_id = 1 + 2 * grp, gates_id = 2 + 2 * grp, carry_id = 5 + grp;
+  const int xready_id = 7 + grp;  // warps 0, 1, 4, 5: X is complete
   float* X = reinterpret_cast<float*>(sm + kOffB);               // 64 x 68 fp32
   float* TL = reinterpret_cast<float*>(sm + kOffTL);             // 64 x 68 fp32
   float* Zs = reinterpret_cast<float*>(sm + kOffZ);              // 32 x 32 fp32
@@ -584,14 +588,19 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
     }
   }
   stores_complete();  // the previous tile's stores (long done by now)
-  ok = gsync_and(ok);
-  if (ok) publish();
 
   // Step 4: T_L = (I + L)^-1.  Step 5 needs no second inverse:
   // (I + A)^-1 diag(beta) = diag(beta) (Gam . T_L) for A[t][j] = beta_t Gam[t][j] KK^T[t][j].
+  // The inverse's first stage (warps 0-1) needs only X, written by warps 0, 1, 4
+  // and 5; the A3 builders (warps 2, 3, 6, 7) finish meanwhile and meet the
+  // group at the inverse's first barrier, after which io 0 releases the
+  // previous tile.  The inverse runs (on whatever X holds) even after a failed
+  // wait, so every thread passes the same barriers; ok is made uniform after it.
+  if ((warp & 3) < 2) named_bar_sync(xready_id, 128);
   prefetch_next();
-  if (ok) invert_unit_lower<C>(X, TL, Zs, tid, gsync);
-  else gsync();
+  invert_unit_lower<C>(X, TL, Zs, tid, gsync, [&]() {
+    if (ok) publish();
+  });
 
   // A2 = [T_L; diag(beta) (Gam . T_L)]: 128 rows x 64 K-cols, K-major 128B swizzle.
   // Thread: 8 columns (col0..col0+7) of T_L rows r0 and r0+32, written as rows
