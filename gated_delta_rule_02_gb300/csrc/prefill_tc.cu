@@ -304,7 +304,7 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
   const bf16* __restrict__ g = P.g;
   const bf16* __restrict__ beta = P.beta;
   float* __restrict__ wsGC = P.wsGC;
-  __shared__ uint64_t bars[kPrepGroups][2];
+  __shared__ uint64_t bars[kPrepGroups][4];
   __shared__ uint32_t tmem_base_sh;
   __shared__ float carry_sh[kPrepGroups];
   __shared__ int abort_sh[kPrepGroups];
@@ -315,10 +315,16 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
                 grp * kPrepGroupSmem;
   const uint32_t sbase = smem_u32(sm);
   const uint32_t bar_tma = smem_u32(&bars[grp][0]), bar_mma = smem_u32(&bars[grp][1]);
+  // G2 and G3 completions of the P stream (bar_p) and of the U stream (bar_u):
+  // two per tile each, so the first wait of a tile is on parity 0, the second on 1.
+  const uint32_t bar_p = smem_u32(&bars[grp][2]), bar_u = smem_u32(&bars[grp][3]);
   // Named barriers of the group: the whole group, its gate warps (0-3) and the
   // two warps of the prefix sum.
   const int sync_id = 1 + 2 * grp, gates_id = 2 + 2 * grp, carry_id = 5 + grp;
-  const int xready_id = 7 + grp;  // warps 0, 1, 4, 5: X is complete
+  // Warps 0, 1, 4, 5 (TMEM lanes 0-63: X, later the P stream) and warps 2, 3, 6,
+  // 7 (lanes 64-127: the U stream).
+  const int pstream_id = 7 + grp, ustream_id = 9 + grp;
+  const bool pstream = (warp & 3) < 2;
   float* X = reinterpret_cast<float*>(sm + kOffB);               // 64 x 68 fp32
   float* TL = reinterpret_cast<float*>(sm + kOffTL);             // 64 x 68 fp32
   float* Zs = reinterpret_cast<float*>(sm + kOffZ);              // 32 x 32 fp32
@@ -340,8 +346,7 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
 
   if (threadIdx.x == 0) {
     for (int q = 0; q < kPrepGroups; ++q) {
-      mbar_init(smem_u32(&bars[q][0]), 1);
-      mbar_init(smem_u32(&bars[q][1]), 1);
+      for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bars[q][i]), 1);
       abort_sh[q] = 0;
     }
     fence_mbar_init();
@@ -428,7 +433,6 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
     }
     unpublished = ~(size_t)0;
   };
-  uint32_t mma_phase = 0;          // completions of bar_mma so far
   int it = 0;
   for (int lin = gid; lin < total && ok; lin += ngroups, ++it) {
   const size_t tile_id = (size_t)head_of(lin) * NT + tile_of(lin);
@@ -529,8 +533,7 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
     mma_commit(bar_mma);
   }
   ok = gsync_and(ok);  // also publishes the gate scalars
-  ok = ok && mbar_wait(bar_mma, mma_phase & 1);
-  ++mma_phase;
+  ok = ok && mbar_wait(bar_mma, it & 1);  // G1 completes once per tile
   tc_fence_after();
   if (ok) {
     // Row t of KK^T (TMEM lanes 0..63) -> row t of X = L (step 4):
@@ -596,7 +599,7 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
   // group at the inverse's first barrier, after which io 0 releases the
   // previous tile.  The inverse runs (on whatever X holds) even after a failed
   // wait, so every thread passes the same barriers; ok is made uniform after it.
-  if ((warp & 3) < 2) named_bar_sync(xready_id, 128);
+  if (pstream) named_bar_sync(pstream_id, 128);
   prefetch_next();
   invert_unit_lower<C>(X, TL, Zs, tid, gsync, [&]() {
     if (ok) publish();
@@ -640,45 +643,53 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
   }
   ok = gsync_and(ok);
 
-  // G2: D2a = A2 K (cols 0..127; rows 0..63 = P = T_L K) and
-  //     D2b = A2 V (cols 128..255; rows 64..127 = U = T_A (beta V)).
+  // From G2 on the tile runs as two streams that meet again before the last
+  // stores: the P stream (warps 0, 1, 4, 5: TMEM lanes 0..63; P, Pt, G M P, Qh;
+  // io 0 and 1) and the U stream (warps 2, 3, 6, 7: lanes 64..127; U, Ut,
+  // y_loc; io 2 and 3), each with its own barrier and MMA completion barrier.
+  // G2 (thread 0): D2b = A2 V (cols 128..255; rows 64..127 = U = T_A (beta V))
+  // first, committed to bar_u, then D2a = A2 K (cols 0..127; rows 0..63 =
+  // P = T_L K), committed to bar_p.
   if (ok && tid == 0) {
     tc_fence_after();
     const uint32_t id2 = idesc_bf16(128, 128, false, true);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       const uint64_t ad = smem_desc(sbase + kOffB + kk * 32, 16, 1024, kSw128);
-      mma_bf16_ss(tmem, ad, smem_desc(sbase + kOffKQ + kk * 2048, 16384, 1024, kSw128), id2,
-                  kk > 0);
-    }
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const uint64_t ad = smem_desc(sbase + kOffB + kk * 32, 16, 1024, kSw128);
       mma_bf16_ss(tmem + 128, ad, smem_desc(sbase + kOffV + kk * 2048, 8192, 1024, kSw128), id2,
                   kk > 0);
     }
-    mma_commit(bar_mma);
+    mma_commit(bar_u);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint64_t ad = smem_desc(sbase + kOffB + kk * 32, 16, 1024, kSw128);
+      mma_bf16_ss(tmem, ad, smem_desc(sbase + kOffKQ + kk * 2048, 16384, 1024, kSw128), id2,
+                  kk > 0);
+    }
+    mma_commit(bar_p);
   }
-  ok = ok && mbar_wait(bar_mma, mma_phase & 1);
-  ++mma_phase;
+  const uint32_t bar_s = pstream ? bar_p : bar_u;
+  const int stream_id = pstream ? pstream_id : ustream_id;
+  ok = ok && mbar_wait(bar_s, 0);
   tc_fence_after();
 
+  // Epilogue thread: row t of its stream (TMEM lane (warp % 4) * 32 + lane),
+  // columns cbeg .. cbeg+63 (warps w and w+4 share a lane quadrant).
+  auto epi_t = [&]() { return ((warp & 3) * 32 + (tid & 31)) & 63; };
+  auto epi_src = [&]() {
+    return tmem + ((uint32_t)((warp & 3) * 32) << 16) + (pstream ? 0 : 128);
+  };
   if (ok) {
+    const int t = epi_t(), cbeg = (warp >> 2) * 64;
+    const uint32_t src = epi_src();
     // P rows (lanes 0..63) and U rows (lanes 64..127): bf16 into the G3 operand
-    // and, scaled, into the workspace: Pt = G_C beta P (step 9), Ut = Gam[C-1][.] U.
-    // Warps w and w+4 share a lane quadrant and take 64 columns each.
-    const int q4 = warp & 3, lrow = q4 * 32 + (tid & 31);
-    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-    const bool top = lrow < 64;
-    const int t = lrow & 63;
-    const uint32_t src = tmem + lane_base + (top ? 0 : 128);
-    const uint32_t bdst = kOffB + (top ? 0 : 16384);
-    const float scale = top ? gc[t / C] * bta[t] : gsuf[t];
-    // Staging for the workspace rows (K and V are dead after G2): 128B-swizzled
-    // 64-column halves, stored below with TMA.
-    const uint32_t stage = top ? kOffKQ : kOffV;
-    const uint32_t half_stride = top ? 16384 : 8192;
-    const int cbeg = (warp >> 2) * 64;
+    // B3 = [P; U] and, scaled, into the workspace: Pt = G_C beta P (step 9),
+    // Ut = Gam[C-1][.] U.  Staging: Pt over K, Ut over V (each stream's G2 has
+    // read them), as 128B-swizzled 64-column halves stored below with TMA.
+    const uint32_t bdst = kOffB + (pstream ? 0 : 16384);
+    const float scale = pstream ? gc[t / C] * bta[t] : gsuf[t];
+    const uint32_t stage = pstream ? kOffKQ : kOffV;
+    const uint32_t half_stride = pstream ? 16384 : 8192;
 #pragma unroll
     for (int c2 = cbeg; c2 < cbeg + 64; c2 += 32) {
       float vv[2][16];  // two 16-column blocks per TMEM round trip
@@ -699,9 +710,10 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
         st_sm16(sm, hs + sw128(t, (col & 63) + 8), pack8(v + 8));
       }
     }
+    fence_proxy_async();
   }
-  if (ok) fence_proxy_async();
-  ok = gsync_and(ok);
+  tc_fence_before();  // this stream's TMEM reads precede its G3
+  named_bar_sync(stream_id, 128);
   if (ok && io >= 0) {
     const int row0 = (int)(tile_id * 128);
     if (io < 2) {
@@ -715,40 +727,30 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
     }
     bulk_commit();
   }
-  if (ok && tid == 0) {
-    // G3: D3a = A3 P (cols 0..127; rows 0..63 = G M P),
-    //     D3b = A3 U (cols 128..255; rows 64..127 = y_loc).
+  // G3 per stream: D3a = A3 P (thread 0; cols 0..127, rows 0..63 = G M P) and
+  // D3b = A3 U (thread 64; cols 128..255, rows 64..127 = y_loc).
+  if (ok && (tid == 0 || tid == 64)) {
     tc_fence_after();
     const uint32_t id3 = idesc_bf16(128, 128, false, true);
+    const uint32_t boff = pstream ? 0 : 16384;
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       const uint64_t ad = smem_desc(sbase + kOffA3 + kk * 32, 16, 1024, kSw128);
-      mma_bf16_ss(tmem, ad, smem_desc(sbase + kOffB + kk * 2048, 8192, 1024, kSw128), id3,
-                  kk > 0);
+      mma_bf16_ss(tmem + (pstream ? 0 : 128), ad,
+                  smem_desc(sbase + kOffB + boff + kk * 2048, 8192, 1024, kSw128), id3, kk > 0);
     }
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const uint64_t ad = smem_desc(sbase + kOffA3 + kk * 32, 16, 1024, kSw128);
-      mma_bf16_ss(tmem + 128, ad,
-                  smem_desc(sbase + kOffB + 16384 + kk * 2048, 8192, 1024, kSw128), id3,
-                  kk > 0);
-    }
-    mma_commit(bar_mma);
+    mma_commit(bar_s);
   }
-  ok = ok && mbar_wait(bar_mma, mma_phase & 1);
-  ++mma_phase;
+  ok = ok && mbar_wait(bar_s, 1);
   tc_fence_after();
 
   if (ok) {
-    const int q4 = warp & 3, lrow = q4 * 32 + (tid & 31);
-    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-    const bool top = lrow < 64;
-    const int t = lrow & 63;
-    const uint32_t src = tmem + lane_base + (top ? 0 : 128);
-    // Staging (A3 and B3 are dead after G3).
-    const uint32_t stage = top ? kOffA3 : kOffB;
+    // Staging over this stream's half of B3 (read only by its own G3): Qh by
+    // the P stream, y_loc / sqrt(Dk) by the U stream.
+    const int t = epi_t(), cbeg = (warp >> 2) * 64;
+    const uint32_t src = epi_src();
+    const uint32_t stage = kOffB + (pstream ? 0 : 16384);
     const float gt = gpw[t];
-    const int cbeg = (warp >> 2) * 64;
 #pragma unroll
     for (int c2 = cbeg; c2 < cbeg + 64; c2 += 32) {
       float vv[2][16];  // two 16-column blocks per TMEM round trip
@@ -759,7 +761,7 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
       for (int hh = 0; hh < 2; ++hh) {
         const int col = c2 + 16 * hh;
         float* v = vv[hh];
-        if (top) {  // Qh = G q - G M P  (step 7, state-free part)
+        if (pstream) {  // Qh = G q - G M P  (step 7, state-free part)
           const uint8_t* qa = sm + kOffKQ + (col >> 6) * 16384 + 8192;
           float q[16];
           unpack8(*reinterpret_cast<const uint4*>(qa + sw128(t, col & 63)), q);
@@ -784,11 +786,12 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
     if (io < 2) {
 #pragma unroll
       for (int c = 0; c < 64 / C; ++c)  // Qh rows of chunk c, half io
-        tma_store_2d(P.tm_a1s, sbase + kOffA3 + io * 8192 + c * C * 128, 64 * io,
+        tma_store_2d(P.tm_a1s, sbase + kOffB + io * 8192 + c * C * 128, 64 * io,
                      row0 + 2 * C * c + C);
     } else {  // y_loc / sqrt(Dk) into y (rows past T are clipped)
       const int h = io - 2, bh = head_of(lin), b = bh / Hv;
-      tma_store_4d(P.tm_y, sbase + kOffB + h * 8192, 64 * h, bh - b * Hv, tile_of(lin) * kTile, b);
+      tma_store_4d(P.tm_y, sbase + kOffB + 16384 + h * 8192, 64 * h, bh - b * Hv,
+                   tile_of(lin) * kTile, b);
     }
     bulk_commit();
     if (io == 0) unpublished = tile_id;
