@@ -139,6 +139,7 @@ __device__ __forceinline__ void l2norm_row_sw128(uint8_t* base, int half_stride,
 constexpr int kPrepGroups = 2;
 constexpr int kPrepGroupThreads = 256;
 constexpr int kPrepThreads = kPrepGroups * kPrepGroupThreads;
+constexpr int kPrepIo = 4;  // I/O threads per group (lane 0 of warps 4-7)
 // Shared-memory map of one group (bytes from its 1024-aligned base).
 constexpr uint32_t kOffKQ = 0;        // [K;Q]: 2 halves x (64 K rows + 64 Q rows) x 128 B
 constexpr uint32_t kOffV = 32768;     // V: 2 halves x 64 rows x 128 B
@@ -213,11 +214,9 @@ __device__ __forceinline__ void warp_store_16x8(float* D, int ldd, const float* 
 //   32 x 32 blocks (C >= 32)  T_10 = -T_11 X_10 T_00      (per 16-block pair)
 //   64 x 64 (C = 64)          T_BA = -T_BB X_BA T_AA      (32-block halves)
 // The block products run on warp-level tf32 MMAs; the group's 256 threads call
-// this (u = thread index in the group, sync = the group's barrier); `first`
-// runs right after the first barrier.
-template <int C, typename Sync, typename First>
-__device__ void invert_unit_lower(const float* X, float* Tm, float* Zs, int u, Sync sync,
-                                  First first) {
+// this (u = thread index in the group, sync = the group's barrier).
+template <int C, typename Sync>
+__device__ void invert_unit_lower(const float* X, float* Tm, float* Zs, int u, Sync sync) {
   for (int idx = u; idx < 64 * 64; idx += kPrepGroupThreads) {
     const int r = idx >> 6, c = idx & 63;
     if ((c >> 4) > (r >> 4) || (c / C) != (r / C)) Tm[r * kLdX + c] = 0.f;
@@ -241,7 +240,6 @@ __device__ void invert_unit_lower(const float* X, float* Tm, float* Zs, int u, S
     for (int r = 0; r < 16; ++r) Tm[(base + r) * kLdX + base + jj] = x[r];
   }
   sync();
-  first();
   const int w = u >> 5, lane = u & 31;
   if constexpr (C >= 32) {
     // Pairs (0,1) and (2,3): warp w < 4 handles pair w/2, columns 8*(w%2)..
@@ -295,8 +293,9 @@ struct PrepParams {
 };
 
 // The prep work of one CTA (both groups): CTA `cta_rank` of `n_ctas` doing prep.
-// With `flags`, each finished tile (b*Hv + hv, n) is published by setting
-// flags[(b*Hv + hv) * NT + n] to 1 once its workspace rows are in memory.
+// With `flags`, each finished tile (b*Hv + hv, n) is published by raising
+// flags[(b*Hv + hv) * NT + n] to kPrepIo: each I/O thread adds 1 once its own
+// stores of the tile are in memory.
 template <int C>
 __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw, int cta_rank,
                                           int n_ctas, int* flags) {
@@ -417,21 +416,18 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
 
   bool ok = true;
   bool tma_pending = gid < total;  // a load phase was issued and not yet waited for
-  size_t unpublished = ~(size_t)0;  // io 0: tile whose flag is not yet set
-  // The I/O threads make their stores of the finished tile complete; after a
-  // group barrier io 0 releases the tile's flag.
-  auto stores_complete = [&]() {
-    if (flags && io >= 0) {
+  // Publishing: each I/O thread adds 1 to a tile's flag once all of its stores
+  // of the tile are in memory, so the flag reaches kPrepIo when the whole tile
+  // is.  It does so after the next tile's loads have landed (they were issued
+  // after these stores), when the wait for the stores is normally over.
+  size_t unpublished = ~(size_t)0;
+  auto publish = [&]() {
+    if (unpublished != ~(size_t)0) {
       bulk_wait_all();
       fence_proxy_async_global();
+      red_release_gpu_add(flags + unpublished, 1);
+      unpublished = ~(size_t)0;
     }
-  };
-  auto publish = [&]() {
-    if (flags && io == 0 && unpublished != ~(size_t)0) {
-      __threadfence();
-      st_release_gpu(flags + unpublished, 1);
-    }
-    unpublished = ~(size_t)0;
   };
   int it = 0;
   for (int lin = gid; lin < total && ok; lin += ngroups, ++it) {
@@ -512,6 +508,7 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
 
   ok = mbar_wait(bar_tma, it & 1);
   tma_pending = false;
+  if (ok && io >= 0) publish();
   if (opts & kOptL2NormQK) {  // rows 0-63 of each half are K, 64-127 Q
     if (ok) l2norm_row_sw128(sm + kOffKQ, 16384, tid >> 1, tid & 1);
     fence_proxy_async();
@@ -590,20 +587,16 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
       }
     }
   }
-  stores_complete();  // the previous tile's stores (long done by now)
-
   // Step 4: T_L = (I + L)^-1.  Step 5 needs no second inverse:
   // (I + A)^-1 diag(beta) = diag(beta) (Gam . T_L) for A[t][j] = beta_t Gam[t][j] KK^T[t][j].
   // The inverse's first stage (warps 0-1) needs only X, written by warps 0, 1, 4
   // and 5; the A3 builders (warps 2, 3, 6, 7) finish meanwhile and meet the
-  // group at the inverse's first barrier, after which io 0 releases the
-  // previous tile.  The inverse runs (on whatever X holds) even after a failed
-  // wait, so every thread passes the same barriers; ok is made uniform after it.
+  // group at the inverse's first barrier.  The inverse runs (on whatever X
+  // holds) even after a failed wait, so every thread passes the same barriers;
+  // ok is made uniform after it.
   if (pstream) named_bar_sync(pstream_id, 128);
   prefetch_next();
-  invert_unit_lower<C>(X, TL, Zs, tid, gsync, [&]() {
-    if (ok) publish();
-  });
+  invert_unit_lower<C>(X, TL, Zs, tid, gsync);
 
   // A2 = [T_L; diag(beta) (Gam . T_L)]: 128 rows x 64 K-cols, K-major 128B swizzle.
   // Thread: 8 columns (col0..col0+7) of T_L rows r0 and r0+32, written as rows
@@ -794,7 +787,6 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
                    tile_of(lin) * kTile, b);
     }
     bulk_commit();
-    if (io == 0) unpublished = tile_id;
   }
   if (io >= 0) {
     // The next tile's K, Q and V are loaded once this thread's stores of Pt
@@ -806,16 +798,17 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
       load_q(next);
       tma_pending = true;
     }
+    if (ok && flags) unpublished = tile_id;
   }
   // No group barrier here: ok is uniform since the last one, and the next
   // tile's gate tables are free (their last reader was the epilogue above), so
   // the gate warps start on the next tile while the I/O threads issue its loads.
   }  // tile loop
 
-  if (io >= 0) bulk_wait_read_all();  // shared memory must outlive the last stores' reads
-  stores_complete();
-  gsync();
-  if (ok) publish();
+  if (io >= 0) {
+    if (ok) publish();
+    bulk_wait_read_all();  // shared memory must outlive the last stores' reads
+  }
   // A group that stopped early lets its last prefetch land before the CTA exits.
   if (io == 0 && tma_pending) mbar_wait(bar_tma, it & 1);
   tc_fence_before();
@@ -974,7 +967,7 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
       if (n >= SM::kStages && !mbar_wait(bar(empty0 + s), ((n / SM::kStages) - 1) & 1)) break;
       const size_t tid_ws = (size_t)bh * NT + n;
       if (flags) {
-        if (!wait_flag(flags + tid_ws)) break;
+        if (!wait_flag(flags + tid_ws, kPrepIo)) break;
         fence_proxy_async_global();
       }
       const uint32_t fb = bar(full0 + s);

@@ -177,14 +177,18 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
 __device__ __forceinline__ void st_release_gpu(int* p, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-// Bounded wait for a flag another CTA sets with st_release_gpu; on timeout it
-// records kErrWaitTimeout and returns false.
-__device__ __forceinline__ bool wait_flag(const int* p) {
-  if (ld_acquire_gpu(p) != 0) return true;
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Bounded wait until a counter other CTAs raise (st_release_gpu or
+// red_release_gpu_add) reaches `target`; on timeout it records kErrWaitTimeout
+// and returns false.
+__device__ __forceinline__ bool wait_flag(const int* p, int target = 1) {
+  if (ld_acquire_gpu(p) >= target) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
     __nanosleep(128);
-    if (ld_acquire_gpu(p) != 0) return true;
+    if (ld_acquire_gpu(p) >= target) return true;
     if (globaltimer() - t0 > kWaitLimitNs) {
       atomicExch(&g_device_error, kErrWaitTimeout);
       return false;
