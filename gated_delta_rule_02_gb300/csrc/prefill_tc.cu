@@ -878,7 +878,8 @@ enum : int {
   kQMt,                // [2] 128
   kQYFree = kQMt + 2,  // 128
   kQYStaged,           // 128: Y of the chunk staged for the reduction
-  kQFin,
+  kQDN,                // D = K^T Ut of the chunk issued and complete
+  kQFin,               // 2: both issuers' last products complete
   kNumQBars
 };
 
@@ -919,7 +920,8 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
     mbar_init(bar(kQMt + 1), 128);
     mbar_init(bar(kQYFree), 128);
     mbar_init(bar(kQYStaged), 128);
-    mbar_init(bar(kQFin), 1);
+    mbar_init(bar(kQDN), 1);
+    mbar_init(bar(kQFin), 2);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -998,8 +1000,15 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
     }
     for (int m = (n > SM::kStages ? n - SM::kStages : 0); m < n; ++m)
       mbar_wait(bar(full0 + m % SM::kStages), (m / SM::kStages) & 1);
-  } else if (warp == 1) {
-    // ---------------------------- MMA issuer -----------------------------
+  } else if (warp == 1 || warp == 15) {
+    // ---------------------------- MMA issuers ----------------------------
+    // Two threads issue the products, so that the serial one is not queued
+    // behind the others: warp 1 issues D += (-M^T) S^T only; warp 15 issues
+    // Y^T = S Qh^T (which needs only the chunk-start state), M^T of the next
+    // chunk and D = K^T Ut of the next chunk.  They are ordered through
+    // mbarriers: D_S(j) waits for D_N(j) (same accumulator); D_N(j+1) waits
+    // until the state group has read D(j); M^T(j+1) overwrites the TMEM operand
+    // of D_S(j-1), complete once the S operand of chunk j is written.
     if (lane == 0) {
       const uint32_t id_kt = idesc_bf16(128, 128, true, true);   // K^T x (Pt | Ut)
       const uint32_t id_s = idesc_bf16(128, 128, false, true);   // (-M^T) x S^T
@@ -1009,55 +1018,72 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
       const SmemDesc d_s = smem_desc_base(sS, 16384, 1024, kSw128);         // S operand
       const SmemDesc d_q = smem_desc_base(sbase + SM::kOffQ, 16, 1024, kSw128);  // Qh, K-major
       bool ok = true;
-      // M^T of chunk j into tM(j & 1), once its tile's MN buffers have landed.
-      auto issue_mt = [&](int j) {
-        if (j % kCt == 0) {
-          if (!(knorm ? wait_knorm(j) : wait_mn(j))) return false;
+      if (warp == 1) {
+        for (int j = 0; j < NC && ok; ++j) {
+          // D += (-M^T) S^T   (the serial step), on D = K^T Ut of the chunk
+          if (!(ok = mbar_wait(bar(kQDN), j & 1))) break;
+          if (!(ok = mbar_wait(bar(kQSop), j & 1))) break;
+          if (!(ok = mbar_wait(bar(kQMt + (j & 1)), (j >> 1) & 1))) break;
           tc_fence_after();
+          const uint32_t ta = tM(j & 1);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ts(tD, ta + 8 * kk, smem_desc_at(d_s, kk * 2048), id_s, 1);
+          mma_commit(bar(kQDs));
         }
-        const uint32_t off = ring_of(j) * SM::kMN + (j % kCt) * C * 128;
+      } else {
+        // M^T of chunk j into tM(j & 1), once its tile's MN buffers have landed.
+        auto issue_mt = [&](int j) {
+          if (j % kCt == 0) {
+            if (!(knorm ? wait_knorm(j) : wait_mn(j))) return false;
+            tc_fence_after();
+          }
+          const uint32_t off = ring_of(j) * SM::kMN + (j % kCt) * C * 128;
 #pragma unroll
-        for (int kk = 0; kk < C / 16; ++kk)
-          mma_bf16_ss(tM(j & 1), smem_desc_at(d_mn_mn, off + SM::kOffK + kk * 2048),
-                      smem_desc_at(d_mn_mn, off + SM::kOffP + kk * 2048), id_kt, kk > 0);
-        mma_commit(bar(kQM + (j & 1)));
-        return true;
-      };
-      if (NC > 0) ok = issue_mt(0);
-      for (int j = 0; j < NC && ok; ++j) {
-        const int c = j % kCt;
-        const uint32_t off = ring_of(j) * SM::kMN + c * C * 128;
-        // D = K^T Ut once chunk j-1's D has been read.
-        if (j > 0 && !(ok = mbar_wait(bar(kQDsFree), (j - 1) & 1))) break;
-        tc_fence_after();
+          for (int kk = 0; kk < C / 16; ++kk)
+            mma_bf16_ss(tM(j & 1), smem_desc_at(d_mn_mn, off + SM::kOffK + kk * 2048),
+                        smem_desc_at(d_mn_mn, off + SM::kOffP + kk * 2048), id_kt, kk > 0);
+          mma_commit(bar(kQM + (j & 1)));
+          return true;
+        };
+        // D = K^T Ut of chunk j into tD (after M^T(j): its MN buffers have landed).
+        auto issue_dn = [&](int j) {
+          tc_fence_after();
+          const uint32_t off = ring_of(j) * SM::kMN + (j % kCt) * C * 128;
 #pragma unroll
-        for (int kk = 0; kk < C / 16; ++kk)
-          mma_bf16_ss(tD, smem_desc_at(d_mn_mn, off + SM::kOffK + kk * 2048),
-                      smem_desc_at(d_mn_mn, off + SM::kOffU + kk * 2048), id_kt, kk > 0);
-        // The tile's MN buffers are free once its last products finish.
-        if (last_of_tile(j)) mma_commit(bar(kQEmptyMN + ring_of(j)));
-        // D += (-M^T) S^T   (the serial step)
-        if (!(ok = mbar_wait(bar(kQSop), j & 1))) break;
-        if (!(ok = mbar_wait(bar(kQMt + (j & 1)), (j >> 1) & 1))) break;
-        tc_fence_after();
-        const uint32_t ta = tM(j & 1);
+          for (int kk = 0; kk < C / 16; ++kk)
+            mma_bf16_ss(tD, smem_desc_at(d_mn_mn, off + SM::kOffK + kk * 2048),
+                        smem_desc_at(d_mn_mn, off + SM::kOffU + kk * 2048), id_kt, kk > 0);
+          mma_commit(bar(kQDN));
+          // The tile's MN buffers are free once its last products finish.
+          if (last_of_tile(j)) mma_commit(bar(kQEmptyMN + ring_of(j)));
+        };
+        if (NC > 0) {
+          ok = issue_mt(0);
+          if (ok) issue_dn(0);
+        }
+        for (int j = 0; j < NC && ok; ++j) {
+          const int c = j % kCt;
+          // Y^T = S Qh^T (A = the S operand read MN-major, B = Qh rows): the state
+          // group rewrites S once it completes.
+          if (!(ok = mbar_wait(bar(kQSop), j & 1))) break;
+          if (c == 0 && !(ok = wait_q(j))) break;
+          if (j > 0 && !(ok = mbar_wait(bar(kQYFree), (j - 1) & 1))) break;
+          tc_fence_after();
+          const uint32_t qoff = ring_of(j) * SM::kQ + c * C * 128;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts(tD, ta + 8 * kk, smem_desc_at(d_s, kk * 2048), id_s, 1);
-        mma_commit(bar(kQDs));
-        // Y^T = S Qh^T (A = the S operand read MN-major, B = Qh rows): the state
-        // group rewrites S once it completes.
-        if (c == 0 && !(ok = wait_q(j))) break;
-        if (j > 0 && !(ok = mbar_wait(bar(kQYFree), (j - 1) & 1))) break;
-        tc_fence_after();
-        const uint32_t qoff = ring_of(j) * SM::kQ + c * C * 128;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ss(tY, smem_desc_at(d_s, kk * 2048),
-                      smem_desc_at(d_q, qoff + (kk >> 2) * 8192 + (kk & 3) * 32), id_y, kk > 0);
-        mma_commit(bar(kQY));
-        // M^T of chunk j+1, converted by the aux group while chunk j finishes.
-        if (j + 1 < NC && !(ok = issue_mt(j + 1))) break;
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tY, smem_desc_at(d_s, kk * 2048),
+                        smem_desc_at(d_q, qoff + (kk >> 2) * 8192 + (kk & 3) * 32), id_y, kk > 0);
+          mma_commit(bar(kQY));
+          if (j + 1 < NC) {
+            // M^T of chunk j+1, converted by the aux group while chunk j finishes.
+            if (!(ok = issue_mt(j + 1))) break;
+            // D = K^T Ut of chunk j+1 once chunk j's D has been read.
+            if (!(ok = mbar_wait(bar(kQDsFree), j & 1))) break;
+            issue_dn(j + 1);
+          }
+        }
       }
       mma_commit(bar(kQFin));
       mbar_wait(bar(kQFin), 0);
@@ -1193,7 +1219,7 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
     }
     if (warp == 10 && lane == 0) bulk_wait_all();
   }
-  // warp 15 and the idle lanes of warps 0 and 14 have no scan work
+  // the idle lanes of warps 0 and 14 have no scan work
   tc_fence_before();
   if (warp != 0 && warp != 14) named_bar_sync(1, kFusedThreads - 64);
   if (warp == 1) tmem_dealloc(tmem, 512);
