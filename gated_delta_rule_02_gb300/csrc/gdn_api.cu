@@ -11,7 +11,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int check_common(int B, int T, int Hk, int Hv, int Dk, int Dv, int dtype) {
   if (B <= 0 || T <= 0 || Hk <= 0 || Hv <= 0 || Dk <= 0 || Dv <= 0) return GDN_ERR_INVALID;
   if (Hv % Hk != 0) return GDN_ERR_INVALID;
-  if (Dk != gdn::kHeadDim || Dv != gdn::kHeadDim) return GDN_ERR_UNSUPPORTED;
+  if (!gdn::head_dim_ok(Dk) || !gdn::head_dim_ok(Dv)) return GDN_ERR_UNSUPPORTED;
   if (dtype != GDN_DTYPE_F32 && dtype != GDN_DTYPE_BF16 && dtype != GDN_DTYPE_F16)
     return GDN_ERR_UNSUPPORTED;
   return GDN_OK;
@@ -30,6 +30,10 @@ int check_pointers(const void* const* ptrs, int n) {
     if (!aligned16(ptrs[i])) return GDN_ERR_ALIGNMENT;
   return GDN_OK;
 }
+// The tensor-core prefill serves bf16 inputs with the head size it is built for.
+bool use_tc(int Dk, int Dv, int dtype) {
+  return dtype == GDN_DTYPE_BF16 && Dk == gdn::kHeadDim && Dv == gdn::kHeadDim;
+}
 }  // namespace
 
 extern "C" {
@@ -39,8 +43,8 @@ size_t gdn_prefill_workspace_bytes(int B, int T, int Hk, int Hv, int Dk, int Dv,
   if (check_common(B, T, Hk, Hv, Dk, Dv, dtype) != GDN_OK) return 0;
   if (chunk != 16 && chunk != 32 && chunk != 64) return 0;
   if (T <= gdn::kShortT) return 0;  // the short-T sequential kernel needs none
-  if (dtype == GDN_DTYPE_BF16) return gdn::prefill_tc_workspace_bytes(B, T, Hv);
-  return gdn::prefill_simt_workspace_bytes(B, T, Hv, chunk);
+  if (use_tc(Dk, Dv, dtype)) return gdn::prefill_tc_workspace_bytes(B, T, Hv);
+  return gdn::prefill_simt_workspace_bytes(B, T, Hv, chunk, Dk, Dv);
 }
 
 int gdn_prefill_ex(const void* q, const void* k, const void* v, const void* g,
@@ -61,11 +65,11 @@ int gdn_prefill_ex(const void* q, const void* k, const void* v, const void* g,
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDN_ERR_ALIGNMENT;
   }
   gdn::PrefillArgs a{q, k, v, g, beta, state_in, state_out, y, B, T, Hk, Hv, chunk,
-                     dtype, options, workspace, workspace_bytes,
+                     dtype, options, Dk, Dv, workspace, workspace_bytes,
                      static_cast<cudaStream_t>(stream)};
-  cudaError_t e = T <= gdn::kShortT       ? gdn::launch_prefill_short(a)
-                  : dtype == GDN_DTYPE_BF16 ? gdn::launch_prefill_tc(a)
-                                            : gdn::launch_prefill_simt(a);
+  cudaError_t e = T <= gdn::kShortT        ? gdn::launch_prefill_short(a)
+                  : use_tc(Dk, Dv, dtype) ? gdn::launch_prefill_tc(a)
+                                          : gdn::launch_prefill_simt(a);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -88,7 +92,7 @@ int gdn_decode_step_ex(const void* q, const void* k, const void* v, const void* 
   st = check_pointers(req, 8);
   if (st != GDN_OK) return st;
   gdn::DecodeArgs a{q, k, v, g, beta, state_in, state_out, y, B, Hk, Hv, dtype, options,
-                    static_cast<cudaStream_t>(stream)};
+                    Dk, Dv, static_cast<cudaStream_t>(stream)};
   cudaError_t e = gdn::launch_decode(a);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
@@ -111,7 +115,7 @@ const char* gdn_status_string(int status) {
   switch (status) {
     case GDN_OK: return "ok";
     case GDN_ERR_INVALID: return "invalid argument (null pointer, size <= 0 or Hv % Hk != 0)";
-    case GDN_ERR_UNSUPPORTED: return "unsupported shape, chunk, dtype or option (Dk = Dv = 128, chunk 16/32/64, f32/bf16/f16)";
+    case GDN_ERR_UNSUPPORTED: return "unsupported shape, chunk, dtype or option (Dk, Dv in {64, 128, 256}, chunk 16/32/64, f32/bf16/f16)";
     case GDN_ERR_ALIGNMENT: return "pointer not 16-byte aligned (workspace: 256-byte)";
     case GDN_ERR_WORKSPACE: return "workspace missing or smaller than gdn_prefill_workspace_bytes()";
     case GDN_ERR_CUDA: return "CUDA launch error";

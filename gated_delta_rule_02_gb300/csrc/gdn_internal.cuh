@@ -10,7 +10,10 @@
 
 namespace gdn {
 
-constexpr int kHeadDim = 128;  // Dk = Dv = 128 is the compiled head size
+// Head sizes: the tensor-core prefill is built for Dk = Dv = kHeadDim; the
+// decode, short-T and fp32 SIMT kernels take Dk and Dv from {64, 128, 256}.
+constexpr int kHeadDim = 128;
+__host__ __device__ constexpr bool head_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
 
 // Input conventions selected by the options word of the *_ex entry points
 // (same bits as GDN_OPT_* in include/gdn.h).
@@ -24,18 +27,19 @@ __host__ __device__ __forceinline__ int key_head(int hv, int Hk, int Hv, int opt
 // 1/|x| from a row's sum of squares (a zero row stays zero).
 __device__ __forceinline__ float inv_norm(float sumsq) { return rsqrtf(fmaxf(sumsq, 1e-30f)); }
 
-// Normalise `rows` fp32 rows of D = 128 (row stride `ld` floats) in shared
-// memory, one warp per row; all `nthreads` threads of the block call this.
-__device__ __forceinline__ void l2norm_rows_f32(float* s, int rows, int ld, int tid, int nthreads) {
+// Normalise `rows` fp32 rows of n <= 256 values (row stride `ld` floats) in
+// shared memory, one warp per row; all `nthreads` threads of the block call this.
+__device__ __forceinline__ void l2norm_rows_f32(float* s, int rows, int n, int ld, int tid,
+                                                int nthreads) {
   const int lane = tid & 31;
   for (int r = tid >> 5; r < rows; r += nthreads >> 5) {
-    float* row = s + r * ld + 4 * lane;
-    float a = row[0], b = row[1], c = row[2], d = row[3];
-    float ss = a * a + b * b + c * c + d * d;
+    float* row = s + r * ld;
+    float ss = 0.f;
+    for (int e = lane; e < n; e += 32) ss = fmaf(row[e], row[e], ss);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
     const float f = inv_norm(ss);
-    row[0] = a * f; row[1] = b * f; row[2] = c * f; row[3] = d * f;
+    for (int e = lane; e < n; e += 32) row[e] *= f;
   }
 }
 
@@ -55,6 +59,7 @@ struct PrefillArgs {
   void* y;
   int B, T, Hk, Hv, chunk, dtype;
   int options;  // kOpt* bits
+  int Dk, Dv;
   void* workspace;
   size_t workspace_bytes;
   cudaStream_t stream;
@@ -71,11 +76,12 @@ struct DecodeArgs {
   void* y;
   int B, Hk, Hv, dtype;
   int options;  // kOpt* bits
+  int Dk, Dv;
   cudaStream_t stream;
 };
 
-// fp32 SIMT chunked path (any dtype; the exact path for fp32 inputs).
-size_t prefill_simt_workspace_bytes(int B, int T, int Hv, int chunk);
+// fp32 SIMT chunked path (any dtype and head size; the exact path for fp32 inputs).
+size_t prefill_simt_workspace_bytes(int B, int T, int Hv, int chunk, int Dk, int Dv);
 cudaError_t launch_prefill_simt(const PrefillArgs& a);
 
 // tcgen05 chunked path (bf16 inputs): prep + scan launches.

@@ -12,11 +12,11 @@
 //     S[r] <- g_t S[r] + d k_t
 //     y_t[r] = (g_t z + d (k_t·q_t)) / sqrt(Dk)      (= S_t[r]·q_t / sqrt(Dk))
 //
-// Layout: one CTA of four warps per (b, hv) head, each warp owning 32 rows,
-// eight lanes per 512-byte row as in the decode kernel.  The CTA first stages
-// the T tokens' k, q, v (as fp32), g, beta and k·q in shared memory; each warp
-// then takes G row groups (4 rows each) at a time through all T tokens with
-// their state in registers.
+// Layout: one CTA of four warps per (b, hv) head, each warp owning Dv/4 rows,
+// eight lanes per row as in the decode kernel (Dk a template parameter, Dv a
+// runtime one).  The CTA first stages the T tokens' k, q, v (as fp32), g, beta
+// and k·q in shared memory; each warp then takes G row groups (4 rows each) at
+// a time through all T tokens with their state in registers.
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -31,19 +31,20 @@ __device__ __forceinline__ void st_state(float* p, float4 v) {
   __stcg(reinterpret_cast<float4*>(p), v);
 }
 
-template <typename T, int G>
+template <typename T, int DK, int G>
 __global__ void __launch_bounds__(kShortThreads)
 short_prefill_kernel(const T* __restrict__ q, const T* __restrict__ k,
                      const T* __restrict__ v, const T* __restrict__ g,
                      const T* __restrict__ beta, const float* state_in,
-                     float* state_out, T* __restrict__ y, int Tlen, int Hk, int Hv,
+                     float* state_out, T* __restrict__ y, int Tlen, int Hk, int Hv, int Dv,
                      int opts, float scale) {
-  constexpr int D = kHeadDim;
+  constexpr int D = DK;
+  constexpr int NJ = DK / 32;  // float4s of a row per lane
   extern __shared__ float4 smem_f4[];
-  float* ks = reinterpret_cast<float*>(smem_f4);  // [Tlen][D]
-  float* qs = ks + Tlen * D;                      // [Tlen][D]
-  float* vs = qs + Tlen * D;                      // [Tlen][D]
-  float* gs = vs + Tlen * D;                      // [Tlen]
+  float* ks = reinterpret_cast<float*>(smem_f4);  // [Tlen][DK]
+  float* qs = ks + Tlen * D;                      // [Tlen][DK]
+  float* vs = qs + Tlen * D;                      // [Tlen][Dv]
+  float* gs = vs + Tlen * Dv;                     // [Tlen]
   float* bs = gs + Tlen;                          // [Tlen]
   float* kqs = bs + Tlen;                         // [Tlen]
 
@@ -57,18 +58,31 @@ short_prefill_kernel(const T* __restrict__ q, const T* __restrict__ k,
   const int rg = lane >> 3;   // row within a group of four
   const int sub = lane & 7;   // lane within the row
 
-  // Stage the tokens: thread tid loads elements 4*(tid%32)..+3 of rows t with
-  // t = tid/32 (mod 4) stepping by 4.
+  // Stage the tokens: warp w takes rows t = w, w+4, ...; lane l loads the
+  // elements 4l..4l+3 (+128, ...) of k and q and of v.
   for (int t = warp; t < Tlen; t += kShortThreads / 32) {
-    const size_t kq_off = (((size_t)b * Tlen + t) * Hk + hk) * D + 4 * lane;
-    const size_t v_off = (((size_t)b * Tlen + t) * Hv + hv) * D + 4 * lane;
-    float kk[4], qq[4], vv[4];
-    load4(k + kq_off, kk);
-    load4(q + kq_off, qq);
-    load4(v + v_off, vv);
+    const size_t kq_off = (((size_t)b * Tlen + t) * Hk + hk) * D;
+    const size_t v_off = (((size_t)b * Tlen + t) * Hv + hv) * Dv;
+    constexpr int NK = (DK + 127) / 128;  // 4-element pieces of a k row per lane
+    float kk[NK][4], qq[NK][4];
+    float sk = 0.f, sq = 0.f;
+#pragma unroll
+    for (int p = 0; p < NK; ++p) {
+      const int e = 4 * lane + 128 * p;
+      if (e < DK) {
+        load4(k + kq_off + e, kk[p]);
+        load4(q + kq_off + e, qq[p]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) kk[p][i] = qq[p][i] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        sk = fmaf(kk[p][i], kk[p][i], sk);
+        sq = fmaf(qq[p][i], qq[p][i], sq);
+      }
+    }
     if (opts & kOptL2NormQK) {
-      float sk = kk[0] * kk[0] + kk[1] * kk[1] + kk[2] * kk[2] + kk[3] * kk[3];
-      float sq = qq[0] * qq[0] + qq[1] * qq[1] + qq[2] * qq[2] + qq[3] * qq[3];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
         sk += __shfl_xor_sync(0xffffffffu, sk, off);
@@ -76,15 +90,29 @@ short_prefill_kernel(const T* __restrict__ q, const T* __restrict__ k,
       }
       const float fk = inv_norm(sk), fq = inv_norm(sq);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        kk[i] *= fk;
-        qq[i] *= fq;
-      }
+      for (int p = 0; p < NK; ++p)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          kk[p][i] *= fk;
+          qq[p][i] *= fq;
+        }
     }
-    *reinterpret_cast<float4*>(ks + t * D + 4 * lane) = make_float4(kk[0], kk[1], kk[2], kk[3]);
-    *reinterpret_cast<float4*>(qs + t * D + 4 * lane) = make_float4(qq[0], qq[1], qq[2], qq[3]);
-    *reinterpret_cast<float4*>(vs + t * D + 4 * lane) = make_float4(vv[0], vv[1], vv[2], vv[3]);
-    float kq = kk[0] * qq[0] + kk[1] * qq[1] + kk[2] * qq[2] + kk[3] * qq[3];
+    float kq = 0.f;
+#pragma unroll
+    for (int p = 0; p < NK; ++p) {
+      const int e = 4 * lane + 128 * p;
+      if (e < DK) {
+        *reinterpret_cast<float4*>(ks + t * D + e) = make_float4(kk[p][0], kk[p][1], kk[p][2], kk[p][3]);
+        *reinterpret_cast<float4*>(qs + t * D + e) = make_float4(qq[p][0], qq[p][1], qq[p][2], qq[p][3]);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) kq = fmaf(kk[p][i], qq[p][i], kq);
+    }
+    for (int e = 4 * lane; e < Dv; e += 128) {
+      float vv[4];
+      load4(v + v_off + e, vv);
+      *reinterpret_cast<float4*>(vs + t * Dv + e) = make_float4(vv[0], vv[1], vv[2], vv[3]);
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
     if (lane == 0) {
@@ -96,25 +124,26 @@ short_prefill_kernel(const T* __restrict__ q, const T* __restrict__ k,
   }
   __syncthreads();
 
-  const float* Sin = state_in ? state_in + (size_t)bh * D * D : nullptr;
-  float* Sout = state_out + (size_t)bh * D * D;
+  const float* Sin = state_in ? state_in + (size_t)bh * Dv * D : nullptr;
+  float* Sout = state_out + (size_t)bh * Dv * D;
+  const int wrows = Dv / 4;  // rows per warp
 
 #pragma unroll 1
-  for (int it = 0; it < 32 / (4 * G); ++it) {
-    const int row0 = warp * 32 + it * 4 * G + rg;  // this lane's row in group gi: row0 + 4*gi
-    float4 s[G][4];
+  for (int it = 0; it < wrows / (4 * G); ++it) {
+    const int row0 = warp * wrows + it * 4 * G + rg;  // this lane's row in group gi: row0 + 4*gi
+    float4 s[G][NJ];
 #pragma unroll
     for (int gi = 0; gi < G; ++gi)
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
+      for (int j = 0; j < NJ; ++j)
         s[gi][j] = Sin ? ld_state(Sin + (size_t)(row0 + 4 * gi) * D + 4 * (sub + 8 * j))
                        : make_float4(0.f, 0.f, 0.f, 0.f);
 
 #pragma unroll 1
     for (int t = 0; t < Tlen; ++t) {
-      float kr[16], qr[16];
+      float kr[4 * NJ], qr[4 * NJ];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < NJ; ++j) {
         const float4 a = *reinterpret_cast<const float4*>(ks + t * D + 4 * (sub + 8 * j));
         const float4 c = *reinterpret_cast<const float4*>(qs + t * D + 4 * (sub + 8 * j));
         kr[4 * j] = a.x; kr[4 * j + 1] = a.y; kr[4 * j + 2] = a.z; kr[4 * j + 3] = a.w;
@@ -126,7 +155,7 @@ short_prefill_kernel(const T* __restrict__ q, const T* __restrict__ k,
       for (int gi = 0; gi < G; ++gi) {
         float xa = 0.f, za = 0.f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < NJ; ++j) {
           xa = fmaf(s[gi][j].x, kr[4 * j + 0], xa);
           xa = fmaf(s[gi][j].y, kr[4 * j + 1], xa);
           xa = fmaf(s[gi][j].z, kr[4 * j + 2], xa);
@@ -146,13 +175,13 @@ short_prefill_kernel(const T* __restrict__ q, const T* __restrict__ k,
           x[gi] += __shfl_xor_sync(0xffffffffu, x[gi], off);
           z[gi] += __shfl_xor_sync(0xffffffffu, z[gi], off);
         }
-      T* yt = y + (((size_t)b * Tlen + t) * Hv + hv) * D;
+      T* yt = y + (((size_t)b * Tlen + t) * Hv + hv) * Dv;
 #pragma unroll
       for (int gi = 0; gi < G; ++gi) {
         const int row = row0 + 4 * gi;
-        const float d = bt * (vs[t * D + row] - gt * x[gi]);
+        const float d = bt * (vs[t * Dv + row] - gt * x[gi]);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < NJ; ++j) {
           s[gi][j].x = fmaf(gt, s[gi][j].x, d * kr[4 * j + 0]);
           s[gi][j].y = fmaf(gt, s[gi][j].y, d * kr[4 * j + 1]);
           s[gi][j].z = fmaf(gt, s[gi][j].z, d * kr[4 * j + 2]);
@@ -164,33 +193,43 @@ short_prefill_kernel(const T* __restrict__ q, const T* __restrict__ k,
 #pragma unroll
     for (int gi = 0; gi < G; ++gi)
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
+      for (int j = 0; j < NJ; ++j)
         st_state(Sout + (size_t)(row0 + 4 * gi) * D + 4 * (sub + 8 * j), s[gi][j]);
   }
 }
 
-size_t short_smem_bytes(int T) { return (size_t)T * (3 * kHeadDim + 3) * sizeof(float); }
+size_t short_smem_bytes(int T, int Dk, int Dv) {
+  return (size_t)T * (2 * Dk + Dv + 3) * sizeof(float);
+}
 
-template <typename T>
+template <typename T, int DK>
 cudaError_t launch_short_t(const PrefillArgs& a) {
-  const float scale = 1.0f / sqrtf((float)kHeadDim);
-  const size_t smem = short_smem_bytes(a.T);
-  cudaError_t e = cudaFuncSetAttribute(short_prefill_kernel<T, 2>,
+  constexpr int G = DK == 256 ? 1 : 2;  // row groups in flight (registers)
+  const float scale = 1.0f / sqrtf((float)DK);
+  const size_t smem = short_smem_bytes(a.T, DK, a.Dv);
+  cudaError_t e = cudaFuncSetAttribute(short_prefill_kernel<T, DK, G>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  short_prefill_kernel<T, 2><<<a.B * a.Hv, kShortThreads, smem, a.stream>>>(
+  short_prefill_kernel<T, DK, G><<<a.B * a.Hv, kShortThreads, smem, a.stream>>>(
       static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v),
       static_cast<const T*>(a.g), static_cast<const T*>(a.beta), a.state_in, a.state_out,
-      static_cast<T*>(a.y), a.T, a.Hk, a.Hv, a.options, scale);
+      static_cast<T*>(a.y), a.T, a.Hk, a.Hv, a.Dv, a.options, scale);
   return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_short_dk(const PrefillArgs& a) {
+  if (a.Dk == 64) return launch_short_t<T, 64>(a);
+  if (a.Dk == 256) return launch_short_t<T, 256>(a);
+  return launch_short_t<T, 128>(a);
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_short(const PrefillArgs& a) {
-  if (a.dtype == 0) return launch_short_t<float>(a);
-  if (a.dtype == 2) return launch_short_t<__half>(a);
-  return launch_short_t<__nv_bfloat16>(a);
+  if (a.dtype == 0) return launch_short_dk<float>(a);
+  if (a.dtype == 2) return launch_short_dk<__half>(a);
+  return launch_short_dk<__nv_bfloat16>(a);
 }
 
 }  // namespace gdn

@@ -51,7 +51,7 @@ extern "C" {
 /* Status codes. */
 #define GDN_OK                  0
 #define GDN_ERR_INVALID       (-1) /* NULL required pointer, a size <= 0, Hv % Hk != 0 */
-#define GDN_ERR_UNSUPPORTED   (-2) /* Dk/Dv other than 128, chunk not 16/32/64, bad dtype */
+#define GDN_ERR_UNSUPPORTED   (-2) /* Dk/Dv not 64/128/256, chunk not 16/32/64, bad dtype */
 #define GDN_ERR_ALIGNMENT     (-3) /* a pointer that is not 16-byte aligned */
 #define GDN_ERR_WORKSPACE     (-4) /* workspace NULL or smaller than gdn_prefill_workspace_bytes */
 #define GDN_ERR_CUDA          (-5) /* the CUDA runtime reported an error at launch; the
@@ -115,7 +115,11 @@ GDN_API size_t gdn_prefill_workspace_bytes(int B, int T, int Hk, int Hv, int Dk,
  *              entry do not matter and on return are unspecified.  It must
  *              not be used by anything else until the work on `stream` is done.
  *   stream     cudaStream_t, or NULL.
- * Dk = Dv = 128.  Returns GDN_OK or a GDN_ERR_* code.
+ * Dk and Dv are each 64, 128 or 256.  bf16 inputs with Dk = Dv = 128 run on
+ * the tensor cores; every other head size and dtype runs the fp32 chunked
+ * path, which for Dk = Dv = 256 runs a chunk of 64 as two chunks of 32 (the
+ * result differs only by rounding; gdn_prefill_workspace_bytes accounts for
+ * it).  Returns GDN_OK or a GDN_ERR_* code.
  */
 GDN_API int gdn_prefill(const void *q, const void *k, const void *v, const void *g,
                 const void *beta, const float *state_in, float *state_out, void *y,
@@ -137,7 +141,8 @@ GDN_API int gdn_prefill_ex(const void *q, const void *k, const void *v, const vo
  *
  *   q, k [B, 1, Hk, Dk]; v, y [B, 1, Hv, Dv]; g, beta [B, 1, Hv]
  *   state_in must not be NULL; state_out may equal state_in (in place).
- * Dk = Dv = 128.  No workspace.  Returns GDN_OK or a GDN_ERR_* code.
+ * Dk and Dv are each 64, 128 or 256.  No workspace.  Returns GDN_OK or a
+ * GDN_ERR_* code.
  */
 GDN_API int gdn_decode_step(const void *q, const void *k, const void *v, const void *g,
                     const void *beta, const float *state_in, float *state_out,

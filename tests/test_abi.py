@@ -56,7 +56,14 @@ def test_workspace_bytes(L):
     assert w(1, 4096, 16, 32, 128, 128, 64, 1) > 0
     assert w(1, 4096, 16, 32, 128, 128, 64, 1) % 256 == 0
     assert w(1, 4096, 16, 32, 128, 128, 48, 1) == 0      # bad chunk
-    assert w(1, 4096, 16, 32, 64, 128, 64, 1) == 0       # unsupported head size
+    assert w(1, 4096, 16, 32, 96, 128, 64, 1) == 0       # unsupported head size
+    assert w(1, 4096, 16, 32, 128, 512, 64, 1) == 0
+    # head sizes 64 and 256 run the fp32 SIMT chunked path (any dtype) ...
+    assert w(1, 4096, 16, 32, 64, 64, 64, 1) > 0
+    assert w(1, 4096, 16, 32, 256, 64, 64, 1) > w(1, 4096, 16, 32, 64, 64, 64, 1)
+    # ... where Dk = Dv = 256 with chunk 64 runs as chunks of 32 (shared memory)
+    assert w(1, 4096, 16, 32, 256, 256, 64, 0) == w(1, 4096, 16, 32, 256, 256, 32, 0)
+    assert w(1, 4096, 16, 32, 128, 128, 64, 0) != w(1, 4096, 16, 32, 128, 128, 32, 0)
     assert w(1, 0, 16, 32, 128, 128, 64, 1) == 0         # empty
     assert w(1, 100, 3, 32, 128, 128, 64, 1) == 0        # Hv % Hk != 0
     # grows with the sequence
@@ -88,8 +95,9 @@ def prefill_args(**over):
     (dict(T=0), gdn.GDN_ERR_INVALID),
     (dict(T=-5), gdn.GDN_ERR_INVALID),
     (dict(Hk=3, Hv=4), gdn.GDN_ERR_INVALID),
-    (dict(Dk=64), gdn.GDN_ERR_UNSUPPORTED),
-    (dict(Dv=256), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(Dk=96), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(Dv=512), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(Dk=32), gdn.GDN_ERR_UNSUPPORTED),
     (dict(chunk=48), gdn.GDN_ERR_UNSUPPORTED),
     (dict(chunk=128), gdn.GDN_ERR_UNSUPPORTED),
     (dict(dtype=7), gdn.GDN_ERR_UNSUPPORTED),
