@@ -848,29 +848,32 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 constexpr int kFusedThreads = kPrepThreads;  // 16 warps
 
 // Two rings of tile buffers: the MN ring (Pt, K, Ut: read by K^T [Pt | Ut],
-// released as soon as those products finish) and the Q ring (Qh, later the
-// staging of y; released after the y reduction has read it).
+// released as soon as those products finish; two stages) and the Q ring (Qh,
+// later the staging of y; released after the y reduction has read it; three
+// stages, since it is held longer).
 struct Scan128Smem {
   static constexpr uint32_t kOffP = 0;              // Pt, 2 x 64 rows x 128 B
   static constexpr uint32_t kOffK = 16384;          // K,  2 x 64 rows x 128 B
   static constexpr uint32_t kOffU = 32768;          // Ut, 2 x 64 rows x 128 B
   static constexpr uint32_t kMN = 49152;
   static constexpr uint32_t kQ = 16384;             // Qh, 2 x 64 rows x 128 B
-  static constexpr int kStages = 3;                 // per ring
-  static constexpr uint32_t kOffQ = kStages * kMN;
-  static constexpr uint32_t kOffS = kOffQ + kStages * kQ;  // S operand: 2 x 128 k-rows x 128 B
-  static constexpr uint32_t kOffGC = kOffS + 32768;        // G_C per Q stage (fp32 x 4)
-  static constexpr uint32_t kTotal = kOffGC + kStages * 16 + 1024;
+  static constexpr int kStagesMN = 2;
+  static constexpr int kStagesQ = 3;
+  static constexpr uint32_t kOffQ = kStagesMN * kMN;
+  static constexpr uint32_t kOffS = kOffQ + kStagesQ * kQ;   // S operand: 2 x 128 k-rows x 128 B
+
+  static constexpr uint32_t kOffGC = kOffS + 32768;          // G_C per Q stage (fp32 x 4)
+  static constexpr uint32_t kTotal = kOffGC + kStagesQ * 16 + 1024;
 };
 constexpr uint32_t kFusedSmem = Scan128Smem::kTotal > kPrepSmem ? Scan128Smem::kTotal : kPrepSmem;
 
 enum : int {
   kQFullMN = 0,
-  kQEmptyMN = kQFullMN + Scan128Smem::kStages,  // MMA commit
-  kQFullQ = kQEmptyMN + Scan128Smem::kStages,
-  kQEmptyQ = kQFullQ + Scan128Smem::kStages,    // 257: state group + the y-reducing thread
-  kQKNorm = kQEmptyQ + Scan128Smem::kStages,    // 128: K rows of the MN stage normalised
-  kQDs = kQKNorm + Scan128Smem::kStages,
+  kQEmptyMN = kQFullMN + Scan128Smem::kStagesMN,  // MMA commit
+  kQFullQ = kQEmptyMN + Scan128Smem::kStagesMN,
+  kQEmptyQ = kQFullQ + Scan128Smem::kStagesQ,     // 257: state group + the y-reducing thread
+  kQKNorm = kQEmptyQ + Scan128Smem::kStagesQ,     // 128: K rows of the MN stage normalised
+  kQDs = kQKNorm + Scan128Smem::kStagesMN,
   kQY,
   kQM,                 // [2]
   kQSop = kQM + 2,     // 256
@@ -903,12 +906,14 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
   auto bar = [&](int i) { return smem_u32(&qbars[i]); };
 
   if (tid == 0) {
-    for (int s = 0; s < SM::kStages; ++s) {
+    for (int s = 0; s < SM::kStagesMN; ++s) {
       mbar_init(bar(kQFullMN + s), 1);
       mbar_init(bar(kQEmptyMN + s), 1);
+      mbar_init(bar(kQKNorm + s), 128);
+    }
+    for (int s = 0; s < SM::kStagesQ; ++s) {
       mbar_init(bar(kQFullQ + s), 1);
       mbar_init(bar(kQEmptyQ + s), 257);
-      mbar_init(bar(kQKNorm + s), 128);
     }
     mbar_init(bar(kQDs), 1);
     mbar_init(bar(kQY), 1);
@@ -935,23 +940,24 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
   const uint32_t tD = tmem, tY = tmem + 384;
   auto tM = [&](int x) { return tmem + 128 + 128 * x; };  // fp32 M^T; cols 0-63 then -M^T bf16
   const uint32_t sS = sbase + SM::kOffS;
-  auto ring_of = [&](int j) { return (j / kCt) % SM::kStages; };
-  auto mn_addr = [&](int j) { return sbase + ring_of(j) * SM::kMN; };
-  auto q_addr = [&](int j) { return sbase + SM::kOffQ + ring_of(j) * SM::kQ; };
+  auto ring_mn = [&](int j) { return (j / kCt) % SM::kStagesMN; };
+  auto ring_q = [&](int j) { return (j / kCt) % SM::kStagesQ; };
+  auto mn_addr = [&](int j) { return sbase + ring_mn(j) * SM::kMN; };
+  auto q_addr = [&](int j) { return sbase + SM::kOffQ + ring_q(j) * SM::kQ; };
   auto last_of_tile = [&](int j) { return (j % kCt) == kCt - 1 || j == NC - 1; };
   auto wait_mn = [&](int j) {
     const int n = j / kCt;
-    return mbar_wait(bar(kQFullMN + n % SM::kStages), (n / SM::kStages) & 1);
+    return mbar_wait(bar(kQFullMN + n % SM::kStagesMN), (n / SM::kStagesMN) & 1);
   };
   // With L2-normalised keys the aux group rewrites each K tile first.
   const bool knorm = (opts & kOptL2NormQK) != 0;
   auto wait_knorm = [&](int j) {
     const int n = j / kCt;
-    return mbar_wait(bar(kQKNorm + n % SM::kStages), (n / SM::kStages) & 1);
+    return mbar_wait(bar(kQKNorm + n % SM::kStagesMN), (n / SM::kStagesMN) & 1);
   };
   auto wait_q = [&](int j) {
     const int n = j / kCt;
-    return mbar_wait(bar(kQFullQ + n % SM::kStages), (n / SM::kStages) & 1);
+    return mbar_wait(bar(kQFullQ + n % SM::kStagesQ), (n / SM::kStagesQ) & 1);
   };
 
   if ((warp == 0 || warp == 14) && lane == 0) {
@@ -963,10 +969,11 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
       prefetch_tmap(tm_k);
       prefetch_tmap(tm_uy);
     }
+    const int stages = mn ? SM::kStagesMN : SM::kStagesQ;
     int n = 0;
     for (; n < NT; ++n) {
-      const int s = n % SM::kStages;
-      if (n >= SM::kStages && !mbar_wait(bar(empty0 + s), ((n / SM::kStages) - 1) & 1)) break;
+      const int s = n % stages;
+      if (n >= stages && !mbar_wait(bar(empty0 + s), ((n / stages) - 1) & 1)) break;
       const size_t tid_ws = (size_t)bh * NT + n;
       if (flags) {
         if (!wait_flag(flags + tid_ws, kPrepIo)) break;
@@ -998,8 +1005,8 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
         }
       }
     }
-    for (int m = (n > SM::kStages ? n - SM::kStages : 0); m < n; ++m)
-      mbar_wait(bar(full0 + m % SM::kStages), (m / SM::kStages) & 1);
+    for (int m = (n > stages ? n - stages : 0); m < n; ++m)
+      mbar_wait(bar(full0 + m % stages), (m / stages) & 1);
   } else if (warp == 1 || warp == 15) {
     // ---------------------------- MMA issuers ----------------------------
     // Two threads issue the products, so that the serial one is not queued
@@ -1038,7 +1045,7 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
             if (!(knorm ? wait_knorm(j) : wait_mn(j))) return false;
             tc_fence_after();
           }
-          const uint32_t off = ring_of(j) * SM::kMN + (j % kCt) * C * 128;
+          const uint32_t off = ring_mn(j) * SM::kMN + (j % kCt) * C * 128;
 #pragma unroll
           for (int kk = 0; kk < C / 16; ++kk)
             mma_bf16_ss(tM(j & 1), smem_desc_at(d_mn_mn, off + SM::kOffK + kk * 2048),
@@ -1049,14 +1056,14 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
         // D = K^T Ut of chunk j into tD (after M^T(j): its MN buffers have landed).
         auto issue_dn = [&](int j) {
           tc_fence_after();
-          const uint32_t off = ring_of(j) * SM::kMN + (j % kCt) * C * 128;
+          const uint32_t off = ring_mn(j) * SM::kMN + (j % kCt) * C * 128;
 #pragma unroll
           for (int kk = 0; kk < C / 16; ++kk)
             mma_bf16_ss(tD, smem_desc_at(d_mn_mn, off + SM::kOffK + kk * 2048),
                         smem_desc_at(d_mn_mn, off + SM::kOffU + kk * 2048), id_kt, kk > 0);
           mma_commit(bar(kQDN));
           // The tile's MN buffers are free once its last products finish.
-          if (last_of_tile(j)) mma_commit(bar(kQEmptyMN + ring_of(j)));
+          if (last_of_tile(j)) mma_commit(bar(kQEmptyMN + ring_mn(j)));
         };
         if (NC > 0) {
           ok = issue_mt(0);
@@ -1070,7 +1077,7 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
           if (c == 0 && !(ok = wait_q(j))) break;
           if (j > 0 && !(ok = mbar_wait(bar(kQYFree), (j - 1) & 1))) break;
           tc_fence_after();
-          const uint32_t qoff = ring_of(j) * SM::kQ + c * C * 128;
+          const uint32_t qoff = ring_q(j) * SM::kQ + c * C * 128;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_bf16_ss(tY, smem_desc_at(d_s, kk * 2048),
@@ -1111,8 +1118,8 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
     for (int j = 0; j < NC; ++j) {
       const int c = j % kCt;
       if (c == 0 && !(ok = wait_q(j))) break;
-      const float Gc = ld_shared_f32(sbase + SM::kOffGC + 16 * ring_of(j) + 4 * c);
-      if (last_of_tile(j)) mbar_arrive(bar(kQEmptyQ + ring_of(j)));
+      const float Gc = ld_shared_f32(sbase + SM::kOffGC + 16 * ring_q(j) + 4 * c);
+      if (last_of_tile(j)) mbar_arrive(bar(kQEmptyQ + ring_q(j)));
       if (!(ok = mbar_wait(bar(kQDs), j & 1))) break;
       tc_fence_after();
 #pragma unroll
@@ -1167,7 +1174,7 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
       if (!wait_mn(j)) return false;
       l2norm_row_sw128(sm + (mn_addr(j) - sbase) + SM::kOffK, 8192, atid >> 1, atid & 1);
       fence_proxy_async();
-      mbar_arrive(bar(kQKNorm + ring_of(j)));
+      mbar_arrive(bar(kQKNorm + ring_mn(j)));
       return true;
     };
     if (knorm && NC > 0) ok = normalise_k(0);
@@ -1214,7 +1221,7 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
           tma_reduce_add_4d(tm_yred, qst + hh * 8192 + c * C * 128, 64 * hh, hv, j * C, b);
         bulk_commit();
         bulk_wait_read_all();  // the Q buffers may be refilled once the reduction has read them
-        if (last_of_tile(j)) mbar_arrive(bar(kQEmptyQ + ring_of(j)));
+        if (last_of_tile(j)) mbar_arrive(bar(kQEmptyQ + ring_q(j)));
       }
     }
     if (warp == 10 && lane == 0) bulk_wait_all();

@@ -30,6 +30,9 @@ SMALL = [
     (1, 64, 1, 2, 64, BF16, 5.0),    # fast decay: G underflows inside a chunk
     (2, 100, 16, 32, 64, BF16, 0.3), # B*Hv = 64 heads: the split prep + scan launches
     (1, 150, 8, 48, 32, BF16, 0.3),  # 48 heads, GQA 6:1: the fused launch at its widest
+    (2, 257, 24, 24, 64, BF16, 0.3), # head pair (24, 24), B = 2, T = 4 chunks + 1 token
+    (1, 1111, 16, 48, 32, BF16, 0.5),  # head pair (16, 48), T = 1111
+    (1, 257, 24, 24, 16, F32, 0.1),
 ]
 
 
