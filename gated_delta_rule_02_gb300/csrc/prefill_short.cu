@@ -204,7 +204,7 @@ size_t short_smem_bytes(int T, int Dk, int Dv) {
 
 template <typename T, int DK>
 cudaError_t launch_short_t(const PrefillArgs& a) {
-  constexpr int G = DK == 256 ? 1 : 2;  // row groups in flight (registers)
+  constexpr int G = DK == 256 ? 1 : 4;  // row groups of a warp in flight (registers)
   const float scale = 1.0f / sqrtf((float)DK);
   const size_t smem = short_smem_bytes(a.T, DK, a.Dv);
   cudaError_t e = cudaFuncSetAttribute(short_prefill_kernel<T, DK, G>,
