@@ -24,11 +24,39 @@ namespace {
 
 constexpr int kShortThreads = 128;
 
-__device__ __forceinline__ float4 ld_state(const float* p) {
-  return __ldcg(reinterpret_cast<const float4*>(p));
+// Two fp32 values in one 64-bit register, for the paired fp32 instructions of
+// sm_100 and later (each lane of a pair rounds as the scalar instruction would).
+using f32x2 = unsigned long long;
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
 }
-__device__ __forceinline__ void st_state(float* p, float4 v) {
-  __stcg(reinterpret_cast<float4*>(p), v);
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
+  f32x2 d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ float sum2(f32x2 a) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a));
+  return lo + hi;
+}
+// A row slice of four floats as two pairs.
+struct Row4 {
+  f32x2 a, b;
+};
+__device__ __forceinline__ Row4 ld_state(const float* p) {
+  const ulonglong2 v = __ldcg(reinterpret_cast<const ulonglong2*>(p));
+  return Row4{v.x, v.y};
+}
+__device__ __forceinline__ void st_state(float* p, Row4 v) {
+  __stcg(reinterpret_cast<ulonglong2*>(p), make_ulonglong2(v.a, v.b));
 }
 
 template <typename T, int DK, int G>
@@ -131,42 +159,38 @@ short_prefill_kernel(const T* __restrict__ q, const T* __restrict__ k,
 #pragma unroll 1
   for (int it = 0; it < wrows / (4 * G); ++it) {
     const int row0 = warp * wrows + it * 4 * G + rg;  // this lane's row in group gi: row0 + 4*gi
-    float4 s[G][NJ];
+    Row4 s[G][NJ];
 #pragma unroll
     for (int gi = 0; gi < G; ++gi)
 #pragma unroll
       for (int j = 0; j < NJ; ++j)
         s[gi][j] = Sin ? ld_state(Sin + (size_t)(row0 + 4 * gi) * D + 4 * (sub + 8 * j))
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
+                       : Row4{0ull, 0ull};
 
 #pragma unroll 1
     for (int t = 0; t < Tlen; ++t) {
-      float kr[4 * NJ], qr[4 * NJ];
+      Row4 kr[NJ], qr[NJ];
 #pragma unroll
       for (int j = 0; j < NJ; ++j) {
-        const float4 a = *reinterpret_cast<const float4*>(ks + t * D + 4 * (sub + 8 * j));
-        const float4 c = *reinterpret_cast<const float4*>(qs + t * D + 4 * (sub + 8 * j));
-        kr[4 * j] = a.x; kr[4 * j + 1] = a.y; kr[4 * j + 2] = a.z; kr[4 * j + 3] = a.w;
-        qr[4 * j] = c.x; qr[4 * j + 1] = c.y; qr[4 * j + 2] = c.z; qr[4 * j + 3] = c.w;
+        const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(ks + t * D + 4 * (sub + 8 * j));
+        const ulonglong2 c = *reinterpret_cast<const ulonglong2*>(qs + t * D + 4 * (sub + 8 * j));
+        kr[j] = Row4{a.x, a.y};
+        qr[j] = Row4{c.x, c.y};
       }
       const float gt = gs[t], bt = bs[t], kq = kqs[t];
       float x[G], z[G];
 #pragma unroll
       for (int gi = 0; gi < G; ++gi) {
-        float xa = 0.f, za = 0.f;
+        f32x2 xa = 0ull, za = 0ull;
 #pragma unroll
         for (int j = 0; j < NJ; ++j) {
-          xa = fmaf(s[gi][j].x, kr[4 * j + 0], xa);
-          xa = fmaf(s[gi][j].y, kr[4 * j + 1], xa);
-          xa = fmaf(s[gi][j].z, kr[4 * j + 2], xa);
-          xa = fmaf(s[gi][j].w, kr[4 * j + 3], xa);
-          za = fmaf(s[gi][j].x, qr[4 * j + 0], za);
-          za = fmaf(s[gi][j].y, qr[4 * j + 1], za);
-          za = fmaf(s[gi][j].z, qr[4 * j + 2], za);
-          za = fmaf(s[gi][j].w, qr[4 * j + 3], za);
+          xa = fma2(s[gi][j].a, kr[j].a, xa);
+          xa = fma2(s[gi][j].b, kr[j].b, xa);
+          za = fma2(s[gi][j].a, qr[j].a, za);
+          za = fma2(s[gi][j].b, qr[j].b, za);
         }
-        x[gi] = xa;
-        z[gi] = za;
+        x[gi] = sum2(xa);
+        z[gi] = sum2(za);
       }
 #pragma unroll
       for (int off = 1; off < 8; off <<= 1)
@@ -176,16 +200,16 @@ short_prefill_kernel(const T* __restrict__ q, const T* __restrict__ k,
           z[gi] += __shfl_xor_sync(0xffffffffu, z[gi], off);
         }
       T* yt = y + (((size_t)b * Tlen + t) * Hv + hv) * Dv;
+      const f32x2 g2 = pack2(gt, gt);
 #pragma unroll
       for (int gi = 0; gi < G; ++gi) {
         const int row = row0 + 4 * gi;
         const float d = bt * (vs[t * Dv + row] - gt * x[gi]);
+        const f32x2 d2 = pack2(d, d);
 #pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-          s[gi][j].x = fmaf(gt, s[gi][j].x, d * kr[4 * j + 0]);
-          s[gi][j].y = fmaf(gt, s[gi][j].y, d * kr[4 * j + 1]);
-          s[gi][j].z = fmaf(gt, s[gi][j].z, d * kr[4 * j + 2]);
-          s[gi][j].w = fmaf(gt, s[gi][j].w, d * kr[4 * j + 3]);
+        for (int j = 0; j < NJ; ++j) {  // S <- g S + d k, element pairs
+          s[gi][j].a = fma2(g2, s[gi][j].a, mul2(d2, kr[j].a));
+          s[gi][j].b = fma2(g2, s[gi][j].b, mul2(d2, kr[j].b));
         }
         if (sub == 0) yt[row] = from_f32<T>(fmaf(gt, z[gi], d * kq) * scale);
       }
