@@ -81,6 +81,8 @@ def lib() -> ctypes.CDLL:
             L.gdn_prefill_ex.restype = i
             L.gdn_decode_step_ex.argtypes = [vp] * 8 + [i] * 6 + [vp, i]
             L.gdn_decode_step_ex.restype = i
+            L.gdn_selftest_wait_timeout.argtypes = [vp]
+            L.gdn_selftest_wait_timeout.restype = i
             _lib = L
     return _lib
 
@@ -93,6 +95,16 @@ def gdn_device_status(clear: bool = False) -> int:
     """GDN_OK, or GDN_ERR_DEVICE_TIMEOUT if a kernel's bounded wait gave up
     (synchronises the device)."""
     return int(lib().gdn_device_status(1 if clear else 0))
+
+
+def gdn_selftest_wait_timeout(stream=None, device=None) -> None:
+    """Enqueue ``gdn_selftest_wait_timeout`` (include/gdn.h): a kernel whose
+    bounded waits run out (about 4 s), so that the next ``gdn_device_status``
+    reports GDN_ERR_DEVICE_TIMEOUT."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    st = lib().gdn_selftest_wait_timeout(_stream_handle(stream, dev))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_selftest_wait_timeout")
 
 
 def gdn_prefill_workspace_bytes(B, T, Hk, Hv, Dk, Dv, chunk, dtype) -> int:

@@ -106,9 +106,17 @@ int gdn_decode_step(const void* q, const void* k, const void* v, const void* g,
 }
 
 int gdn_device_status(int clear) {
-  const int v = gdn::prefill_tc_device_error(clear != 0);
-  if (v < 0) return GDN_ERR_CUDA;
-  return v ? GDN_ERR_DEVICE_TIMEOUT : GDN_OK;
+  // Each translation unit with bounded waits has its own device error word.
+  if (cudaDeviceSynchronize() != cudaSuccess) return GDN_ERR_CUDA;
+  const int a = gdn::prefill_tc_device_error(clear != 0);
+  const int b = gdn::wait_hook_device_error(clear != 0);
+  if (a < 0 || b < 0) return GDN_ERR_CUDA;
+  return (a || b) ? GDN_ERR_DEVICE_TIMEOUT : GDN_OK;
+}
+
+int gdn_selftest_wait_timeout(void* stream) {
+  const cudaError_t e = gdn::launch_wait_timeout_hook(static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 const char* gdn_status_string(int status) {

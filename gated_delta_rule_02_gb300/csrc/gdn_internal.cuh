@@ -90,6 +90,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a);
 // Reads (and optionally clears) the tensor-core kernels' device error word;
 // -1 if it cannot be read.
 int prefill_tc_device_error(bool clear);
+cudaError_t launch_wait_timeout_hook(cudaStream_t stream);
+int wait_hook_device_error(bool clear);
 
 // Short sequences (T <= kShortT): the sequential rule with the state on chip,
 // no workspace.

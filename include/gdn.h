@@ -189,13 +189,26 @@ GDN_API int gdn_prefill_noalloc(const void *q, const void *k, const void *v, con
 
 /*
  * Device-side health: every wait inside the tensor-core kernels (on an
- * mbarrier fed by TMA or by the tensor core) is bounded; a wait that gives up
+ * mbarrier fed by TMA or by the tensor core, or on a tile flag that another
+ * CTA raises) is bounded; a wait that gives up
  * sets a device error word and the kernel returns early, leaving its outputs
  * unspecified.  This call synchronises the device, reads that word and
  * returns GDN_OK, GDN_ERR_DEVICE_TIMEOUT, or GDN_ERR_CUDA if it cannot be
  * read.  A non-zero `clear` resets the word.
  */
 GDN_API int gdn_device_status(int clear);
+
+/*
+ * Failure-detection hook (for tests of gdn_device_status): enqueues on
+ * `stream` one single-thread kernel that runs the library's two bounded waits
+ * on things that never complete -- an mbarrier phase no thread arrives on,
+ * then a device flag no code raises.  Each gives up after its limit (2 s), so
+ * the kernel ends after about 4 s having set the device error word, and the
+ * next gdn_device_status returns GDN_ERR_DEVICE_TIMEOUT.  It reads and writes
+ * no caller memory and leaves the CUDA context usable.  Returns GDN_OK, or
+ * GDN_ERR_CUDA if the launch failed.
+ */
+GDN_API int gdn_selftest_wait_timeout(void *stream);
 
 /* A static, NUL-terminated description of a status code. */
 GDN_API const char *gdn_status_string(int status);
