@@ -195,10 +195,13 @@ def roofline(alg_bytes, seconds, hbm_gbs, kind, traffic=None):
 
 
 def prefill_launches(w, dev):
-    """Kernels one gdn_prefill call launches: bf16 runs prep and scan as one
+    """Kernels one gdn_prefill call launches: T <= 32 one (the sequential
+    short-T kernel); bf16 with 128-wide heads runs prep and scan as one
     cooperative kernel when B*Hv is at most a third of the SMs, else as two;
-    fp32 always as two."""
-    if w.torch_dtype != torch.bfloat16:
+    the fp32 chunked path always two."""
+    if w.T <= 32:
+        return 1
+    if w.torch_dtype != torch.bfloat16 or w.Dk != 128 or w.Dv != 128:
         return 2
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     return 1 if 3 * w.B * w.Hv <= sms else 2

@@ -156,6 +156,15 @@ short_prefill_kernel(const T* __restrict__ q, const T* __restrict__ k,
   float* Sout = state_out + (size_t)bh * Dv * D;
   const int wrows = Dv / 4;  // rows per warp
 
+  // The registers hold S scaled: S = gam * St, gam the product of the gates since
+  // the last renormalisation (the same for every row of the head).  Then
+  //     x = gam (St·k),  z = gam (St·q),  gn = gam g_t,
+  //     d = beta_t (v_t[r] - gn (St·k)),   y_t[r] = gn (St·q) + d (k_t·q_t),
+  //     St <- St + (d / gn) k_t,  gam <- gn,
+  // one paired FMA per element pair instead of a multiply and an FMA.  When gn
+  // leaves [2^-24, 2^24] (a zero gate included) the registers are brought back
+  // to scale, St <- gn St + d k_t, gam <- 1: a branch that is uniform over the
+  // CTA, since every row sees the same gates.
 #pragma unroll 1
   for (int it = 0; it < wrows / (4 * G); ++it) {
     const int row0 = warp * wrows + it * 4 * G + rg;  // this lane's row in group gi: row0 + 4*gi
@@ -166,6 +175,7 @@ short_prefill_kernel(const T* __restrict__ q, const T* __restrict__ k,
       for (int j = 0; j < NJ; ++j)
         s[gi][j] = Sin ? ld_state(Sin + (size_t)(row0 + 4 * gi) * D + 4 * (sub + 8 * j))
                        : Row4{0ull, 0ull};
+    float gam = 1.f;
 
 #pragma unroll 1
     for (int t = 0; t < Tlen; ++t) {
@@ -192,33 +202,86 @@ short_prefill_kernel(const T* __restrict__ q, const T* __restrict__ k,
         x[gi] = sum2(xa);
         z[gi] = sum2(za);
       }
+      const float gn = gam * gt;
+      T* yt = y + (((size_t)b * Tlen + t) * Hv + hv) * Dv;
+      if constexpr (G == 4) {
+        // Sum the eight partial dot products of a lane (x and z of four rows)
+        // over the row's eight lanes in a transposing butterfly: after it lane
+        // `sub` holds the full x[sub] (sub < 4) or z[sub - 4].
+        const bool b2 = (sub & 4) != 0, b1 = (sub & 2) != 0, b0 = (sub & 1) != 0;
+        float h4[4];
 #pragma unroll
-      for (int off = 1; off < 8; off <<= 1)
+        for (int i = 0; i < 4; ++i) {
+          const float keep = b2 ? z[i] : x[i], send = b2 ? x[i] : z[i];
+          h4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
+        float h2[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const float keep = b1 ? h4[2 + i] : h4[i], send = b1 ? h4[i] : h4[2 + i];
+          h2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+        }
+        const float own = (b0 ? h2[1] : h2[0]) + __shfl_xor_sync(0xffffffffu, b0 ? h2[0] : h2[1], 1);
+        const int base = lane & ~7;
+#pragma unroll
+        for (int gi = 0; gi < 4; ++gi) x[gi] = __shfl_sync(0xffffffffu, own, base | gi);
+        // Lane 4 + gi owns z of row gi and stores that row's y.
+        const float xo = __shfl_sync(0xffffffffu, own, base | (sub & 3));
+        const int ro = row0 + 4 * (sub & 3);
+        const float dd = bt * (vs[t * Dv + ro] - gn * xo);
+        if (b2) yt[ro] = from_f32<T>(fmaf(gn, own, dd * kq) * scale);
+      } else {
+#pragma unroll
+        for (int off = 1; off < 8; off <<= 1)
+#pragma unroll
+          for (int gi = 0; gi < G; ++gi) {
+            x[gi] += __shfl_xor_sync(0xffffffffu, x[gi], off);
+            z[gi] += __shfl_xor_sync(0xffffffffu, z[gi], off);
+          }
 #pragma unroll
         for (int gi = 0; gi < G; ++gi) {
-          x[gi] += __shfl_xor_sync(0xffffffffu, x[gi], off);
-          z[gi] += __shfl_xor_sync(0xffffffffu, z[gi], off);
+          const int row = row0 + 4 * gi;
+          const float dd = bt * (vs[t * Dv + row] - gn * x[gi]);
+          if (sub == 0) yt[row] = from_f32<T>(fmaf(gn, z[gi], dd * kq) * scale);
         }
-      T* yt = y + (((size_t)b * Tlen + t) * Hv + hv) * Dv;
-      const f32x2 g2 = pack2(gt, gt);
+      }
+      float d[G];
 #pragma unroll
-      for (int gi = 0; gi < G; ++gi) {
-        const int row = row0 + 4 * gi;
-        const float d = bt * (vs[t * Dv + row] - gt * x[gi]);
-        const f32x2 d2 = pack2(d, d);
+      for (int gi = 0; gi < G; ++gi) d[gi] = bt * (vs[t * Dv + row0 + 4 * gi] - gn * x[gi]);
+      if (gn >= 0x1p-24f && gn <= 0x1p24f) {
+        const float inv = 1.f / gn;
 #pragma unroll
-        for (int j = 0; j < NJ; ++j) {  // S <- g S + d k, element pairs
-          s[gi][j].a = fma2(g2, s[gi][j].a, mul2(d2, kr[j].a));
-          s[gi][j].b = fma2(g2, s[gi][j].b, mul2(d2, kr[j].b));
+        for (int gi = 0; gi < G; ++gi) {
+          const float c = d[gi] * inv;
+          const f32x2 c2 = pack2(c, c);
+#pragma unroll
+          for (int j = 0; j < NJ; ++j) {  // St <- St + (d / gn) k
+            s[gi][j].a = fma2(c2, kr[j].a, s[gi][j].a);
+            s[gi][j].b = fma2(c2, kr[j].b, s[gi][j].b);
+          }
         }
-        if (sub == 0) yt[row] = from_f32<T>(fmaf(gt, z[gi], d * kq) * scale);
+        gam = gn;
+      } else {
+        const f32x2 g2 = pack2(gn, gn);
+#pragma unroll
+        for (int gi = 0; gi < G; ++gi) {
+          const f32x2 d2 = pack2(d[gi], d[gi]);
+#pragma unroll
+          for (int j = 0; j < NJ; ++j) {  // St <- gn St + d k
+            s[gi][j].a = fma2(g2, s[gi][j].a, mul2(d2, kr[j].a));
+            s[gi][j].b = fma2(g2, s[gi][j].b, mul2(d2, kr[j].b));
+          }
+        }
+        gam = 1.f;
       }
     }
+    const f32x2 gam2 = pack2(gam, gam);
 #pragma unroll
     for (int gi = 0; gi < G; ++gi)
 #pragma unroll
       for (int j = 0; j < NJ; ++j)
-        st_state(Sout + (size_t)(row0 + 4 * gi) * D + 4 * (sub + 8 * j), s[gi][j]);
+        st_state(Sout + (size_t)(row0 + 4 * gi) * D + 4 * (sub + 8 * j),
+                 Row4{mul2(gam2, s[gi][j].a), mul2(gam2, s[gi][j].b)});
   }
 }
 
