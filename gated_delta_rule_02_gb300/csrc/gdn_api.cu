@@ -17,7 +17,7 @@ int check_common(int B, int T, int Hk, int Hv, int Dk, int Dv, int dtype) {
   return GDN_OK;
 }
 
-// Option bits this build understands (GDN_OPT_* in include/gdn.h).
+// Option bits the library understands (GDN_OPT_* in include/gdn.h).
 constexpr int kKnownOptions = GDN_OPT_TILED_HEADS | GDN_OPT_LOG_GATE | GDN_OPT_L2NORM_QK;
 static_assert(GDN_OPT_TILED_HEADS == gdn::kOptTiledHeads && GDN_OPT_LOG_GATE == gdn::kOptLogGate &&
                   GDN_OPT_L2NORM_QK == gdn::kOptL2NormQK,
