@@ -9,7 +9,8 @@ The oracle is pinned to things other than itself:
   * closed forms and special cases: beta = 0 (pure decay), g = beta = 1 with
     orthonormal keys (the rule stores v_i under k_i and reduces to causal
     linear attention), beta = 1 with unit keys (S_t k_t = v_t for any gate),
-    a hand-worked two-token example (tests/golden);
+    a hand-worked two-token example (tests/golden), one token in closed form
+    written as a projection;
   * invariants: GQA grouped map = MHA on repeated heads, linearity in
     (S_0, V), a vanishing gate resets the state, split/resume.
 A mutation test plants plausible mistakes in a NumPy copy of the recurrence
@@ -202,10 +203,33 @@ def pin_split_resume(impl):
     return max(rel_err(y, np.concatenate([ya, yb], axis=1)), rel_err(s, sb)), 1e-14
 
 
+def pin_one_token_projection(impl):
+    """T = 1 in closed form, arranged as a projection: the update is
+    S_1 = g S_0 (I - beta k k^T) + beta v k^T (the state decays, its component
+    along k is partly removed, and beta v is written along k), y = S_1 q / sqrt(Dk).
+    Keys are not normalised, heads are grouped (Hv/Hk = 2)."""
+    rng = np.random.default_rng(22)
+    q, k, v, g, beta, s0 = rand_case(rng, B=2, T=1, Hk=2, Hv=4, Dk=6, Dv=5, unit_keys=False)
+    y, s = impl(q, k, v, g, beta, s0)
+    B, _, Hk, Dk = q.shape
+    Hv = v.shape[2]
+    ys = np.zeros_like(y)
+    ss = np.zeros_like(s)
+    for b in range(B):
+        for hv in range(Hv):
+            hk = hv // (Hv // Hk)
+            kk, qq, vv = k[b, 0, hk], q[b, 0, hk], v[b, 0, hv]
+            gg, bb = g[b, 0, hv], beta[b, 0, hv]
+            proj = np.eye(Dk) - bb * np.outer(kk, kk)
+            ss[b, hv] = gg * s0[b, hv] @ proj + bb * np.outer(vv, kk)
+            ys[b, 0, hv] = ss[b, hv] @ qq / np.sqrt(Dk)
+    return max(rel_err(y, ys), rel_err(s, ss)), 1e-13
+
+
 PINS = [pin_chunked_wy, pin_single_solve, pin_product_form, pin_beta_zero,
         pin_orthonormal_store, pin_causal_linear_attention, pin_unit_key_overwrite,
         pin_hand_worked, pin_gqa_grouped, pin_linearity, pin_vanishing_gate_resets,
-        pin_split_resume]
+        pin_split_resume, pin_one_token_projection]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
