@@ -176,3 +176,39 @@ def test_short_t_scaled_state_equals_the_rule(gates):
     y, s = short_t_model(q[0, :, 0], k[0, :, 0], v[0, :, 0], g[0, :, 0], beta[0, :, 0], s0[0, 0])
     assert rel_err(y, yo[0, :, 0]) < 1e-12
     assert rel_err(s, so[0, 0]) < 1e-12
+
+
+def test_two_chunks_compose_into_one_affine_step():
+    """A chunk maps the state affinely, S <- S F + N with F = G_C I - Pt^T K and
+    N = Ut^T K, so two chunks compose into one step S <- S (F1 F2) + (N1 F2 + N2),
+    and both chunks' outputs come from the first chunk's start state:
+    [Y_1 | Y_2] = S [Qh_1^T | F1 Qh_2^T] + [0 | N1 Qh_2^T].  Everything but the
+    products with S is independent of the state."""
+    rng = np.random.default_rng(3)
+    C, Dk, Dv, T = 32, 16, 12, 128
+    q, k, v, g, beta, s0 = rand_problem(rng, T, 1, 1, Dk, Dv)
+    yo, so = oracle.gdn_sequential(q, k, v, g, beta, s0)
+    q, k, v, g, beta, s0 = q[0, :, 0], k[0, :, 0], v[0, :, 0], g[0, :, 0], beta[0, :, 0], s0[0, 0]
+
+    def chunk(sl):
+        Q, K, V, gc, bc = q[sl], k[sl], v[sl], g[sl], beta[sl]
+        _, G, gam = gate_tables(gc)
+        KK, QK = K @ K.T, Q @ K.T
+        TL = np.linalg.inv(np.eye(C) + np.tril(KK * bc[None, :], -1))
+        P, U = TL @ K, (bc[:, None] * (gam * TL)) @ V
+        M = np.tril(QK * bc[None, :])
+        Qh = G[:, None] * Q - G[:, None] * (M @ P)
+        F = G[-1] * np.eye(Dk) - (G[-1] * bc[:, None] * P).T @ K
+        N = (gam[-1][:, None] * U).T @ K
+        return F, N, Qh, (gam * QK) @ U
+
+    S, ys = s0.copy(), []
+    for p in range(T // (2 * C)):
+        F1, N1, Q1, y1 = chunk(slice(2 * p * C, (2 * p + 1) * C))
+        F2, N2, Q2, y2 = chunk(slice((2 * p + 1) * C, (2 * p + 2) * C))
+        Y = S @ np.hstack([Q1.T, F1 @ Q2.T])
+        Y[:, C:] += N1 @ Q2.T
+        ys.append((Y.T + np.vstack([y1, y2])) / np.sqrt(Dk))
+        S = S @ (F1 @ F2) + (N1 @ F2 + N2)
+    assert rel_err(np.vstack(ys), yo[0, :, 0]) < 1e-12
+    assert rel_err(S, so[0, 0]) < 1e-12
