@@ -23,7 +23,9 @@
  * (metaltile-std `gated_delta_wy.rs`, "Layouts"; the state stays fp32.)
  *
  * Ownership: the caller owns every buffer, including any workspace; the
- * library allocates no device memory.  All work is enqueued on `stream`
+ * library makes no device allocation at run time (the fixed scratch of
+ * gdn_prefill_noalloc is a static array of the library image, 32 MiB, in
+ * device memory from the moment the library is loaded).  All work is enqueued on `stream`
  * (a cudaStream_t; NULL means the legacy default stream) and the calls
  * return without synchronising.  state_in == state_out (in place) is
  * allowed; any other overlap between inputs and outputs is undefined.
