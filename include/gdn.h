@@ -25,7 +25,8 @@
  * Ownership: the caller owns every buffer, including any workspace; the
  * library makes no device allocation at run time (the fixed scratch of
  * gdn_prefill_noalloc is a static array of the library image, 32 MiB, in
- * device memory from the moment the library is loaded).  All work is enqueued on `stream`
+ * device memory once the library's kernels are loaded into a CUDA context).  All work
+ * is enqueued on `stream`
  * (a cudaStream_t; NULL means the legacy default stream) and the calls
  * return without synchronising.  state_in == state_out (in place) is
  * allowed; any other overlap between inputs and outputs is undefined.
