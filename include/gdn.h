@@ -25,11 +25,11 @@
  * Ownership: the caller owns every buffer, including any workspace; the
  * library makes no device allocation at run time (the fixed scratch of
  * gdn_prefill_noalloc is a static array of the library image, 32 MiB, in
- * device memory once the library's kernels are loaded into a CUDA context).  All work
- * is enqueued on `stream`
- * (a cudaStream_t; NULL means the legacy default stream) and the calls
- * return without synchronising.  state_in == state_out (in place) is
- * allowed; any other overlap between inputs and outputs is undefined.
+ * device memory once the library's kernels are loaded into a CUDA context).
+ * All work is enqueued on `stream` (a cudaStream_t; NULL means the legacy
+ * default stream) and the calls return without synchronising.
+ * state_in == state_out (in place) is allowed; any other overlap between
+ * inputs and outputs is undefined.
  *
  * Errors: every argument is checked on the host before anything is
  * launched; on a non-zero return nothing has been enqueued and the outputs
