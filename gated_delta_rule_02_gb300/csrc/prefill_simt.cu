@@ -76,8 +76,10 @@ intra_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
   float* sg = sG + C;
   float* sb = sg + C;
 
-  const int n = blockIdx.x;
-  const int bh = blockIdx.y;
+  // One-dimensional grid (chunk fastest): blockIdx.x = n + N bh, so B Hv is not
+  // held to the 65535 blocks of a grid's y dimension.
+  const int n = blockIdx.x % N;
+  const int bh = blockIdx.x / N;
   const int b = bh / Hv;
   const int hv = bh - b * Hv;
   const int hk = key_head(hv, Hk, Hv, opts);
@@ -214,8 +216,10 @@ scan_simt_kernel(const T* __restrict__ k, const float* __restrict__ ws,
   float* sYl = sUt + C * R;        // [C][R]
   float* sW = sYl + C * R;         // [R][C]
 
-  const int tile = blockIdx.x;
-  const int bh = blockIdx.y;
+  // One-dimensional grid (row tile fastest): blockIdx.x = tile + (Dv / R) bh.
+  const int tiles = Dv / R;
+  const int tile = blockIdx.x % tiles;
+  const int bh = blockIdx.x / tiles;
   const int b = bh / Hv;
   const int hv = bh - b * Hv;
   const int hk = key_head(hv, Hk, Hv, opts);
@@ -280,6 +284,8 @@ template <typename T, int C>
 cudaError_t launch_t(const PrefillArgs& a) {
   const int N = (a.T + C - 1) / C;
   const int BH = a.B * a.Hv;
+  // One block per (chunk, head) and per (row tile, head) on a 1-D grid.
+  if ((long long)N * BH > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   float* ws = static_cast<float*>(a.workspace);
   float* wsG = ws + (size_t)BH * N * chunk_block_floats(C, a.Dk, a.Dv);
   const size_t smem_i = intra_smem_bytes(C, a.Dk, a.Dv);
@@ -291,14 +297,14 @@ cudaError_t launch_t(const PrefillArgs& a) {
   e = cudaFuncSetAttribute(scan_simt_kernel<T, C>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_s);
   if (e != cudaSuccess) return e;
-  intra_simt_kernel<T, C><<<dim3(N, BH), kThreads, smem_i, a.stream>>>(
+  intra_simt_kernel<T, C><<<(unsigned)(N * BH), kThreads, smem_i, a.stream>>>(
       static_cast<const T*>(a.q), static_cast<const T*>(a.k),
       static_cast<const T*>(a.v), static_cast<const T*>(a.g),
       static_cast<const T*>(a.beta), ws, wsG, a.T, a.Hk, a.Hv, N, a.Dk, a.Dv, a.options);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const float scale = 1.0f / sqrtf((float)a.Dk);
-  scan_simt_kernel<T, C><<<dim3(a.Dv / kRows, BH), kThreads, smem_s, a.stream>>>(
+  scan_simt_kernel<T, C><<<(unsigned)(a.Dv / kRows * BH), kThreads, smem_s, a.stream>>>(
       static_cast<const T*>(a.k), ws, wsG, a.state_in, a.state_out,
       static_cast<T*>(a.y), a.T, a.Hk, a.Hv, N, a.Dk, a.Dv, a.options, scale);
   return cudaGetLastError();
