@@ -41,19 +41,22 @@ import gdn_inputs  # noqa: E402
 FLUSH_BYTES = 256 << 20
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per call from one
-# ncu capture, summarised under profiles/.  Valid only for the kernel sources
-# it was taken on (sha256 prefix of those files); otherwise reported as null.
+# ncu capture, summarised under profiles/, per workload.  Valid only for the
+# kernel sources it was taken on (sha256 prefix of those files); otherwise
+# reported as null.
 _KDIR = os.path.join(ROOT, "gated_delta_rule_02_gb300", "csrc")
 MEASURED_TRAFFIC = {
-    "prefill": {"sources": ["prefill_tc.cu", "sm100_ptx.cuh"], "sha": "84515aefd06eb1aa",
-                "bytes": 152.0e6},
-    "decode": {"sources": ["decode.cu"], "sha": "48a64c9af36e1446", "bytes": 210.7e6},
+    "prefill_t4096": {"sources": ["prefill_tc.cu", "sm100_ptx.cuh"], "sha": "84515aefd06eb1aa",
+                      "bytes": 152.0e6},
+    "decode_b64": {"sources": ["decode.cu"], "sha": "48a64c9af36e1446", "bytes": 210.7e6},
 }
 
 
 def measured_traffic(key):
     import hashlib
-    entry = MEASURED_TRAFFIC[key]
+    entry = MEASURED_TRAFFIC.get(key)
+    if entry is None:
+        return None
     m = hashlib.sha256()
     try:
         for name in entry["sources"]:
@@ -62,6 +65,8 @@ def measured_traffic(key):
     except OSError:
         return None
     return entry["bytes"] if m.hexdigest()[:16] == entry["sha"] else None
+
+
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -207,7 +212,8 @@ def prefill_launches(w, dev):
     return 1 if 3 * w.B * w.Hv <= sms else 2
 
 
-def median_ms(pairs):
+def event_ms(pairs):
+    """Elapsed milliseconds of each (start, end) CUDA event pair."""
     return [a.elapsed_time(b) for a, b in pairs]
 
 
@@ -215,6 +221,8 @@ def median_ms(pairs):
 # our arm
 # ----------------------------------------------------------------------------
 def bench_prefill(gdn, w, dev, steps, warmup, world):
+    """Median CUDA-event time (ms) of one gdn_prefill call over ``steps``
+    timed calls, each preceded (outside the events) by a 256 MiB L2 flush."""
     ins = {n: t.to(dev) for n, t in gdn_inputs.workload_inputs(w).items()}
     y = torch.empty((w.B, w.T, w.Hv, w.Dv), dtype=w.torch_dtype, device=dev)
     s_out = torch.empty((w.B, w.Hv, w.Dv, w.Dk), dtype=torch.float32, device=dev)
@@ -245,8 +253,8 @@ def bench_prefill(gdn, w, dev, steps, warmup, world):
     torch.cuda.synchronize(dev)
     barrier(world)
     wall = time.perf_counter() - t0
-    times = median_ms(pairs)
-    return sum(times) / len(times), wall
+    times = event_ms(pairs)
+    return statistics.median(times), wall
 
 
 def bench_prefill_e2e(gdn, w, dev, steps, warmup):
@@ -285,9 +293,12 @@ def bench_prefill_e2e(gdn, w, dev, steps, warmup):
             "ms_per_step": round(sec * 1e3, 4)}
 
 
-def bench_decode(gdn, w, dev, replays=3):
+def bench_decode(gdn, w, dev, replays=5):
     """256 successive decode steps captured in one CUDA graph (state in place);
-    the state (134 MB) is larger than the L2."""
+    the state (134 MB) is larger than the L2.  Before each timed replay the
+    state is reset from a saved copy and the L2 is then flushed (256 MiB
+    write), so no part of the state starts warm; the median replay is taken.
+    Returns (us per step, cold), (us per step without the flush, warm)."""
     steps = w.steps
     s = gdn_inputs.workload_inputs(w, step=0)["s0"].to(dev)
     step_in = []
@@ -314,19 +325,24 @@ def bench_decode(gdn, w, dev, replays=3):
     torch.cuda.synchronize(dev)
     graph.replay()
     torch.cuda.synchronize(dev)
-    times = []
-    for _ in range(replays):
-        s_work.copy_(s)
-        torch.cuda.synchronize(dev)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        graph.replay()
-        b.record()
-        torch.cuda.synchronize(dev)
-        times.append(a.elapsed_time(b))
-    ms_graph = min(times)
-    us_step = ms_graph * 1e3 / steps
-    return us_step
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def timed(cold):
+        times = []
+        for _ in range(replays):
+            s_work.copy_(s)
+            if cold:
+                flush.zero_()
+            torch.cuda.synchronize(dev)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            graph.replay()
+            b.record()
+            torch.cuda.synchronize(dev)
+            times.append(a.elapsed_time(b))
+        return statistics.median(times) * 1e3 / steps
+
+    return timed(True), timed(False)
 
 
 def oracle_sample(w, n_kh):
@@ -374,6 +390,50 @@ def cpu_baseline_prefill(w, min_seconds=10.0, max_reps=50):
                       f"{reps} runs, {total:.1f} s"}
 
 
+def cpu_chunked_fp32(w, n_heads=2, chunk=32):
+    """The fp32 host chunked form (the oracle package's Woodbury-Young form in
+    float32, chunk 32: the host comparison of ferrox-core ``gdn_chunk.rs``),
+    timed on ``n_heads`` value heads of the workload in a child process pinned
+    to one BLAS/OpenMP thread, scaled to tokens/s of the whole workload."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1",
+               MKL_NUM_THREADS="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-chunked-sample", w.name,
+           "--sample-heads", str(n_heads), "--sample-chunk", str(chunk)]
+    try:
+        out = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600,
+                             check=True).stdout.strip().splitlines()[-1]
+        sec, hv = json.loads(out)
+    except (subprocess.SubprocessError, ValueError, IndexError, OSError) as e:
+        return {"unavailable": f"{type(e).__name__}"}
+    value = w.B * w.T * hv / w.Hv / sec
+    return {"value": round(value, 2), "unit": "tokens/s", "cores": 1,
+            "kind": "fp32 host chunked form (oracle package, chunk 32)",
+            "sample": f"{hv} of {w.Hv} value heads x B={w.B} x T={w.T}, fp32, {sec:.1f} s; "
+                      f"tokens/s scaled by {hv}/{w.Hv}"}
+
+
+def _cpu_chunked_sample_main(name, n_heads, chunk):
+    import numpy as np
+
+    from oracle import forms
+    w = gdn_inputs.WORKLOADS[name]
+    grp = w.Hv // w.Hk
+    sub, hv = oracle_sample(w, -(-n_heads // grp))
+    t0 = time.perf_counter()
+    forms.chunked_wy(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], sub["s0"],
+                     chunk=chunk, dtype=np.float32)
+    print(json.dumps([time.perf_counter() - t0, hv]), flush=True)
+    return 0
+
+
+def workload_config(w, world):
+    """The ``config`` object of a line, identical on both arms."""
+    return {"workload": w.name, "B": w.B, "T": w.T, "Hk": w.Hk, "Hv": w.Hv,
+            "Dk": w.Dk, "Dv": w.Dv, "chunk": w.chunk, "input_dtype": w.dtype,
+            "state": "fp32", "l2": "256 MiB flush write between timed steps",
+            "parallelism": f"replicas x{world}"}
+
+
 # ----------------------------------------------------------------------------
 # reference arm: the fp64 oracle on the host cores
 # ----------------------------------------------------------------------------
@@ -396,8 +456,7 @@ def run_reference(args, w):
         "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "T": w.T, "Hk": w.Hk, "Hv": w.Hv,
-                   "Dk": w.Dk, "Dv": w.Dv, "chunk": w.chunk, "input_dtype": w.dtype},
+        "config": workload_config(w, args.gpus),
         "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s",
                          "cores": oracle_threads(w.B * hv), "kind": "oracle",
                          "sample": sample},
@@ -410,6 +469,34 @@ def run_reference(args, w):
 
 METRIC = "GDN prefill tokens/s (B=1 T=4096 Hk=16 Hv=32 D=128 bf16 C=64) and decode steps/s"
 
+# The other prefill workloads of the plan, timed after the headline one.
+EXTRA_PREFILL = ["fp32_t64", "prefill_b4_t2048", "prefill_t65536", "prefill_b64_t16"]
+
+
+def prefill_entry(gdn, w, dev, steps, warmup, hbm, peak_kind, world):
+    ms, _ = bench_prefill(gdn, w, dev, steps, warmup, world)
+    ms = max_over_ranks(ms, world)
+    r = roofline(prefill_alg_bytes(w), ms / 1e3, hbm, peak_kind, measured_traffic(w.name))
+    r["scope"] = "whole gdn_prefill call (all its kernels)"
+    r["tensor_tflops"] = round(prefill_alg_flops(w) / (ms / 1e3) / 1e12, 2)
+    return {"ms_per_step": round(ms, 4), "steps": steps,
+            "tokens_per_s": round(world * w.B * w.T / (ms / 1e3), 1),
+            "launches_per_step": prefill_launches(w, dev), "dtype": w.dtype,
+            "config": workload_config(w, world), "roofline": r}
+
+
+def decode_entry(gdn, dev, hbm, peak_kind):
+    dw = gdn_inputs.WORKLOADS["decode_b64"]
+    us, us_warm = bench_decode(gdn, dw, dev)
+    return {
+        "workload": dw.name, "steps_per_s": round(1e6 / us, 1),
+        "tokens_per_s": round(dw.B * 1e6 / us, 1), "us_per_step": round(us, 3),
+        "us_per_step_warm_l2": round(us_warm, 3), "launches_per_step": 1,
+        "timing": "256 steps in one CUDA graph, state in place (134 MB > L2); median of 5 "
+                  "replays, each after a state reset and a 256 MiB L2 flush",
+        "roofline": roofline(decode_alg_bytes(dw), us / 1e6, hbm, peak_kind,
+                             measured_traffic("decode_b64"))}
+
 
 def main():
     ap = argparse.ArgumentParser()
@@ -419,10 +506,16 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill_t4096")
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip decode, e2e and cpu_baseline (for profiling runs)")
+                    help="skip the other workloads, decode, e2e and cpu_baseline")
     ap.add_argument("--only", default="all", choices=["all", "prefill", "decode"],
                     help="profiling runs: time one path only (prints a partial line)")
+    ap.add_argument("--cpu-chunked-sample", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--sample-heads", type=int, default=2, help=argparse.SUPPRESS)
+    ap.add_argument("--sample-chunk", type=int, default=32, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.cpu_chunked_sample:
+        return _cpu_chunked_sample_main(args.cpu_chunked_sample, args.sample_heads,
+                                        args.sample_chunk)
     args.warmup = max(args.warmup, 3)
     w = gdn_inputs.WORKLOADS[args.workload]
     if args.impl == "reference":
@@ -435,12 +528,9 @@ def main():
     gdn.lib()
     hbm, bf16, peak_kind = load_peaks()
     if args.only == "decode":
-        dw = gdn_inputs.WORKLOADS["decode_b64"]
-        us = bench_decode(gdn, dw, dev)
-        print(json.dumps({"partial": "decode only", "workload": dw.name,
-                          "us_per_step": round(us, 3),
-                          "roofline": roofline(decode_alg_bytes(dw), us / 1e6, hbm,
-                                               peak_kind)}), flush=True)
+        d = decode_entry(gdn, dev, hbm, peak_kind)
+        d["partial"] = "decode only"
+        print(json.dumps(d), flush=True)
         return 0
     if args.only == "prefill":
         args.no_extras = True
@@ -457,31 +547,31 @@ def main():
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "T": w.T, "Hk": w.Hk, "Hv": w.Hv,
-                   "Dk": w.Dk, "Dv": w.Dv, "chunk": w.chunk, "state": "fp32",
-                   "l2": "256 MiB flush write between timed steps",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(w, world),
         "roofline": roofline(prefill_alg_bytes(w), ms / 1e3, hbm, peak_kind,
-                             measured_traffic("prefill") if w.name == "prefill_t4096" else None),
+                             measured_traffic(w.name)),
         "gpu_launches": prefill_launches(w, dev) * args.steps,
         "clocks": clocks,
     }
     line["roofline"]["scope"] = "whole gdn_prefill call (all its kernels)"
     line["roofline"]["tensor_tflops"] = round(prefill_alg_flops(w) / (ms / 1e3) / 1e12, 2)
+    line["timing"] = "median of the timed steps (CUDA events on the launching stream)"
 
     if not args.no_extras:
         if rank == 0 or world > 1:
             line["e2e"] = bench_prefill_e2e(gdn, w, dev, max(3, args.steps // 5), 2)
-        dw = gdn_inputs.WORKLOADS["decode_b64"]
-        us = bench_decode(gdn, dw, dev)
-        line["decode"] = {
-            "workload": dw.name, "steps_per_s": round(1e6 / us, 1),
-            "tokens_per_s": round(dw.B * 1e6 / us, 1), "us_per_step": round(us, 3),
-            "timing": "256 steps in one CUDA graph, state in place (134 MB > L2)",
-            "roofline": roofline(decode_alg_bytes(dw), us / 1e6, hbm, peak_kind,
-                                 measured_traffic("decode"))}
+        workloads = {}
+        for name in EXTRA_PREFILL:
+            ew = gdn_inputs.WORKLOADS[name]
+            if ew.name == w.name:
+                continue
+            workloads[name] = prefill_entry(gdn, ew, dev, 20, 3, hbm, peak_kind, world)
+        workloads["decode_b64"] = decode_entry(gdn, dev, hbm, peak_kind)
+        line["workloads"] = workloads
+        line["decode"] = workloads["decode_b64"]
         if rank == 0 and world == 1:
             line["cpu_baseline"] = cpu_baseline_prefill(w)
+            line["cpu_baseline"]["chunked_fp32"] = cpu_chunked_fp32(w)
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0

@@ -8,10 +8,21 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Size limits, checked in 64-bit before any product is formed in int: the
+// kernels index heads (B*Hv, times up to 16 row tiles or chunk counts) and
+// tokens (B*T) with 32-bit grid and TMA coordinates.
+constexpr long long kMaxHeads = 1LL << 20;          // B*Hv
+constexpr long long kMaxTokens = (1LL << 31) - 1;   // B*T
+constexpr long long kMaxHeadChunks = 1LL << 24;     // B*Hv*ceil(T/16)
+
 int check_common(int B, int T, int Hk, int Hv, int Dk, int Dv, int dtype) {
   if (B <= 0 || T <= 0 || Hk <= 0 || Hv <= 0 || Dk <= 0 || Dv <= 0) return GDN_ERR_INVALID;
   if (Hv % Hk != 0) return GDN_ERR_INVALID;
   if (!gdn::head_dim_ok(Dk) || !gdn::head_dim_ok(Dv)) return GDN_ERR_UNSUPPORTED;
+  const long long heads = (long long)B * Hv;
+  if (heads > kMaxHeads || (long long)B * T > kMaxTokens ||
+      heads * (((long long)T + 15) / 16) > kMaxHeadChunks)
+    return GDN_ERR_UNSUPPORTED;
   if (dtype != GDN_DTYPE_F32 && dtype != GDN_DTYPE_BF16 && dtype != GDN_DTYPE_F16)
     return GDN_ERR_UNSUPPORTED;
   return GDN_OK;
@@ -123,7 +134,7 @@ const char* gdn_status_string(int status) {
   switch (status) {
     case GDN_OK: return "ok";
     case GDN_ERR_INVALID: return "invalid argument (null pointer, size <= 0 or Hv % Hk != 0)";
-    case GDN_ERR_UNSUPPORTED: return "unsupported shape, chunk, dtype or option (Dk, Dv in {64, 128, 256}, chunk 16/32/64, f32/bf16/f16)";
+    case GDN_ERR_UNSUPPORTED: return "unsupported shape, chunk, dtype or option (Dk, Dv in {64, 128, 256}, chunk 16/32/64, f32/bf16/f16; B*Hv <= 2^20, B*T < 2^31, B*Hv*ceil(T/16) <= 2^24)";
     case GDN_ERR_ALIGNMENT: return "pointer not 16-byte aligned (workspace: 256-byte)";
     case GDN_ERR_WORKSPACE: return "workspace missing or smaller than gdn_prefill_workspace_bytes()";
     case GDN_ERR_CUDA: return "CUDA launch error";

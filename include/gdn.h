@@ -24,8 +24,8 @@
  *
  * Ownership: the caller owns every buffer, including any workspace; the
  * library makes no device allocation at run time (the fixed scratch of
- * gdn_prefill_noalloc is a static array of the library image, 32 MiB, in
- * device memory once the library's kernels are loaded into a CUDA context).
+ * gdn_prefill_noalloc is a static array of the library image, in device
+ * memory once the library's kernels are loaded into a CUDA context).
  * All work is enqueued on `stream` (a cudaStream_t; NULL means the legacy
  * default stream) and the calls return without synchronising.
  * state_in == state_out (in place) is allowed; any other overlap between
@@ -54,7 +54,9 @@ extern "C" {
 /* Status codes. */
 #define GDN_OK                  0
 #define GDN_ERR_INVALID       (-1) /* NULL required pointer, a size <= 0, Hv % Hk != 0 */
-#define GDN_ERR_UNSUPPORTED   (-2) /* Dk/Dv not 64/128/256, chunk not 16/32/64, bad dtype */
+#define GDN_ERR_UNSUPPORTED   (-2) /* Dk/Dv not 64/128/256, chunk not 16/32/64, bad dtype,
+                                      or a size beyond the limits: B*Hv > 2^20,
+                                      B*T > 2^31 - 1, B*Hv*ceil(T/16) > 2^24 */
 #define GDN_ERR_ALIGNMENT     (-3) /* a pointer that is not 16-byte aligned */
 #define GDN_ERR_WORKSPACE     (-4) /* workspace NULL or smaller than gdn_prefill_workspace_bytes */
 #define GDN_ERR_CUDA          (-5) /* the CUDA runtime reported an error at launch; the
@@ -162,26 +164,26 @@ GDN_API int gdn_decode_step_ex(const void *q, const void *k, const void *v, cons
  * Prefill for callers that cannot allocate device memory.  This entry point
  * has no counterpart in the source pages; it exists for the library's users.
  *
- * gdn_prefill needs a caller-allocated workspace.  Callers that cannot call
- * cudaMalloc -- code running while a CUDA graph is captured, plug-ins handed
- * raw device pointers without an allocator of their own, paths that cannot
- * afford cudaMalloc's implicit synchronisation -- can call this instead.  It
- * computes exactly what gdn_prefill computes (same arguments and meaning,
- * minus the workspace) and allocates nothing: its scratch is a fixed array
- * of GDN_NOALLOC_SCRATCH_BYTES built into the library, one per GPU that loads
- * the library, held until the process exits.
+ * gdn_prefill needs a caller-allocated workspace.  Some callers cannot call
+ * cudaMalloc: plug-ins that a host application hands raw device pointers but
+ * no allocator of their own (and that must not take memory behind the host's
+ * pool), and latency-critical paths that cannot afford cudaMalloc's implicit
+ * device synchronisation.  They can call this instead.  It computes exactly
+ * what gdn_prefill computes (same arguments and meaning, minus the workspace)
+ * and allocates nothing: its scratch is a fixed array of
+ * GDN_NOALLOC_SCRATCH_BYTES built into the library, one per CUDA context that
+ * loads the library's kernels, held until that context is destroyed.
  *
  *   Limit: the problem's gdn_prefill_workspace_bytes(...) must not exceed
- *   GDN_NOALLOC_SCRATCH_BYTES (32 MiB: for bf16 inputs, B*Hv*ceil(T/64) up to
- *   682 tiles, e.g. T = 4096 with B*Hv = 10, or T = 1024 with B*Hv = 42);
- *   larger problems return GDN_ERR_NOALLOC_LIMIT with nothing enqueued.
- *   Set-up: the first call on each device (with that device current) looks
- *   up the array's device address once; make that first call before any
- *   stream capture.
- *   Sharing: every call on a device uses the same array, and the array keeps
- *   the previous call's contents (nothing in it needs to start at zero).  Two
- *   calls whose work overlaps on the GPU (different streams, no ordering
- *   between them) race on it and give undefined results; order them.
+ *   GDN_NOALLOC_SCRATCH_BYTES; larger problems return GDN_ERR_NOALLOC_LIMIT
+ *   with nothing enqueued.
+ *   Set-up: the first call in each CUDA context (with that context current)
+ *   looks up the array's device address once and remembers it for that
+ *   context; make that first call before any stream capture.
+ *   Sharing: every call in a context uses the same array, and the array
+ *   keeps the previous call's contents (nothing in it needs to start at
+ *   zero).  Two calls whose work overlaps on the GPU (different streams, no
+ *   ordering between them) race on it and give undefined results; order them.
  * Returns GDN_OK or a GDN_ERR_* code, as gdn_prefill.
  */
 #define GDN_NOALLOC_SCRATCH_BYTES (32u << 20)

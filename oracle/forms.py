@@ -62,14 +62,21 @@ def _gate_ratios(gc: np.ndarray) -> np.ndarray:
     return gam
 
 
-def chunked_wy(q, k, v, g, beta, s0=None, chunk=32):
-    """Chunked Woodbury-Young form, steps 1-9 of metaltile-std ``gated_delta_wy.rs``."""
+def chunked_wy(q, k, v, g, beta, s0=None, chunk=32, dtype=np.float64):
+    """Chunked Woodbury-Young form, steps 1-9 of metaltile-std ``gated_delta_wy.rs``.
+
+    ``dtype`` is the arithmetic type: float64 for the pins; float32 gives the
+    fp32 host chunked form the pages time against the sequential one
+    (ferrox-core ``gdn_chunk.rs``, ``CHUNK``), used only as a CPU baseline.
+    """
     q, k, v, g, beta, s0, (B, T, Hk, Hv, Dk, Dv) = _unpack(q, k, v, g, beta, s0)
+    if dtype != np.float64:
+        q, k, v, g, beta, s0 = (a.astype(dtype) for a in (q, k, v, g, beta, s0))
     C = chunk
     group = Hv // Hk
-    y = np.zeros((B, T, Hv, Dv))
-    s_out = np.zeros((B, Hv, Dv, Dk))
-    eye = np.eye(C)
+    y = np.zeros((B, T, Hv, Dv), dtype=dtype)
+    s_out = np.zeros((B, Hv, Dv, Dk), dtype=dtype)
+    eye = np.eye(C, dtype=dtype)
     for b in range(B):
         for hv in range(Hv):
             hk = hv // group
@@ -77,8 +84,9 @@ def chunked_wy(q, k, v, g, beta, s0=None, chunk=32):
             for start in range(0, T, C):
                 n = min(C, T - start)
                 # Step 1: gather the chunk, padded to C rows with g=1, beta=0.
-                Q = np.zeros((C, Dk)); K = np.zeros((C, Dk)); V = np.zeros((C, Dv))
-                gc = np.ones(C); bc = np.zeros(C)
+                Q = np.zeros((C, Dk), dtype=dtype); K = np.zeros((C, Dk), dtype=dtype)
+                V = np.zeros((C, Dv), dtype=dtype)
+                gc = np.ones(C, dtype=dtype); bc = np.zeros(C, dtype=dtype)
                 Q[:n] = q[b, start:start + n, hk]
                 K[:n] = k[b, start:start + n, hk]
                 V[:n] = v[b, start:start + n, hv]
@@ -86,7 +94,7 @@ def chunked_wy(q, k, v, g, beta, s0=None, chunk=32):
                 bc[:n] = beta[b, start:start + n, hv]
                 # Step 2: prefix gates and their ratios.
                 G = np.cumprod(gc)
-                gam = _gate_ratios(gc)
+                gam = _gate_ratios(gc).astype(dtype)
                 # Step 3: KK^T.
                 kkt = K @ K.T
                 # Step 4: (I + L) p = K, L[t, j] = beta_j KK^T[t, j] for j < t.
@@ -105,7 +113,7 @@ def chunked_wy(q, k, v, g, beta, s0=None, chunk=32):
                 corr = np.tril(qkt * bc[None, :]) @ s0p.T   # [C, Dv]
                 y_pass = G[:, None] * (s0q.T - corr)
                 # Step 8: output (with the 1/sqrt(Dk) scale).
-                y[b, start:start + n, hv] = ((y_pass + y_local) / np.sqrt(Dk))[:n]
+                y[b, start:start + n, hv] = ((y_pass + y_local) / dtype(np.sqrt(Dk)))[:n]
                 # Step 9: S_end = G_C (S0 - S0 (beta*p)^T K) + sum_j (G_C/G_j) u_j k_j^T.
                 S = G[C - 1] * (S - (s0p * bc[None, :]) @ K) + \
                     (U * gam[C - 1][:, None]).T @ K

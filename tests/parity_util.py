@@ -49,26 +49,3 @@ def gpu_prefill(ins, chunk, dev, state_mode="given", options=0):
 def oracle_prefill(ins, zero_state=False):
     s0 = None if zero_state else ins["s0"]
     return oracle.gdn_sequential(*(ins[n] for n in NAMES), s0)
-
-
-def head_slice(ins, heads):
-    """Inputs restricted to the listed (b, hv) heads, stacked as a batch of
-    single-head problems (Hk = Hv = 1), so the oracle can follow a few heads
-    of a large workload over the whole sequence."""
-    Hk, Hv = ins["q"].shape[2], ins["v"].shape[2]
-    grp = Hv // Hk
-    out = {}
-    for n in ("q", "k"):
-        out[n] = torch.stack([ins[n][b, :, hv // grp] for b, hv in heads])[:, :, None]
-    out["v"] = torch.stack([ins["v"][b, :, hv] for b, hv in heads])[:, :, None]
-    for n in ("g", "beta"):
-        out[n] = torch.stack([ins[n][b, :, hv] for b, hv in heads])[:, :, None]
-    out["s0"] = torch.stack([ins["s0"][b, hv] for b, hv in heads])[:, None]
-    return out
-
-
-def pick_heads(y, s, heads):
-    """Select (b, hv) heads from full GPU outputs, in head_slice's layout."""
-    ys = np.stack([y[b, :, hv] for b, hv in heads])[:, :, None]
-    ss = np.stack([s[b, hv] for b, hv in heads])[:, None]
-    return ys, ss

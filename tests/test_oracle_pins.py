@@ -21,7 +21,9 @@ import os
 
 import numpy as np
 import pytest
+import torch
 
+import gdn_inputs
 import oracle
 from oracle import forms
 
@@ -353,3 +355,18 @@ def test_oracle_matches_chunk_forms_at_head_dim_128(chunk, T):
     ys, ss = forms.chunked_single_solve(*args, chunk=chunk)
     for a, b in ((yc, y), (sc, s), (ys, y), (ss, s)):
         assert rel_err(a, b) <= 1e-11
+
+
+def test_fp32_chunked_form_tracks_the_oracle():
+    """The float32 run of the chunked WY form (timed only as a CPU baseline)
+    computes the same rule: it agrees with the fp64 sequential oracle to
+    float32 rounding on a multi-chunk case with a ragged tail."""
+    ins = gdn_inputs.make_inputs(1, 75, 1, 2, 16, 16, torch.float32, seed=12, u_max=0.5,
+                                 s0_std=0.1)
+    names = ("q", "k", "v", "g", "beta")
+    y32, s32 = forms.chunked_wy(*(ins[n] for n in names), ins["s0"], chunk=32,
+                                dtype=np.float32)
+    assert y32.dtype == np.float32 and s32.dtype == np.float32
+    yo, so = oracle.gdn_sequential(*(ins[n] for n in names), ins["s0"])
+    assert np.max(np.abs(y32 - yo)) <= 1e-5 * np.max(np.abs(yo))
+    assert np.max(np.abs(s32 - so)) <= 1e-5 * np.max(np.abs(so))

@@ -1,6 +1,6 @@
 """gdn_prefill_noalloc: the prefill for callers that cannot allocate device
-memory (graph capture in progress, plug-ins without an allocator, paths that
-cannot take cudaMalloc's implicit synchronisation).  It uses a fixed scratch
+memory (plug-ins handed device pointers but no allocator of their own, paths
+that cannot take cudaMalloc's implicit synchronisation).  It uses a fixed scratch
 buffer built into the library instead of a caller workspace.
 
 This file is collected last on purpose.  The test calls the entry point
