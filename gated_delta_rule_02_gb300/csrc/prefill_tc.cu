@@ -70,14 +70,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
 }
-// 16 consecutive floats from a 16-byte-aligned shared address.
-__device__ __forceinline__ void ld16f(const float* p, float* o) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float4 f = *reinterpret_cast<const float4*>(p + 4 * i);
-    o[4 * i] = f.x; o[4 * i + 1] = f.y; o[4 * i + 2] = f.z; o[4 * i + 3] = f.w;
-  }
-}
 // 16-byte store through a generic pointer into shared memory: unlike the asm
 // form it lets the compiler schedule the surrounding shared loads freely.
 __device__ __forceinline__ void st_sm16(uint8_t* base, uint32_t off, uint4 v) {
@@ -136,23 +128,53 @@ __device__ __forceinline__ void l2norm_row_sw128(uint8_t* base, int half_stride,
 // The prep kernel is persistent: one CTA per SM holds two independent groups
 // of eight warps, each with its own shared-memory map, 256 TMEM columns and
 // mbarriers, each looping over tiles.
+//
+// Per tile (64 tokens of one (b, hv) head; 64 / C chunks, every C x C matrix
+// block diagonal by chunk) a group runs, with T_L = (I + L)^-1 and
+// T_A = diag(beta) (Gam . T_L) (the second solve of step 5 without a second
+// inverse, (I + A)^-1 diag(beta) = diag(beta)(Gam . T_L)):
+//   G1  [K; Q] K^T                              -> KK^T, QK^T        (step 3)
+//   build  L = beta_j KK^T (strict lower), A3 = [diag(G) M; Gam . QK^T]
+//          with M[t][i] = beta_i QK^T[t][i] (i <= t)
+//   T_L    16 x 16 diagonal blocks by substitution (fp32), then the 16 -> 32
+//          -> 64 merges T_BA = -T_BB (L_BA T_AA) on warp-level bf16 MMAs  (step 4)
+//   coefs  cP = diag(G_C beta) T_L, cU = diag(Gam[C-1][.]) T_A
+//   GW  A3 [T_L | T_A]  -> W_M = diag(G) M T_L,  W_Y = (Gam . QK^T) T_A
+//   F1  [cP; -W_M] K    -> Pt = G_C beta P (step 9), Qh - diag(G) Q  (step 7)
+//   F2  [cU; W_Y / sqrt(Dk)] V -> Ut = Gam[C-1][.] U (step 9), y_loc / sqrt(Dk) (step 6)
+// so every row of the two final products is an output.
 constexpr int kPrepGroups = 2;
 constexpr int kPrepGroupThreads = 256;
 constexpr int kPrepThreads = kPrepGroups * kPrepGroupThreads;
-constexpr int kPrepIo = 4;  // I/O threads per group (lane 0 of warps 4-7)
-// Shared-memory map of one group (bytes from its 1024-aligned base).
+// A tile's flag counts to kTilePublished: each of the group's two I/O threads
+// (lane 0 of warps 2 and 6) adds 1 once its own stores of the tile are in
+// global memory.
+constexpr int kTilePublished = 2;
+// Shared-memory map of one group (bytes from its 1024-aligned base).  The
+// bf16 operand blocks X0..X5 are 64 rows x 64 columns, 128B-swizzled (8 KB).
 constexpr uint32_t kOffKQ = 0;        // [K;Q]: 2 halves x (64 K rows + 64 Q rows) x 128 B
 constexpr uint32_t kOffV = 32768;     // V: 2 halves x 64 rows x 128 B
-constexpr uint32_t kOffA3 = 49152;    // A3 (128 rows x 64 K-cols, one 128B half)
-constexpr uint32_t kOffB = 65536;     // X | T_L | Z (fp32) during the inverse; then A2 over X;
-                                      // then P, U (bf16, MN-major, 16 KB each)
-constexpr int kLdX = 68;
-constexpr uint32_t kOffTL = kOffB + 64 * kLdX * 4;
-constexpr uint32_t kOffZ = kOffTL + 64 * kLdX * 4;       // 32 x 32 fp32
-constexpr uint32_t kOffSmall = kOffZ + 32 * 32 * 4;      // per-token scalars
-constexpr int kLdGd = 20;                                 // row stride of the in-block ratios
-constexpr uint32_t kPrepGroupSmem = (kOffSmall + (64 * 6 + 256 + 4 + 64 * kLdGd) * 4 + 1023) & ~1023u;
+// Once F1 has read X0, X1 (and GW X2, X3), X0..X3 stage the tile's A1 rows
+// ([Pt; Qh] per chunk, 32 KB); once F2 has read X4, X5 and V, they stage y_loc
+// and Ut.  Staging blocks hold rows of 128 values as [row][64-column half],
+// each 128-byte unit 128B-swizzled, which is the box layout of the 3-D (A1,
+// Ut) and 5-D (y) tensor maps the stores use: one TMA store per output.
+constexpr uint32_t kOffX0 = 49152;    // cP                 | A1 staging (X0..X3)
+constexpr uint32_t kOffX1 = 57344;    // A3 top, then -W_M
+constexpr uint32_t kOffX2 = 65536;    // A3 bottom
+constexpr uint32_t kOffX3 = 73728;    // T_A
+constexpr uint32_t kOffX4 = 81920;    // cU                 | y_loc staging (X4, X5)
+constexpr uint32_t kOffX5 = 90112;    // T_L, then W_Y
+constexpr uint32_t kOffXd = 98304;    // fp32 [4][16][16]: the diagonal 16 x 16 blocks of L
+constexpr int kLd1 = 24;              // bf16 row stride (elements) of the 16-wide scratch
+constexpr int kLd2 = 40;              // bf16 row stride of the 32-wide scratch
+constexpr uint32_t kOffXl1 = kOffXd + 4096;          // bf16 [2][16][kLd1]: L_10, L_32
+constexpr uint32_t kOffXl2 = kOffXl1 + 2 * 16 * kLd1 * 2;  // bf16 [32][kLd2]: L_BA
+constexpr uint32_t kOffZs = kOffXl2 + 32 * kLd2 * 2;       // bf16 [32][kLd2] (merge products)
+constexpr uint32_t kOffSmall = kOffZs + 32 * kLd2 * 2;     // per-token scalars
+constexpr uint32_t kPrepGroupSmem = (kOffSmall + (64 * 9 + 4) * 4 + 1023) & ~1023u;
 constexpr uint32_t kPrepSmem = kPrepGroups * kPrepGroupSmem + 1024;
+static_assert(kPrepSmem <= 232448, "prep shared memory");
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -165,110 +187,60 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
-// Warp-level 16 x 8 x 8 tf32 MMA (fp32 accumulate): the inverse's block
-// products are too small for tcgen05 (M >= 64) and too latency-sensitive for
-// scalar FMAs.  Fragment layout (g = lane / 4, t = lane % 4):
-//   A 16 x 8 row-major: a0 (g, t) a1 (g+8, t) a2 (g, t+4) a3 (g+8, t+4)
-//   B  8 x 8:           b0 (t, g) b1 (t+4, g)
-//   D 16 x 8:           d0 (g, 2t) d1 (g, 2t+1) d2 (g+8, 2t) d3 (g+8, 2t+1)
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
+// Warp-level m16n8k16 bf16 MMA (fp32 accumulate) with ldmatrix operand loads:
+// the inverse's block products are too small for tcgen05 (M >= 64).
+// Fragments (g = lane / 4, c = lane % 4): A 16 x 16 row-major in four 8 x 8
+// matrices (rows 0-7 / 8-15 x cols 0-7 / 8-15), B 16 x 8 with b0 = rows 2c,
+// 2c+1 of column g and b1 the same 8 rows down, D d0 (g, 2c) d1 (g, 2c+1)
+// d2 (g+8, 2c) d3 (g+8, 2c+1).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
 }
-__device__ __forceinline__ void mma_tf32(float* d, const uint32_t* a, const uint32_t* bb) {
+__device__ __forceinline__ void ldsm_x2_trans(uint32_t addr, uint32_t* r) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, const uint32_t* b) {
   asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(bb[0]), "r"(bb[1]));
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
-// D(16 x 8) = A[ra.., ca..](16 x K) * B[rb.., cb..](K x 8), fp32 row-major
-// operands with row strides lda, ldb; K a multiple of 8.
-template <int K>
-__device__ __forceinline__ void warp_gemm_16x8(float* d, const float* A, int lda, const float* Bm,
-                                               int ldb, int lane) {
-  const int g = lane >> 2, t = lane & 3;
-  d[0] = d[1] = d[2] = d[3] = 0.f;
-#pragma unroll
-  for (int k0 = 0; k0 < K; k0 += 8) {
-    const uint32_t a[4] = {to_tf32(A[g * lda + k0 + t]), to_tf32(A[(g + 8) * lda + k0 + t]),
-                           to_tf32(A[g * lda + k0 + t + 4]),
-                           to_tf32(A[(g + 8) * lda + k0 + t + 4])};
-    const uint32_t bb[2] = {to_tf32(Bm[(k0 + t) * ldb + g]), to_tf32(Bm[(k0 + t + 4) * ldb + g])};
-    mma_tf32(d, a, bb);
-  }
+// Lane address of an ldmatrix.x4 A fragment (rows r0.., cols c0..) and of an
+// ldmatrix.x2.trans B fragment (rows k0.. of a row-major [k][n] block, cols
+// n0..): in a plain row-major bf16 array of `ld` elements per row ...
+__device__ __forceinline__ uint32_t a_frag_addr(uint32_t base, int ld, int r0, int c0, int lane) {
+  return base + ((r0 + (lane & 7) + 8 * ((lane >> 3) & 1)) * ld + c0 + 8 * (lane >> 4)) * 2;
 }
-__device__ __forceinline__ void warp_store_16x8(float* D, int ldd, const float* d, int lane,
-                                                float sign) {
-  const int g = lane >> 2, t = lane & 3;
-  D[g * ldd + 2 * t] = sign * d[0];
-  D[g * ldd + 2 * t + 1] = sign * d[1];
-  D[(g + 8) * ldd + 2 * t] = sign * d[2];
-  D[(g + 8) * ldd + 2 * t + 1] = sign * d[3];
+__device__ __forceinline__ uint32_t b_frag_addr(uint32_t base, int ld, int k0, int n0, int lane) {
+  return base + ((k0 + (lane & 15)) * ld + n0) * 2;
 }
-
-// T = (I + X)^-1 for X strictly lower triangular and block diagonal by chunk
-// (zero across chunks), by blocked forward substitution:
-//   16 x 16 diagonal blocks   T_ii = (I + X_ii)^-1       (one column per thread)
-//   32 x 32 blocks (C >= 32)  T_10 = -T_11 X_10 T_00      (per 16-block pair)
-//   64 x 64 (C = 64)          T_BA = -T_BB X_BA T_AA      (32-block halves)
-// The block products run on warp-level tf32 MMAs; the group's 256 threads call
-// this (u = thread index in the group, sync = the group's barrier).
-template <int C, typename Sync>
-__device__ void invert_unit_lower(const float* X, float* Tm, float* Zs, int u, Sync sync) {
-  for (int idx = u; idx < 64 * 64; idx += kPrepGroupThreads) {
-    const int r = idx >> 6, c = idx & 63;
-    if ((c >> 4) > (r >> 4) || (c / C) != (r / C)) Tm[r * kLdX + c] = 0.f;
-  }
-  if (u < 64) {
-    const int base = (u >> 4) * 16, jj = u & 15;
-    float x[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      float a0 = (r == jj) ? 1.f : 0.f, a1 = 0.f;
-      const float* xr = X + (base + r) * kLdX + base;
-#pragma unroll
-      for (int s = 0; s + 1 < r; s += 2) {
-        a0 = fmaf(-xr[s], x[s], a0);
-        a1 = fmaf(-xr[s + 1], x[s + 1], a1);
-      }
-      if (r & 1) a0 = fmaf(-xr[r - 1], x[r - 1], a0);
-      x[r] = a0 + a1;
-    }
-#pragma unroll
-    for (int r = 0; r < 16; ++r) Tm[(base + r) * kLdX + base + jj] = x[r];
-  }
-  sync();
-  const int w = u >> 5, lane = u & 31;
-  if constexpr (C >= 32) {
-    // Pairs (0,1) and (2,3): warp w < 4 handles pair w/2, columns 8*(w%2)..
-    float d[4];
-    const int p = (w >> 1) & 1, nt = w & 1;
-    const int r0 = (2 * p + 1) * 16, c0 = 2 * p * 16;
-    if (w < 4) {
-      warp_gemm_16x8<16>(d, X + r0 * kLdX + c0, kLdX, Tm + c0 * kLdX + c0 + nt * 8, kLdX, lane);
-      warp_store_16x8(Zs + p * 256 + nt * 8, 16, d, lane, 1.f);
-    }
-    sync();
-    if (w < 4) {
-      warp_gemm_16x8<16>(d, Tm + r0 * kLdX + r0, kLdX, Zs + p * 256 + nt * 8, 16, lane);
-      warp_store_16x8(Tm + r0 * kLdX + c0 + nt * 8, kLdX, d, lane, -1.f);
-    }
-    sync();
-  }
-  if constexpr (C == 64) {
-    // M = X[32:64][0:32] T[0:32][0:32], then T[32:64][0:32] = -T[32:64][32:64] M;
-    // warp w computes the 16 x 8 tile (w/4, w%4) of each.
-    float d[4];
-    const int mt = w >> 2, nt = w & 3;
-    warp_gemm_16x8<32>(d, X + (32 + mt * 16) * kLdX, kLdX, Tm + nt * 8, kLdX, lane);
-    warp_store_16x8(Zs + mt * 16 * 32 + nt * 8, 32, d, lane, 1.f);
-    sync();
-    warp_gemm_16x8<32>(d, Tm + (32 + mt * 16) * kLdX + 32, kLdX, Zs + nt * 8, 32, lane);
-    warp_store_16x8(Tm + (32 + mt * 16) * kLdX + nt * 8, kLdX, d, lane, -1.f);
-    sync();
-  }
+// ... and in a 128B-swizzled 64-column block (row stride 128 B).
+__device__ __forceinline__ uint32_t a_frag_addr_sw(uint32_t base, int r0, int c0, int lane) {
+  const int r = r0 + (lane & 7) + 8 * ((lane >> 3) & 1), c = c0 + 8 * (lane >> 4);
+  return base + sw128(r, c);
+}
+__device__ __forceinline__ uint32_t b_frag_addr_sw(uint32_t base, int k0, int n0, int lane) {
+  return base + sw128(k0 + (lane & 15), n0);
+}
+// Writes a 16 x 8 fp32 fragment times `sign` as bf16 at (r0, c0) of a
+// swizzled block / of a row-major bf16 array.
+__device__ __forceinline__ void st_frag_sw(uint8_t* blk, int r0, int c0, const float* d, float sign,
+                                           int lane) {
+  const int g = lane >> 2, c = 2 * (lane & 3);
+  *reinterpret_cast<uint32_t*>(blk + sw128(r0 + g, c0 + c)) = pack_bf16x2(sign * d[0], sign * d[1]);
+  *reinterpret_cast<uint32_t*>(blk + sw128(r0 + g + 8, c0 + c)) =
+      pack_bf16x2(sign * d[2], sign * d[3]);
+}
+__device__ __forceinline__ void st_frag(uint8_t* arr, int ld, int r0, int c0, const float* d,
+                                        int lane) {
+  const int g = lane >> 2, c = 2 * (lane & 3);
+  *reinterpret_cast<uint32_t*>(arr + ((r0 + g) * ld + c0 + c) * 2) = pack_bf16x2(d[0], d[1]);
+  *reinterpret_cast<uint32_t*>(arr + ((r0 + g + 8) * ld + c0 + c) * 2) = pack_bf16x2(d[2], d[3]);
 }
 
 // Everything the prep work needs (the tensor maps are kernel parameters).
@@ -276,26 +248,22 @@ struct PrepParams {
   const bf16* k;  // the raw inputs, for L2 prefetches
   const bf16* q;
   const bf16* v;
-  const CUtensorMap* tm_k;
-  const CUtensorMap* tm_q;
-  const CUtensorMap* tm_v;
-  const CUtensorMap* tm_a1s;
-  const CUtensorMap* tm_us;
+  const CUtensorMap* tm_a1o;  // A1 as [rows][2][64] (3-D), box {64, 2, 128}
+  const CUtensorMap* tm_uo;   // Ut as [rows][2][64], box {64, 2, 64}
+  const CUtensorMap* tm_yo;   // y as [B][T][Hv][2][64] (5-D), box {64, 2, 1, 64, 1}
   const bf16* g;
   const bf16* beta;
   float* wsGC;
   int T, Hk, Hv, NT, BH;
   int opts;  // kOpt* bits
-  // y_loc / sqrt(Dk) goes straight to y ([B, T, Hv, 128], 64-token boxes); the
-  // scan then adds Qh S^T / sqrt(Dk) to it.
-  const CUtensorMap* tm_y;
+  // y_loc / sqrt(Dk) goes straight into y; the scan then adds Qh S^T / sqrt(Dk).
   float yscale;
 };
 
 // The prep work of one CTA (both groups): CTA `cta_rank` of `n_ctas` doing prep.
 // With `flags`, each finished tile (b*Hv + hv, n) is published by raising
-// flags[(b*Hv + hv) * NT + n] to kPrepIo: each I/O thread adds 1 once its own
-// stores of the tile are in memory.
+// flags[(b*Hv + hv) * NT + n] to kTilePublished: each I/O thread adds 1 once
+// its own stores of the tile are in global memory.
 template <int C>
 __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw, int cta_rank,
                                           int n_ctas, int* flags) {
@@ -303,38 +271,35 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
   const bf16* __restrict__ g = P.g;
   const bf16* __restrict__ beta = P.beta;
   float* __restrict__ wsGC = P.wsGC;
-  __shared__ uint64_t bars[kPrepGroups][4];
+  // Per group: K and Q landed (128 cp.async arrivals, stream A), G1, GW, F1, F2,
+  // V landed (128 arrivals, stream B) -- each completes once per tile.
+  __shared__ uint64_t bars[kPrepGroups][6];
   __shared__ uint32_t tmem_base_sh;
   __shared__ float carry_sh[kPrepGroups];
   __shared__ int abort_sh[kPrepGroups];
   const int grp = threadIdx.x / kPrepGroupThreads;
-  const int tid = threadIdx.x % kPrepGroupThreads, warp = tid >> 5;  // within the group
+  const int tid = threadIdx.x % kPrepGroupThreads, warp = tid >> 5, lane = tid & 31;
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~(uintptr_t)1023) +
                 grp * kPrepGroupSmem;
   const uint32_t sbase = smem_u32(sm);
-  const uint32_t bar_tma = smem_u32(&bars[grp][0]), bar_mma = smem_u32(&bars[grp][1]);
-  // G2 and G3 completions of the P stream (bar_p) and of the U stream (bar_u):
-  // two per tile each, so the first wait of a tile is on parity 0, the second on 1.
-  const uint32_t bar_p = smem_u32(&bars[grp][2]), bar_u = smem_u32(&bars[grp][3]);
-  // Named barriers of the group: the whole group, its gate warps (0-3) and the
-  // two warps of the prefix sum.
-  const int sync_id = 1 + 2 * grp, gates_id = 2 + 2 * grp, carry_id = 5 + grp;
-  // Warps 0, 1, 4, 5 (TMEM lanes 0-63: X, later the P stream) and warps 2, 3, 6,
-  // 7 (lanes 64-127: the U stream).
-  const int pstream_id = 7 + grp, ustream_id = 9 + grp;
-  const bool pstream = (warp & 3) < 2;
-  float* X = reinterpret_cast<float*>(sm + kOffB);               // 64 x 68 fp32
-  float* TL = reinterpret_cast<float*>(sm + kOffTL);             // 64 x 68 fp32
-  float* Zs = reinterpret_cast<float*>(sm + kOffZ);              // 32 x 32 fp32
-  float* lam = reinterpret_cast<float*>(sm + kOffSmall);         // chunk-local sum of log2 g
+  const uint32_t bar_tma = smem_u32(&bars[grp][0]), bar_g1 = smem_u32(&bars[grp][1]);
+  const uint32_t bar_gw = smem_u32(&bars[grp][2]), bar_f1 = smem_u32(&bars[grp][3]);
+  const uint32_t bar_f2 = smem_u32(&bars[grp][4]), bar_v = smem_u32(&bars[grp][5]);
+  // Named barriers of the group: the whole group, the two warps of the gate
+  // prefix sums, the two epilogue streams (warps 0-3: F1; warps 4-7: F2) and the
+  // four warps on the KK^T lanes (0, 1, 4, 5).
+  const int sync_id = 1 + grp, carry_id = 3 + grp, streamA_id = 5 + grp, streamB_id = 7 + grp;
+  const int kk_id = 9 + grp;
+  const bool streamA = warp < 4;
+  float* Xd = reinterpret_cast<float*>(sm + kOffXd);
+  float* lam = reinterpret_cast<float*>(sm + kOffSmall);  // chunk-local sum of log2 g
   float* bta = lam + 64;
   float* gsuf = bta + 64;   // g_{t+1} ... g_{chunk end}
   float* gpw = gsuf + 64;   // G_t = g_{chunk start} ... g_t
   float* sfac = gpw + 64;   // 2^(lam[end of t's 16-block] - lam_t)
-  float* rfac = sfac + 64;  // [64][4]: 2^(lam_t - lam[end of block b]), b before t's block
+  float* rfac = sfac + 64;  // [64][4]: 2^(lam_t - lam[end of block b]), b before t's block, same chunk
   float* gc = rfac + 256;   // G at each chunk's end
-  float* gdiag = gc + 4;    // [64][kLdGd]: Gam[t][j] for j in t's 16-block, j <= t
   auto gsync = [&]() { named_bar_sync(sync_id, kPrepGroupThreads); };
   // Group-wide AND of ok (sticky: a group that failed a wait stops).
   auto gsync_and = [&](bool v) {
@@ -345,7 +310,7 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
 
   if (threadIdx.x == 0) {
     for (int q = 0; q < kPrepGroups; ++q) {
-      for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bars[q][i]), 1);
+      for (int i = 0; i < 6; ++i) mbar_init(smem_u32(&bars[q][i]), (i == 0 || i == 5) ? 128 : 1);
       abort_sh[q] = 0;
     }
     fence_mbar_init();
@@ -366,27 +331,40 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
   const int gid = cta_rank * kPrepGroups + grp;
   auto head_of = [&](int lin) { return lin % BH; };
   auto tile_of = [&](int lin) { return lin / BH; };
-  // The group's TMA traffic is spread over four threads (lane 0 of warps 4-7),
-  // since one thread issues these instructions slowly.  I/O thread `io`
-  // owns one 64-column half: io 0/1 load K and Q half io and store the Pt and
-  // Qh halves staged over K; io 2/3 load V half io-2 and store the Ut and y_loc
-  // halves staged over V.  Each waits for its own stores before reloading the
-  // region they read.  io 0 posts the byte count of the whole tile.
-  const int io = (warp >= 4 && (tid & 31) == 0) ? warp - 4 : -1;
-  // K and V of tile `lin` (io 0 also posts the byte count of K, Q and V) ...
-  auto load_kv = [&](int lin) {
-    const int bh = head_of(lin), n = tile_of(lin);
-    const int b = bh / Hv, hv = bh - b * Hv, hk = key_head(hv, Hk, Hv, opts), t0 = n * kTile;
-    if (io == 0) mbar_expect_tx(bar_tma, 6 * 8192);
-    if (io < 2) tma_load_4d(sbase + kOffKQ + io * 16384, P.tm_k, bar_tma, 64 * io, hk, t0, b);
-    else tma_load_4d(sbase + kOffV + (io - 2) * 8192, P.tm_v, bar_tma, 64 * (io - 2), hv, t0, b);
+  // Inputs come in with cp.async (16 bytes a thread, written straight into the
+  // 128B-swizzled operand layout; rows past T read as zeros), which does not
+  // queue behind the TMA stores of the outputs.  Stream A (warps 0-3) loads the
+  // next tile's K and Q once this tile's F1 and Qh epilogue are done with them;
+  // stream B (warps 4-7) loads a tile's V at its start, once the previous Ut
+  // store (staged over V) has read it.  Each of the 128 threads then arrives on
+  // the tile's barrier when its copies have landed.
+  auto load_rows = [&](const bf16* src, int heads, int hh, int b, int t0, uint32_t dst_base,
+                       uint32_t half_stride) {
+    const int u = tid & 127;
+#pragma unroll 4
+    for (int i = 0; i < 8; ++i) {
+      const int idx = u + 128 * i, r = idx >> 4, cc = idx & 15;
+      const int tok = t0 + r;
+      const bf16* gp = src + (((size_t)b * T + (tok < T ? tok : T - 1)) * heads + hh) * kD + cc * 8;
+      cp_async16(dst_base + (cc >> 3) * half_stride + sw128(r, (cc & 7) * 8), gp,
+                 tok < T ? 16u : 0u);
+    }
   };
-  // ... and its Q (io 0 and 1).
-  auto load_q = [&](int lin) {
-    const int bh = head_of(lin), n = tile_of(lin);
-    const int b = bh / Hv, hv = bh - b * Hv, hk = key_head(hv, Hk, Hv, opts), t0 = n * kTile;
-    if (io < 2) tma_load_4d(sbase + kOffKQ + io * 16384 + 8192, P.tm_q, bar_tma, 64 * io, hk, t0, b);
+  auto load_kq = [&](int lin) {  // stream A
+    const int bh = head_of(lin), b = bh / Hv, hv = bh - b * Hv;
+    const int hk = key_head(hv, Hk, Hv, opts), t0 = tile_of(lin) * kTile;
+    load_rows(P.k, Hk, hk, b, t0, sbase + kOffKQ, 16384);
+    load_rows(P.q, Hk, hk, b, t0, sbase + kOffKQ + 8192, 16384);
+    cp_async_mbar_arrive(bar_tma);
   };
+  auto load_v = [&](int lin) {  // stream B
+    const int bh = head_of(lin), b = bh / Hv, hv = bh - b * Hv, t0 = tile_of(lin) * kTile;
+    load_rows(P.v, Hv, hv, b, t0, sbase + kOffV, 8192);
+    cp_async_mbar_arrive(bar_v);
+  };
+  // The two I/O threads issue the tile's TMA stores (io 0: A1; io 1: y_loc and
+  // Ut) and publish the tile once those have landed.
+  const int io = tid == 64 ? 0 : (tid == 192 ? 1 : -1);
   // Gate and beta of token `tid` of a tile, read one tile ahead into registers
   // as raw bf16 bits (converted when used, so the load is not waited for here).
   // Padded tokens: decay 1 (gate 1.0, or log-gate 0.0), beta 0.
@@ -406,65 +384,48 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
     }
   };
   auto bits_to_f32 = [](uint16_t x) { return __uint_as_float((uint32_t)x << 16); };
-  if (gid < total && io >= 0) {
-    prefetch_tmap(io < 2 ? P.tm_k : P.tm_v);
-    if (io < 2) prefetch_tmap(P.tm_q);
-    load_kv(gid);
-    load_q(gid);
+  if (io == 0) prefetch_tmap(P.tm_a1o);
+  if (io == 1) {
+    prefetch_tmap(P.tm_yo);
+    prefetch_tmap(P.tm_uo);
+  }
+  if (gid < total) {
+    if (streamA) load_kq(gid);
+    else load_v(gid);
   }
   load_gates(gid);
 
   bool ok = true;
-  bool tma_pending = gid < total;  // a load phase was issued and not yet waited for
-  // Publishing: each I/O thread adds 1 to a tile's flag once all of its stores
-  // of the tile are in memory, so the flag reaches kPrepIo when the whole tile
-  // is.  It does so after the next tile's loads have landed (they were issued
-  // after these stores), when the wait for the stores is normally over.
+  // The tile whose stores this I/O thread has issued but not yet published.
   size_t unpublished = ~(size_t)0;
   auto publish = [&]() {
     if (unpublished != ~(size_t)0) {
       bulk_wait_all();
       fence_proxy_async_global();
-      red_release_gpu_add(flags + unpublished, 1);
+      if (flags) red_release_gpu_add(flags + unpublished, 1);
       unpublished = ~(size_t)0;
     }
   };
+  // TMEM lane quadrant of this warp, its row in a 128-lane accumulator and the
+  // token row t of a 64-row half.
+  const int q4 = warp & 3, lrow = q4 * 32 + lane, trow = lrow & 63;
+  const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
   int it = 0;
-  for (int lin = gid; lin < total && ok; lin += ngroups, ++it) {
+  // ok (false once a bounded wait has given up) is made uniform by the first
+  // group barrier of each tile, where the loop stops, so every thread passes the
+  // same barriers.
+  for (int lin = gid; lin < total; lin += ngroups, ++it) {
   const size_t tile_id = (size_t)head_of(lin) * NT + tile_of(lin);
   const int next = lin + ngroups;
   const float gv_cur = bits_to_f32(g_next), bt_cur = bits_to_f32(b_next);
   load_gates(next);
-  // Warm L2 with the next tile's K, Q and V rows: warps 2-7 (u = tid - 64), one
-  // 256-byte token row of one tensor per thread, as plain prefetches that leave
-  // the TMA unit free.  Issued while those warps wait for the inverse's first
-  // stage, which only warps 0-1 work on.
-  auto prefetch_next = [&]() {
-    const int u = tid - 64;
-    if (next >= total || u < 0 || u >= 3 * kTile) return;
-    const int nbh = head_of(next), nb = nbh / Hv, nhv = nbh - nb * Hv;
-    const int nhk = key_head(nhv, Hk, Hv, opts), tok = tile_of(next) * kTile + (u & (kTile - 1));
-    if (tok < T) {
-      const int which = u / kTile;  // 0: K, 1: Q, 2: V
-      const bf16* base = which == 0 ? P.k : (which == 1 ? P.q : P.v);
-      const int heads = which == 2 ? Hv : Hk, hh = which == 2 ? nhv : nhk;
-      const char* row = reinterpret_cast<const char*>(base + (((size_t)nb * T + tok) * heads + hh) * kD);
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(row) : "memory");
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(row + 128) : "memory");
-    }
-  };
-
   // Gates (step 2).  Padded tokens take g = 1, beta = 0.  Decay products are
   // carried as chunk-local prefix sums lam of log2 g: G_t = 2^lam_t and
   // Gam[t][j] = 2^(lam_t - lam_j) (j <= t) -- never a quotient, so a vanishing
-  // product underflows to 0.  Gam is used factored per 16-token block b:
-  // across 16-token blocks, Gam[t][j] = rfac[t][b(j)] * sfac[j] with the
-  // block end as the split point, so both factors are products of decays (<= 1);
-  // inside a block it is 2^(lam_t - lam_j) directly.  Warps 0-1 form the
-  // prefix sums (one token per thread); warps 0-3 then derive the tables (two
-  // threads per token).
+  // product underflows to 0.  Warps 0-1 form the prefix sums (one token per
+  // thread) and the per-token tables.
   if (tid < 64) {
-    const int t = tid, lane = tid & 31;
+    const int t = tid;
     bta[t] = bt_cur;  // padded tokens: g = 1, beta = 0
     // log2 of the decay (clamped: a vanishing decay underflows the products to 0)
     float l = fmaxf((opts & kOptLogGate) ? gv_cur * 1.4426950408889634f : lg2(gv_cur), -1000.f);
@@ -480,45 +441,35 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
       if (tid >= 32) l += carry_sh[grp];
     }
     lam[t] = l;
-  }
-  if (tid < 128) {
-    named_bar_sync(gates_id, 128);
-    const int t = tid >> 1, p = tid & 1;
-    const float l = lam[t];
-    const int tb = t & ~15, tt = t & 15;
-    float* gd = gdiag + t * kLdGd + 8 * p;
+    named_bar_sync(carry_id, 64);
+    // Per-token tables: G_t, the decay to the chunk's end, and the two
+    // factors of Gam across 16-token blocks (both products of decays, <= 1):
+    // Gam[t][j] = rfac[t][b(j)] sfac[j] for j in an earlier block b(j).
+    const int cs = (t / C) * C, tb = t >> 4;
+    gsuf[t] = ex2(lam[cs + C - 1] - l);
+    gpw[t] = ex2(l);
+    sfac[t] = ex2(lam[t | 15] - l);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int j = 8 * p + e;  // in-block ratios (entries past t are never read)
-      gd[e] = j <= tt ? ex2(l - lam[tb + j]) : 0.f;
-    }
-    const int ce = (t / C) * C + C - 1, cs = (t / C) * C;
-    const float lend = lam[ce];
-    if (p == 0) {
-      gsuf[t] = ex2(lend - l);
-      gpw[t] = ex2(l);
-      sfac[t] = ex2(lam[(t | 15)] - l);
-    } else {
-#pragma unroll
-      for (int bb = 0; bb < 4; ++bb)
-        rfac[t * 4 + bb] = (bb * 16 >= cs && bb < (t >> 4)) ? ex2(l - lam[bb * 16 + 15]) : 0.f;
-      if (t == ce) gc[t / C] = ex2(lend);
-    }
+    for (int bb = 0; bb < 4; ++bb)
+      rfac[t * 4 + bb] = (bb < tb && 16 * bb >= cs) ? ex2(l - lam[16 * bb + 15]) : 0.f;
+    if ((t % C) == C - 1) gc[t / C] = ex2(l);
   }
 
-  ok = mbar_wait(bar_tma, it & 1);
-  tma_pending = false;
-  if (ok && io >= 0) publish();
+  ok = ok && mbar_wait(bar_tma, it & 1);
+  fence_proxy_async();  // the cp.async writes of K, Q, seen before the tensor core reads them
+  // The previous tile's stores have read their staging (X0..X5, V) before this
+  // tile rewrites it.
+  if (io >= 0) bulk_wait_read_all();
   if (opts & kOptL2NormQK) {  // rows 0-63 of each half are K, 64-127 Q
     if (ok) l2norm_row_sw128(sm + kOffKQ, 16384, tid >> 1, tid & 1);
     fence_proxy_async();
     gsync();
   }
-  // G1: D[128 x 64] = [K; Q] K^T  (TMEM columns 0..63), issued outside the gate
-  // warps (lane 1 of warp 4).  The previous tile's last stores must have read A3 and X, which
-  // this tile rewrites after G1.
-  if (io >= 0) bulk_wait_read_all();
-  if (ok && tid == 129) {
+  ok = gsync_and(ok);  // also publishes the gate scalars
+  if (!ok) break;
+  // G1: D[128 x 64] = [K; Q] K^T (TMEM columns 0..63), issued by a thread
+  // outside the gate warps (lane 1 of warp 4).
+  if (tid == 129) {
     tc_fence_after();
     const uint32_t id1 = idesc_bf16(128, 64, false, false);
 #pragma unroll
@@ -527,290 +478,341 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
       mma_bf16_ss(tmem, smem_desc(a, 16, 1024, kSw128), smem_desc(a, 16, 1024, kSw128), id1,
                   kk > 0);
     }
-    mma_commit(bar_mma);
+    mma_commit(bar_g1);
   }
-  ok = gsync_and(ok);  // also publishes the gate scalars
-  ok = ok && mbar_wait(bar_mma, it & 1);  // G1 completes once per tile
+  if (io >= 0) publish();        // the previous tile, stored a while ago
+  if (!streamA && it > 0) load_v(lin);  // V for F2, over the previous Ut staging
+  ok = ok && mbar_wait(bar_g1, it & 1);
   tc_fence_after();
-  if (ok) {
-    // Row t of KK^T (TMEM lanes 0..63) -> row t of X = L (step 4):
-    //   X[t][j] = beta_j KK^T[t][j], j < t in t's chunk.
-    // Row t of QK^T (lanes 64..127) -> rows t and 64+t of
-    //   A3 = [diag(G) M; Gam . QK^T], M[t][i] = beta_i QK^T[t][i], i <= t (steps 6, 7).
-    // Warps w and w+4 share TMEM lane quadrant w % 4 and take 32 columns each.
-    const int q4 = warp & 3, lrow = q4 * 32 + (tid & 31);
-    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-    const int t = lrow & 63;
-    const int cs = (t / C) * C, bt = t >> 4;
-    const float gt = gpw[t];
+  // Warps w and w+4 share TMEM lane quadrant w % 4 and take 32 columns each.
+  // The warps on the KK^T lanes (0, 1, 4, 5) build L and go on to the
+  // inverse's diagonal blocks, which need nothing else; the warps on the QK^T
+  // lanes (2, 3, 6, 7) build A3 meanwhile and meet them at the first merge.
+  const bool kk_lanes = lrow < 64;
+  {
+    const int t = trow, cs = (t / C) * C, tb = t >> 4;
     const int cbeg = (warp >> 2) * 32;
-    float vv[2][16];  // both 16-column blocks, one TMEM round trip
-    tmem_ld16(tmem + lane_base + cbeg, vv[0]);
-    tmem_ld16(tmem + lane_base + cbeg + 16, vv[1]);
-    tmem_wait_ld();
+    float v[32];
+    if (ok) {
+      tmem_ld16(tmem + lane_base + cbeg, v);
+      tmem_ld16(tmem + lane_base + cbeg + 16, v + 16);
+      tmem_wait_ld();
+    }
+    if (kk_lanes) {
+      // Row t of KK^T -> L[t][j] = beta_j KK^T[t][j], j < t in t's chunk: its
+      // diagonal 16 x 16 block in fp32 (Xd) and, as bf16, the blocks the merges
+      // read (L_10, L_32 in Xl1; L_BA in Xl2).
+      if (ok) {
 #pragma unroll
-    for (int c0 = cbeg; c0 < cbeg + 32; c0 += 16) {
-      const float* v = vv[(c0 - cbeg) >> 4];
-      // A 16-column block lies wholly inside or outside t's chunk (16 | C); it
-      // is before, on or after t's own 16-block.
-      const int cb = c0 >> 4, tt = t & 15;
-      const bool live = c0 >= cs && cb <= bt, diag = cb == bt;
-      float b16[16];
-      ld16f(bta + c0, b16);
-      if (lrow < 64) {
-        float o[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) o[e] = (live && (!diag || e < tt)) ? b16[e] * v[e] : 0.f;
-#pragma unroll
-        for (int e = 0; e < 16; e += 4)
-          *reinterpret_cast<float4*>(X + t * kLdX + c0 + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
-      } else {
-        float top[16], bot[16], gam[16];
-        if (diag) {
-          ld16f(gdiag + t * kLdGd, gam);
-        } else {
-          ld16f(sfac + c0, gam);
-          const float rb = rfac[t * 4 + cb];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) gam[e] *= rb;
+        for (int e = 0; e < 32; ++e) {
+          const int j = cbeg + e;
+          v[e] = (j < t && j >= cs) ? bta[j] * v[e] : 0.f;
         }
+        if ((tb >> 1) == (cbeg >> 5)) {  // t's diagonal block lies in these 32 columns
+          float* xd = Xd + tb * 256 + (t & 15) * 16;
+          const bool hi = tb & 1;  // which 16 of the 32 columns (selects keep v in registers)
+          float src[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) src[e] = hi ? v[16 + e] : v[e];
+#pragma unroll
+          for (int e = 0; e < 16; e += 4)
+            *reinterpret_cast<float4*>(xd + e) =
+                make_float4(src[e], src[e + 1], src[e + 2], src[e + 3]);
+        }
+        uint8_t* xl1 = sm + kOffXl1;
+        if (cbeg == 0 && t >= 16 && t < 32) {  // L_10: rows 16-31, cols 0-15
+          uint8_t* row = xl1 + ((t - 16) * kLd1) * 2;
+          *reinterpret_cast<uint4*>(row) = pack8(v);
+          *reinterpret_cast<uint4*>(row + 16) = pack8(v + 8);
+        }
+        if (cbeg == 32 && t >= 48) {  // L_32: rows 48-63, cols 32-47
+          uint8_t* row = xl1 + ((16 + t - 48) * kLd1) * 2;
+          *reinterpret_cast<uint4*>(row) = pack8(v);
+          *reinterpret_cast<uint4*>(row + 16) = pack8(v + 8);
+        }
+        if (cbeg == 0 && t >= 32) {  // L_BA: rows 32-63, cols 0-31
+          uint8_t* row = sm + kOffXl2 + ((t - 32) * kLd2) * 2;
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) *reinterpret_cast<uint4*>(row + 2 * e) = pack8(v + e);
+        }
+      }
+      tc_fence_before();
+      named_bar_sync(kk_id, 128);
+      // Step 4, T_L = (I + L)^-1 into X5 (bf16, row-major [t][j]): the
+      // diagonal 16 x 16 blocks (warps 0, 1), and zeros in the blocks no merge
+      // writes (warps 4, 5).  It runs on whatever L holds even after a failed
+      // wait, so every thread passes the same barriers.
+      uint8_t* x5 = sm + kOffX5;
+      if (warp < 4) {
+        // block bl, column jj, by forward substitution (fp32)
+        const int bl = tid >> 4, jj = tid & 15;
+        const float* xd = Xd + bl * 256;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          float a0 = (r == jj) ? 1.f : 0.f, a1 = 0.f;
+          const float* xr = xd + r * 16;
+#pragma unroll
+          for (int s = 0; s + 1 < r; s += 2) {
+            a0 = fmaf(-xr[s], x[s], a0);
+            a1 = fmaf(-xr[s + 1], x[s + 1], a1);
+          }
+          if (r & 1) a0 = fmaf(-xr[r - 1], x[r - 1], a0);
+          x[r] = a0 + a1;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+          *reinterpret_cast<bf16*>(x5 + sw128(16 * bl + r, 16 * bl + jj)) =
+              __float2bfloat16_rn(x[r]);
+      } else {
+        // above the diagonal, and across chunks (C < 64): 32 16-byte pieces a block
+        for (int p = tid - 128; p < 16 * 32; p += 64) {
+          const int blk = p >> 5, rb = blk >> 2, cb = blk & 3;
+          if (cb > rb || (16 * rb) / C != (16 * cb) / C) {
+            const int r = 16 * rb + ((p & 31) >> 1), c = 16 * cb + 8 * (p & 1);
+            *reinterpret_cast<uint4*>(x5 + sw128(r, c)) = make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
+    } else if (ok) {
+      // Row t of QK^T -> rows t of A3 top (X1) and bottom (X2):
+      //   diag(G) M and Gam . QK^T,  M[t][i] = beta_i QK^T[t][i], i <= t.
+      // Gam inside t's 16-block is 2^(lam_t - lam_j); across blocks it is
+      // rfac[t][b] sfac[j].
+      const float gt = gpw[t], lt = lam[t];
+      float top[32];
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        const int jb = (cbeg >> 4) + hb;
+        const float rb = jb < 4 ? rfac[t * 4 + jb] : 0.f;
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const bool keep = live && (!diag || e <= tt);
-          top[e] = keep ? gt * b16[e] * v[e] : 0.f;
-          bot[e] = keep ? gam[e] * v[e] : 0.f;
+          const int j = cbeg + 16 * hb + e;
+          const bool keep = j <= t && j >= cs;
+          const float gm = jb == tb ? ex2(lt - lam[j]) : rb * sfac[j];
+          top[16 * hb + e] = keep ? gt * bta[j] * v[16 * hb + e] : 0.f;
+          v[16 * hb + e] = keep ? gm * v[16 * hb + e] : 0.f;
         }
-        st_sm16(sm, kOffA3 + sw128(t, c0), pack8(top));
-        st_sm16(sm, kOffA3 + sw128(t, c0 + 8), pack8(top + 8));
-        st_sm16(sm, kOffA3 + sw128(64 + t, c0), pack8(bot));
-        st_sm16(sm, kOffA3 + sw128(64 + t, c0 + 8), pack8(bot + 8));
       }
+#pragma unroll
+      for (int e = 0; e < 32; e += 8) {
+        st_sm16(sm, kOffX1 + sw128(t, cbeg + e), pack8(top + e));
+        st_sm16(sm, kOffX2 + sw128(t, cbeg + e), pack8(v + e));
+      }
+      fence_proxy_async();
     }
   }
-  // Step 4: T_L = (I + L)^-1.  Step 5 needs no second inverse:
-  // (I + A)^-1 diag(beta) = diag(beta) (Gam . T_L) for A[t][j] = beta_t Gam[t][j] KK^T[t][j].
-  // The inverse's first stage (warps 0-1) needs only X, written by warps 0, 1, 4
-  // and 5; the A3 builders (warps 2, 3, 6, 7) finish meanwhile and meet the
-  // group at the inverse's first barrier.  The inverse runs (on whatever X
-  // holds) even after a failed wait, so every thread passes the same barriers;
-  // ok is made uniform after it.
-  if (pstream) named_bar_sync(pstream_id, 128);
-  prefetch_next();
-  invert_unit_lower<C>(X, TL, Zs, tid, gsync);
+  tc_fence_before();
+  gsync();
 
-  // A2 = [T_L; diag(beta) (Gam . T_L)]: 128 rows x 64 K-cols, K-major 128B swizzle.
-  // Thread: 8 columns (col0..col0+7) of T_L rows r0 and r0+32, written as rows
-  // t and 64+t of A2.
-  if (ok) {
-    const int col0 = (tid & 7) * 8, r0 = tid >> 3, bj = col0 >> 4;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int t = r0 + 32 * i;
-      const float4 a = *reinterpret_cast<const float4*>(TL + t * kLdX + col0);
-      const float4 c4 = *reinterpret_cast<const float4*>(TL + t * kLdX + col0 + 4);
-      float v[8] = {a.x, a.y, a.z, a.w, c4.x, c4.y, c4.z, c4.w};
-      st_sm16(sm, kOffB + sw128(t, col0), pack8(v));
-      // T_L is zero above the diagonal and across chunks (rfac is 0 there too).
-      float f[8];
-      const float bt = bta[t];
-      if (bj < (t >> 4)) {
-        const float rb = bt * rfac[t * 4 + bj];
-        const float4 s0 = *reinterpret_cast<const float4*>(sfac + col0);
-        const float4 s1 = *reinterpret_cast<const float4*>(sfac + col0 + 4);
-        f[0] = s0.x * rb; f[1] = s0.y * rb; f[2] = s0.z * rb; f[3] = s0.w * rb;
-        f[4] = s1.x * rb; f[5] = s1.y * rb; f[6] = s1.z * rb; f[7] = s1.w * rb;
-      } else {
-        const float* gd = gdiag + t * kLdGd + (col0 & 15);
-        const float4 s0 = *reinterpret_cast<const float4*>(gd);
-        const float4 s1 = *reinterpret_cast<const float4*>(gd + 4);
-        f[0] = s0.x * bt; f[1] = s0.y * bt; f[2] = s0.z * bt; f[3] = s0.w * bt;
-        f[4] = s1.x * bt; f[5] = s1.y * bt; f[6] = s1.z * bt; f[7] = s1.w * bt;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = (col0 + e <= t) ? f[e] : 0.f;
+  // Step 4, merges of the diagonal blocks of T_L (in X5).
+  {
+    uint8_t* x5 = sm + kOffX5;
+    const uint32_t x5a = sbase + kOffX5, zsa = sbase + kOffZs;
+    uint8_t* zs = sm + kOffZs;
+    if constexpr (C >= 32) {
+      // 16 -> 32: T_R0 = -T_RR (L_R0 T_00) for the block pairs p = 0, 1 (R = 2p+1,
+      // 0 = 2p); warp w < 4 takes pair w / 2, output columns 8 (w % 2) ...
+      const int p = (warp >> 1) & 1, nh = warp & 1, R = 16 * (2 * p + 1), c0 = 32 * p;
+      if (warp < 4) {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t a[4], bb[2];
+        ldsm_x4(a_frag_addr(sbase + kOffXl1, kLd1, 16 * p, 0, lane), a);
+        ldsm_x2_trans(b_frag_addr_sw(x5a, c0, c0 + 8 * nh, lane), bb);
+        mma_bf16_16816(d, a, bb);
+        st_frag(zs, kLd1, 16 * p, 8 * nh, d, lane);
       }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] *= f[e];
-      st_sm16(sm, kOffB + sw128(64 + t, col0), pack8(v));
+      gsync();
+      if (warp < 4) {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t a[4], bb[2];
+        ldsm_x4(a_frag_addr_sw(x5a, R, R, lane), a);
+        ldsm_x2_trans(b_frag_addr(zsa, kLd1, 16 * p, 8 * nh, lane), bb);
+        mma_bf16_16816(d, a, bb);
+        st_frag_sw(x5, R, c0 + 8 * nh, d, -1.f, lane);
+      }
+      gsync();
     }
+    if constexpr (C == 64) {
+      // 32 -> 64: T_BA = -T_BB (L_BA T_AA), A = [0, 32), B = [32, 64); warp w
+      // takes the 16 x 8 output tile (w / 4, w % 4) of each product.
+      const int mt = warp >> 2, nt = warp & 3;
+      {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t a[4], bb[2];
+#pragma unroll
+        for (int k0 = 0; k0 < 32; k0 += 16) {
+          ldsm_x4(a_frag_addr(sbase + kOffXl2, kLd2, 16 * mt, k0, lane), a);
+          ldsm_x2_trans(b_frag_addr_sw(x5a, k0, 8 * nt, lane), bb);
+          mma_bf16_16816(d, a, bb);
+        }
+        st_frag(zs, kLd2, 16 * mt, 8 * nt, d, lane);
+      }
+      gsync();
+      {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t a[4], bb[2];
+#pragma unroll
+        for (int k0 = 0; k0 < 32; k0 += 16) {
+          ldsm_x4(a_frag_addr_sw(x5a, 32 + 16 * mt, 32 + k0, lane), a);
+          ldsm_x2_trans(b_frag_addr(zsa, kLd2, k0, 8 * nt, lane), bb);
+          mma_bf16_16816(d, a, bb);
+        }
+        st_frag_sw(x5, 32 + 16 * mt, 8 * nt, d, -1.f, lane);
+      }
+      gsync();
+    }
+  }
+
+  // Coefficients, row t, columns 16 cg .. 16 cg + 15 (four threads a row):
+  //   T_A = beta_t Gam[t][j] T_L[t][j]      -> X3
+  //   cP  = G_C beta_t T_L[t][j]            -> X0
+  //   cU  = Gam[C-1][t] T_A[t][j]           -> X4
+  // T_L is zero above the diagonal and across chunks, and so is Gam here.
+  if (ok) {
+    const int t = tid >> 2, c0 = 16 * (tid & 3), cs = (t / C) * C;
+    const float bt = bta[t], lt = lam[t], gcp = gc[t / C] * bt, gs = gsuf[t];
+    float tl[16], ta[16], cp[16], cu[16];
+    unpack8(*reinterpret_cast<const uint4*>(sm + kOffX5 + sw128(t, c0)), tl);
+    unpack8(*reinterpret_cast<const uint4*>(sm + kOffX5 + sw128(t, c0 + 8)), tl + 8);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int j = c0 + e;
+      const float gm = (j <= t && j >= cs) ? ex2(lt - lam[j]) : 0.f;
+      ta[e] = bt * gm * tl[e];
+      cp[e] = gcp * tl[e];
+      cu[e] = gs * ta[e];
+    }
+    st_sm16(sm, kOffX3 + sw128(t, c0), pack8(ta));
+    st_sm16(sm, kOffX3 + sw128(t, c0 + 8), pack8(ta + 8));
+    st_sm16(sm, kOffX0 + sw128(t, c0), pack8(cp));
+    st_sm16(sm, kOffX0 + sw128(t, c0 + 8), pack8(cp + 8));
+    st_sm16(sm, kOffX4 + sw128(t, c0), pack8(cu));
+    st_sm16(sm, kOffX4 + sw128(t, c0 + 8), pack8(cu + 8));
     fence_proxy_async();
   }
   ok = gsync_and(ok);
 
-  // From G2 on the tile runs as two streams that meet again before the last
-  // stores: the P stream (warps 0, 1, 4, 5: TMEM lanes 0..63; P, Pt, G M P, Qh;
-  // io 0 and 1) and the U stream (warps 2, 3, 6, 7: lanes 64..127; U, Ut,
-  // y_loc; io 2 and 3), each with its own barrier and MMA completion barrier.
-  // G2 (thread 0): D2b = A2 V (cols 128..255; rows 64..127 = U = T_A (beta V))
-  // first, committed to bar_u, then D2a = A2 K (cols 0..127; rows 0..63 =
-  // P = T_L K), committed to bar_p.
+  // GW (thread 0): D[128 x 128] = A3 [T_A | T_L]: rows 0-63 x cols 64-127 are
+  // W_M = diag(G) M T_L, rows 64-127 x cols 0-63 are W_Y = (Gam . QK^T) T_A.
   if (ok && tid == 0) {
     tc_fence_after();
-    const uint32_t id2 = idesc_bf16(128, 128, false, true);
+    const uint32_t idw = idesc_bf16(128, 128, false, true);
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const uint64_t ad = smem_desc(sbase + kOffB + kk * 32, 16, 1024, kSw128);
-      mma_bf16_ss(tmem + 128, ad, smem_desc(sbase + kOffV + kk * 2048, 8192, 1024, kSw128), id2,
-                  kk > 0);
-    }
-    mma_commit(bar_u);
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const uint64_t ad = smem_desc(sbase + kOffB + kk * 32, 16, 1024, kSw128);
-      mma_bf16_ss(tmem, ad, smem_desc(sbase + kOffKQ + kk * 2048, 16384, 1024, kSw128), id2,
-                  kk > 0);
-    }
-    mma_commit(bar_p);
+    for (int kk = 0; kk < 4; ++kk)
+      mma_bf16_ss(tmem, smem_desc(sbase + kOffX1 + kk * 32, 16, 1024, kSw128),
+                  smem_desc(sbase + kOffX3 + kk * 2048, 16384, 1024, kSw128), idw, kk > 0);
+    mma_commit(bar_gw);
   }
-  const uint32_t bar_s = pstream ? bar_p : bar_u;
-  const int stream_id = pstream ? pstream_id : ustream_id;
-  ok = ok && mbar_wait(bar_s, 0);
+  ok = ok && mbar_wait(bar_gw, it & 1);
   tc_fence_after();
-
-  // Epilogue thread: row t of its stream (TMEM lane (warp % 4) * 32 + lane),
-  // columns cbeg .. cbeg+63 (warps w and w+4 share a lane quadrant).
-  auto epi_t = [&]() { return ((warp & 3) * 32 + (tid & 31)) & 63; };
-  auto epi_src = [&]() {
-    return tmem + ((uint32_t)((warp & 3) * 32) << 16) + (pstream ? 0 : 128);
-  };
   if (ok) {
-    const int t = epi_t(), cbeg = (warp >> 2) * 64;
-    const uint32_t src = epi_src();
-    // P rows (lanes 0..63) and U rows (lanes 64..127): bf16 into the G3 operand
-    // B3 = [P; U] and, scaled, into the workspace: Pt = G_C beta P (step 9),
-    // Ut = Gam[C-1][.] U.  Staging: Pt over K, Ut over V (each stream's G2 has
-    // read them), as 128B-swizzled 64-column halves stored below with TMA.
-    const uint32_t bdst = kOffB + (pstream ? 0 : 16384);
-    const float scale = pstream ? gc[t / C] * bta[t] : gsuf[t];
-    const uint32_t stage = pstream ? kOffKQ : kOffV;
-    const uint32_t half_stride = pstream ? 16384 : 8192;
+    // -W_M over A3 top (X1), W_Y / sqrt(Dk) over T_L (X5): both operands of GW,
+    // which has completed.  32 columns per thread.
+    const int t = trow, c0 = (warp >> 2) * 32;
+    float v[32];
+    const bool top = lrow < 64;
+    tmem_ld16(tmem + lane_base + (top ? 64 : 0) + c0, v);
+    tmem_ld16(tmem + lane_base + (top ? 64 : 0) + c0 + 16, v + 16);
+    tmem_wait_ld();
+    const float s = top ? -1.f : P.yscale;
 #pragma unroll
-    for (int c2 = cbeg; c2 < cbeg + 64; c2 += 32) {
-      float vv[2][16];  // two 16-column blocks per TMEM round trip
-      tmem_ld16(src + c2, vv[0]);
-      tmem_ld16(src + c2 + 16, vv[1]);
+    for (int e = 0; e < 32; ++e) v[e] *= s;
+    const uint32_t dst = top ? kOffX1 : kOffX5;
+#pragma unroll
+    for (int e = 0; e < 32; e += 8) st_sm16(sm, dst + sw128(t, c0 + e), pack8(v + e));
+    fence_proxy_async();
+  }
+  tc_fence_before();
+  ok = gsync_and(ok);
+
+  // F1 = [cP; -W_M] K (TMEM columns 0..127), F2 = [cU; W_Y / sqrt(Dk)] V
+  // (columns 128..255), issued by thread 0; F1 commits to bar_f1 (stream A),
+  // F2 to bar_f2 (stream B: it also covers F1, issued before it).
+  if (ok && tid == 0) {
+    ok = mbar_wait(bar_v, it & 1);  // V of this tile has landed
+    fence_proxy_async();
+  }
+  if (ok && tid == 0) {
+    tc_fence_after();
+    const uint32_t idf = idesc_bf16(128, 128, false, true);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_bf16_ss(tmem, smem_desc(sbase + kOffX0 + kk * 32, 16, 1024, kSw128),
+                  smem_desc(sbase + kOffKQ + kk * 2048, 16384, 1024, kSw128), idf, kk > 0);
+    mma_commit(bar_f1);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_bf16_ss(tmem + 128, smem_desc(sbase + kOffX4 + kk * 32, 16, 1024, kSw128),
+                  smem_desc(sbase + kOffV + kk * 2048, 8192, 1024, kSw128), idf, kk > 0);
+    mma_commit(bar_f2);
+  }
+  // A failed V wait on thread 0 leaves F1 / F2 unissued: the others' waits on
+  // them then time out as well (bounded), and ok turns false everywhere.
+  ok = ok && mbar_wait(streamA ? bar_f1 : bar_f2, it & 1);
+  tc_fence_after();
+  if (ok) {
+    // Epilogue, 128 columns of row t per thread, staged as [row][half]
+    // (128-byte units, 128B-swizzled) for one TMA store per output:
+    //   warps 0, 1: Pt (F1, lanes 0-63)        -> A1 staging (X0..X3), row a(t)
+    //   warps 2, 3: Qh = G_t q_t + F1 (64-127) -> A1 staging, row a(t) + C
+    //   warps 4, 5: Ut (F2, lanes 0-63)        -> V, row t
+    //   warps 6, 7: y_loc / sqrt(Dk) (F2)      -> X4, X5, row t
+    // with a(t) = 2C (t / C) + t mod C, the row of Pt_t in the tile's A1 rows.
+    const int t = trow;
+    const uint32_t src = tmem + lane_base + (streamA ? 0 : 128);
+    const bool top = lrow < 64;
+    const float gt = gpw[t];
+    const int srow = streamA ? 2 * C * (t / C) + (t % C) + (top ? 0 : C) : t;
+    const uint32_t sbuf = streamA ? kOffX0 : (top ? kOffV : kOffX4);
+#pragma unroll
+    for (int c2 = 0; c2 < 128; c2 += 32) {
+      float v[32];
+      tmem_ld16(src + c2, v);
+      tmem_ld16(src + c2 + 16, v + 16);
       tmem_wait_ld();
+      const int h = c2 >> 6, cc = c2 & 63;
+      if (streamA && !top) {
+        const uint32_t qsrc = kOffKQ + h * 16384 + 8192;
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int col = c2 + 16 * hh;
-        float* v = vv[hh];
-        const uint32_t atom = bdst + (col >> 6) * 8192;
-        st_sm16(sm, atom + sw128(t, col & 63), pack8(v));
-        st_sm16(sm, atom + sw128(t, (col & 63) + 8), pack8(v + 8));
+        for (int e = 0; e < 32; e += 8) {
+          float q8[8];
+          unpack8(*reinterpret_cast<const uint4*>(sm + qsrc + sw128(t, cc + e)), q8);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] *= scale;
-        const uint32_t hs = stage + (col >> 6) * half_stride;
-        st_sm16(sm, hs + sw128(t, col & 63), pack8(v));
-        st_sm16(sm, hs + sw128(t, (col & 63) + 8), pack8(v + 8));
+          for (int i = 0; i < 8; ++i) v[e + i] = fmaf(gt, q8[i], v[e + i]);
+        }
       }
+#pragma unroll
+      for (int e = 0; e < 32; e += 8)
+        st_sm16(sm, sbuf + sw128(2 * srow + h, cc + e), pack8(v + e));
     }
     fence_proxy_async();
   }
-  tc_fence_before();  // this stream's TMEM reads precede its G3
-  named_bar_sync(stream_id, 128);
-  if (ok && io >= 0) {
-    const int row0 = (int)(tile_id * 128);
-    if (io < 2) {
-#pragma unroll
-      for (int c = 0; c < 64 / C; ++c)  // Pt rows of chunk c, half io
-        tma_store_2d(P.tm_a1s, sbase + kOffKQ + io * 16384 + c * C * 128, 64 * io,
-                     row0 + 2 * C * c);
-    } else {
-      tma_store_2d(P.tm_us, sbase + kOffV + (io - 2) * 8192, 64 * (io - 2),
-                   (int)(tile_id * kTile));  // Ut rows
-    }
-    bulk_commit();
-  }
-  // G3 per stream: D3a = A3 P (thread 0; cols 0..127, rows 0..63 = G M P) and
-  // D3b = A3 U (thread 64; cols 128..255, rows 64..127 = y_loc).
-  if (ok && (tid == 0 || tid == 64)) {
-    tc_fence_after();
-    const uint32_t id3 = idesc_bf16(128, 128, false, true);
-    const uint32_t boff = pstream ? 0 : 16384;
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const uint64_t ad = smem_desc(sbase + kOffA3 + kk * 32, 16, 1024, kSw128);
-      mma_bf16_ss(tmem + (pstream ? 0 : 128), ad,
-                  smem_desc(sbase + kOffB + boff + kk * 2048, 8192, 1024, kSw128), id3, kk > 0);
-    }
-    mma_commit(bar_s);
-  }
-  ok = ok && mbar_wait(bar_s, 1);
-  tc_fence_after();
-
-  if (ok) {
-    // Staging over this stream's half of B3 (read only by its own G3): Qh by
-    // the P stream, y_loc / sqrt(Dk) by the U stream.
-    const int t = epi_t(), cbeg = (warp >> 2) * 64;
-    const uint32_t src = epi_src();
-    const uint32_t stage = kOffB + (pstream ? 0 : 16384);
-    const float gt = gpw[t];
-#pragma unroll
-    for (int c2 = cbeg; c2 < cbeg + 64; c2 += 32) {
-      float vv[2][16];  // two 16-column blocks per TMEM round trip
-      tmem_ld16(src + c2, vv[0]);
-      tmem_ld16(src + c2 + 16, vv[1]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int col = c2 + 16 * hh;
-        float* v = vv[hh];
-        if (pstream) {  // Qh = G q - G M P  (step 7, state-free part)
-          const uint8_t* qa = sm + kOffKQ + (col >> 6) * 16384 + 8192;
-          float q[16];
-          unpack8(*reinterpret_cast<const uint4*>(qa + sw128(t, col & 63)), q);
-          unpack8(*reinterpret_cast<const uint4*>(qa + sw128(t, (col & 63) + 8)), q + 8);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = gt * q[j] - v[j];
-        } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] *= P.yscale;
-        }
-        const uint32_t hs = stage + (col >> 6) * 8192;
-        st_sm16(sm, hs + sw128(t, col & 63), pack8(v));
-        st_sm16(sm, hs + sw128(t, (col & 63) + 8), pack8(v + 8));
-      }
-    }
-  }
   if (ok && tid < 64 / C) wsGC[tile_id * 4 + tid] = gc[tid];
-  if (ok) fence_proxy_async();
-  ok = gsync_and(ok);
-  if (ok && io >= 0) {
-    const int row0 = (int)(tile_id * 128);
-    if (io < 2) {
-#pragma unroll
-      for (int c = 0; c < 64 / C; ++c)  // Qh rows of chunk c, half io
-        tma_store_2d(P.tm_a1s, sbase + kOffB + io * 8192 + c * C * 128, 64 * io,
-                     row0 + 2 * C * c + C);
-    } else {  // y_loc / sqrt(Dk) into y (rows past T are clipped)
-      const int h = io - 2, bh = head_of(lin), b = bh / Hv;
-      tma_store_4d(P.tm_y, sbase + kOffB + 16384 + h * 8192, 64 * h, bh - b * Hv,
-                   tile_of(lin) * kTile, b);
+  tc_fence_before();  // the next tile's G1 rewrites these TMEM columns
+  named_bar_sync(streamA ? streamA_id : streamB_id, 128);
+  if (ok) {
+    if (io == 0) {  // A1 rows of the tile (Pt and Qh of each chunk)
+      tma_store_3d(P.tm_a1o, sbase + kOffX0, 0, 0, (int)(tile_id * 128));
+      bulk_commit();
+    } else if (io == 1) {
+      const int bh = head_of(lin), b = bh / Hv;
+      tma_store_5d(P.tm_yo, sbase + kOffX4, 0, 0, bh - b * Hv, tile_of(lin) * kTile,
+                   b);  // y_loc / sqrt(Dk) (rows past T are clipped)
+      tma_store_3d(P.tm_uo, sbase + kOffV, 0, 0, (int)(tile_id * kTile));  // Ut
+      bulk_commit();
     }
-    bulk_commit();
+    unpublished = tile_id;
+    // K (read by F1) and Q (read by the Qh epilogue) are free: the next tile's
+    // come in while this tile's stores drain.
+    if (streamA && next < total) load_kq(next);
   }
-  if (io >= 0) {
-    // The next tile's K, Q and V are loaded once this thread's stores of Pt
-    // or Ut (staged in K and V) have read them; Q was last read by the
-    // epilogue above.  The Qh / y_loc staging is waited for before the next G1.
-    bulk_wait_read<1>();
-    if (ok && next < total) {
-      load_kv(next);
-      load_q(next);
-      tma_pending = true;
-    }
-    if (ok && flags) unpublished = tile_id;
-  }
-  // No group barrier here: ok is uniform since the last one, and the next
-  // tile's gate tables are free (their last reader was the epilogue above), so
-  // the gate warps start on the next tile while the I/O threads issue its loads.
   }  // tile loop
 
-  if (io >= 0) {
-    if (ok) publish();
-    bulk_wait_read_all();  // shared memory must outlive the last stores' reads
-  }
-  // A group that stopped early lets its last prefetch land before the CTA exits.
-  if (io == 0 && tma_pending) mbar_wait(bar_tma, it & 1);
+  gsync();
+  if (ok && io >= 0) publish();  // the group's last tile
+  if (io >= 0) bulk_wait_all();   // shared memory must outlive the stores' reads
+  cp_async_wait_all();            // and every copy into it must have landed
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x < 32) tmem_dealloc(tmem_base_sh, 256 * kPrepGroups);
@@ -818,15 +820,14 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
 
 template <int C>
 __global__ void __launch_bounds__(kPrepThreads, 1)
-prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
-               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_a1s,
-               const __grid_constant__ CUtensorMap tm_us, const __grid_constant__ CUtensorMap tm_y,
-               const bf16* kin, const bf16* qin, const bf16* vin, const bf16* __restrict__ g,
-               const bf16* __restrict__ beta, float* __restrict__ wsGC, int T, int Hk, int Hv,
-               int NT, int BH, int opts, float scale) {
+prep_tc_kernel(const __grid_constant__ CUtensorMap tm_a1o, const __grid_constant__ CUtensorMap tm_uo,
+               const __grid_constant__ CUtensorMap tm_yo, const bf16* kin, const bf16* qin,
+               const bf16* vin, const bf16* __restrict__ g, const bf16* __restrict__ beta,
+               float* __restrict__ wsGC, int T, int Hk, int Hv, int NT, int BH, int opts,
+               float scale) {
   extern __shared__ uint8_t smem_raw[];
-  const PrepParams P{kin, qin, vin, &tm_k, &tm_q, &tm_v, &tm_a1s, &tm_us, g, beta, wsGC,
-                     T, Hk, Hv, NT, BH, opts, &tm_y, scale};
+  const PrepParams P{kin, qin, vin, &tm_a1o, &tm_uo, &tm_yo, g, beta, wsGC,
+                     T, Hk, Hv, NT, BH, opts, scale};
   prep_role<C>(P, smem_raw, blockIdx.x, gridDim.x, nullptr);
 }
 
@@ -976,7 +977,7 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
       if (n >= stages && !mbar_wait(bar(empty0 + s), ((n / stages) - 1) & 1)) break;
       const size_t tid_ws = (size_t)bh * NT + n;
       if (flags) {
-        if (!wait_flag(flags + tid_ws, kPrepIo)) break;
+        if (!wait_flag(flags + tid_ws, kTilePublished)) break;
         fence_proxy_async_global();
       }
       const uint32_t fb = bar(full0 + s);
@@ -1239,8 +1240,10 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_a1s,
                      const __grid_constant__ CUtensorMap tm_us,
-                     const __grid_constant__ CUtensorMap tm_y,
-                     const __grid_constant__ CUtensorMap tm_yred, const bf16* kin,
+                     const __grid_constant__ CUtensorMap tm_yred,
+                     const __grid_constant__ CUtensorMap tm_a1o,
+                     const __grid_constant__ CUtensorMap tm_uo,
+                     const __grid_constant__ CUtensorMap tm_yo, const bf16* kin,
                      const bf16* qin, const bf16* vin, const bf16* __restrict__ g,
                      const bf16* __restrict__ beta, float* __restrict__ wsGC, int* flags,
                      const float* state_in, float* state_out, int T, int Hk, int Hv, int NT,
@@ -1250,8 +1253,8 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_k,
     scan_role128<C>(&tm_a1s, &tm_k, &tm_us, &tm_yred, wsGC, flags, state_in, state_out, T, Hk,
                     Hv, NT, blockIdx.x, opts, scale, smem_raw);
   } else {
-    const PrepParams P{kin, qin, vin, &tm_k, &tm_q, &tm_v, &tm_a1s, &tm_us, g, beta, wsGC,
-                       T, Hk, Hv, NT, BH, opts, &tm_y, scale};
+    const PrepParams P{kin, qin, vin, &tm_a1o, &tm_uo, &tm_yo, g, beta, wsGC,
+                       T, Hk, Hv, NT, BH, opts, scale};
     prep_role<C>(P, smem_raw, blockIdx.x - BH, gridDim.x - BH, flags);
   }
 }
@@ -1322,6 +1325,31 @@ bool make_rows_map(CUtensorMap* m, const void* base, size_t rows, int box_cols, 
 }
 
 
+// Rows of 128 bf16 values seen as [rows][2 halves][64] (3-D), box {64, 2,
+// box_rows}: the box lands in shared memory as [row][half] 128-byte units.
+bool make_rows_halves_map(CUtensorMap* m, const void* base, size_t rows, int box_rows) {
+  const cuuint64_t dims[3] = {64, 2, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {128, (cuuint64_t)kD * 2};
+  const cuuint32_t box[3] = {64, 2, (cuuint32_t)box_rows};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// [B, T, H, 128] bf16 seen as [B][T][H][2][64] (5-D), box {64, 2, 1, 64, 1}.
+bool make_bthd_halves_map(CUtensorMap* m, const void* base, int B, int T, int H) {
+  const cuuint64_t dims[5] = {64, 2, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+  const cuuint64_t strides[4] = {128, (cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2,
+                                 (cuuint64_t)T * H * kD * 2};
+  const cuuint32_t box[5] = {64, 2, 1, (cuuint32_t)kTile, 1};
+  const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims,
+                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms() {
   static int cache[64] = {};
@@ -1346,12 +1374,15 @@ cudaError_t launch_c(const PrefillArgs& a) {
   float* wsGC = reinterpret_cast<float*>(ws + w.gc);
 
   if (!encode_fn()) return cudaErrorNotSupported;
-  CUtensorMap tk, tq, tv, ta1s, tus, ty, tyred;
+  CUtensorMap tk, tq, tv, ta1s, tus, tyred, ta1o, tuo, tyo;
   if (!make_bthd_map(&tk, a.k, a.B, a.T, a.Hk) || !make_bthd_map(&tq, a.q, a.B, a.T, a.Hk) ||
       !make_bthd_map(&tv, a.v, a.B, a.T, a.Hv) ||
       !make_rows_map(&ta1s, wsA1, (size_t)BH * NT * 128, 64, C, true) ||
       !make_rows_map(&tus, wsU, (size_t)BH * NT * kTile, 64, 64, true) ||
-      !make_bthd_map(&ty, a.y, a.B, a.T, a.Hv) || !make_bthd_map(&tyred, a.y, a.B, a.T, a.Hv, C))
+      !make_bthd_map(&tyred, a.y, a.B, a.T, a.Hv, C) ||
+      !make_rows_halves_map(&ta1o, wsA1, (size_t)BH * NT * 128, 128) ||
+      !make_rows_halves_map(&tuo, wsU, (size_t)BH * NT * kTile, kTile) ||
+      !make_bthd_halves_map(&tyo, a.y, a.B, a.T, a.Hv))
     return cudaErrorInvalidValue;
 
   const float scale = 1.0f / sqrtf((float)kD);
@@ -1380,9 +1411,9 @@ cudaError_t launch_c(const PrefillArgs& a) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fused_prefill_kernel<C>, tk, tq, tv, ta1s, tus, ty, tyred, k,
-                              q, v, g, beta, wsGC, flags, a.state_in, a.state_out, a.T, a.Hk,
-                              a.Hv, NT, BH, a.options, scale);
+    return cudaLaunchKernelEx(&cfg, fused_prefill_kernel<C>, tk, tq, tv, ta1s, tus, tyred, ta1o,
+                              tuo, tyo, k, q, v, g, beta, wsGC, flags, a.state_in, a.state_out,
+                              a.T, a.Hk, a.Hv, NT, BH, a.options, scale);
   }
 
   // Split path: the persistent prep kernel on every SM, then one scan CTA per head.
@@ -1394,8 +1425,7 @@ cudaError_t launch_c(const PrefillArgs& a) {
   if (e != cudaSuccess) return e;
   const int prep_ctas = std::min(sms, (BH * NT + kPrepGroups - 1) / kPrepGroups);
   prep_tc_kernel<C><<<prep_ctas, kPrepThreads, kPrepSmem, a.stream>>>(
-      tk, tq, tv, ta1s, tus, ty, k, q, v, g, beta, wsGC, a.T, a.Hk, a.Hv, NT, BH, a.options,
-      scale);
+      ta1o, tuo, tyo, k, q, v, g, beta, wsGC, a.T, a.Hk, a.Hv, NT, BH, a.options, scale);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   scan_head_kernel<C><<<BH, kFusedThreads, Scan128Smem::kTotal, a.stream>>>(
