@@ -201,12 +201,12 @@ def roofline(alg_bytes, seconds, hbm_gbs, kind, traffic=None):
 
 def prefill_launches(w, dev):
     """Kernels one gdn_prefill call launches: T <= 32 one (the sequential
-    short-T kernel); bf16 with 128-wide heads runs prep and scan as one
-    cooperative kernel when B*Hv is at most a third of the SMs, else as two;
-    the fp32 chunked path always two."""
+    short-T kernel); bf16 or fp16 with 128-wide heads runs prep and scan as
+    one cooperative kernel when B*Hv is at most a third of the SMs, else as
+    two; the fp32 chunked path always two."""
     if w.T <= 32:
         return 1
-    if w.torch_dtype != torch.bfloat16 or w.Dk != 128 or w.Dv != 128:
+    if w.dtype == "f32" or w.Dk != 128 or w.Dv != 128:
         return 2
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     return 1 if 3 * w.B * w.Hv <= sms else 2
@@ -470,7 +470,8 @@ def run_reference(args, w):
 METRIC = "GDN prefill tokens/s (B=1 T=4096 Hk=16 Hv=32 D=128 bf16 C=64) and decode steps/s"
 
 # The other prefill workloads of the plan, timed after the headline one.
-EXTRA_PREFILL = ["fp32_t64", "prefill_b4_t2048", "prefill_t65536", "prefill_b64_t16"]
+EXTRA_PREFILL = ["fp32_t64", "prefill_b4_t2048", "prefill_t65536", "prefill_b64_t16",
+                 "prefill_t4096_f16"]
 
 
 def prefill_entry(gdn, w, dev, steps, warmup, hbm, peak_kind, world):

@@ -41,9 +41,11 @@ int check_pointers(const void* const* ptrs, int n) {
     if (!aligned16(ptrs[i])) return GDN_ERR_ALIGNMENT;
   return GDN_OK;
 }
-// The tensor-core prefill serves bf16 inputs with the head size it is built for.
+// The tensor-core prefill serves 16-bit inputs (bf16, fp16) with the head size
+// it is built for.
 bool use_tc(int Dk, int Dv, int dtype) {
-  return dtype == GDN_DTYPE_BF16 && Dk == gdn::kHeadDim && Dv == gdn::kHeadDim;
+  return (dtype == GDN_DTYPE_BF16 || dtype == GDN_DTYPE_F16) && Dk == gdn::kHeadDim &&
+         Dv == gdn::kHeadDim;
 }
 }  // namespace
 

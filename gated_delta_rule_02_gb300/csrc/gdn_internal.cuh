@@ -84,7 +84,7 @@ struct DecodeArgs {
 size_t prefill_simt_workspace_bytes(int B, int T, int Hv, int chunk, int Dk, int Dv);
 cudaError_t launch_prefill_simt(const PrefillArgs& a);
 
-// tcgen05 chunked path (bf16 inputs): prep + scan launches.
+// tcgen05 chunked path (bf16 or fp16 inputs): prep + scan launches.
 size_t prefill_tc_workspace_bytes(int B, int T, int Hv);
 cudaError_t launch_prefill_tc(const PrefillArgs& a);
 // Reads (and optionally clears) the tensor-core kernels' device error word;

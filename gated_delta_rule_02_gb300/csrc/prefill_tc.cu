@@ -1,4 +1,4 @@
-// Chunked prefill on the tcgen05 tensor cores (bf16 inputs, fp32 state).
+// Chunked prefill on the tcgen05 tensor cores (bf16 or fp16 inputs, fp32 state).
 //
 // The method is the chunked Woodbury-Young form of metaltile-std
 // `gated_delta_wy.rs` (module docs, "Algorithm", steps 1-9), with the decay
@@ -41,6 +41,47 @@ namespace {
 using namespace ptx;
 using bf16 = __nv_bfloat16;
 
+// The 16-bit input types the tensor cores take here (kind::f16: A and B of one
+// product always share a type, so every operand the kernels build is stored
+// in the input type): bf16 and fp16.
+template <typename E>
+struct ElemT;
+template <>
+struct ElemT<__nv_bfloat16> {
+  static constexpr uint32_t kFmt = 1;        // tcgen05 kind::f16 A/B format field
+  static constexpr uint16_t kOne = 0x3f80;   // 1.0
+  static constexpr CUtensorMapDataType kTmap = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  __device__ static uint32_t pack2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ static float2 unpack2(uint32_t w) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+  }
+  __device__ static float bits(uint16_t x) { return __uint_as_float((uint32_t)x << 16); }
+  __device__ static __nv_bfloat16 from(float x) { return __float2bfloat16_rn(x); }
+};
+template <>
+struct ElemT<__half> {
+  static constexpr uint32_t kFmt = 0;
+  static constexpr uint16_t kOne = 0x3c00;
+  static constexpr CUtensorMapDataType kTmap = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  __device__ static uint32_t pack2(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ static float2 unpack2(uint32_t w) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&w));
+  }
+  __device__ static float bits(uint16_t x) { return __half2float(__ushort_as_half(x)); }
+  __device__ static __half from(float x) { return __float2half_rn(x); }
+};
+// Instruction descriptor of a kind::f16 product with A and B of type E.
+template <typename E>
+__host__ __device__ constexpr uint32_t idesc_e(int M, int N, bool a_mn, bool b_mn) {
+  return idesc_kind_f16(M, N, a_mn, b_mn, ElemT<E>::kFmt);
+}
+
 constexpr int kTile = 64;   // tokens per tile
 constexpr int kD = kHeadDim;
 
@@ -53,8 +94,8 @@ inline WsLayout ws_layout(int BH, int NT) {
   WsLayout w;
   const size_t tiles = (size_t)BH * NT;
   w.a1 = 0;
-  w.u = align256(tiles * 128 * kD * sizeof(bf16));
-  w.gc = w.u + align256(tiles * kTile * kD * sizeof(bf16));
+  w.u = align256(tiles * 128 * kD * 2);  // 16-bit elements
+  w.gc = w.u + align256(tiles * kTile * kD * 2);
   w.flags = w.gc + align256(tiles * 4 * sizeof(float));
   w.total = w.flags + align256(tiles * sizeof(int));
   return w;
@@ -66,9 +107,9 @@ inline WsLayout ws_layout(int BH, int NT) {
 __device__ __forceinline__ uint32_t sw128(int row, int col) {
   return row * 128 + ((((col >> 3) ^ (row & 7))) << 4) + (col & 7) * 2;
 }
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&h);
+template <typename E>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  return ElemT<E>::pack2(a, b);
 }
 // 16-byte store through a generic pointer into shared memory: unlike the asm
 // form it lets the compiler schedule the surrounding shared loads freely.
@@ -80,24 +121,26 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
   return v;
 }
+template <typename E>
 __device__ __forceinline__ void unpack8(uint4 v, float* f) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
-    float2 p = __bfloat1622float2(h);
+    const float2 p = ElemT<E>::unpack2(w[i]);
     f[2 * i] = p.x;
     f[2 * i + 1] = p.y;
   }
 }
+template <typename E>
 __device__ __forceinline__ uint4 pack8(const float* f) {
-  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                    pack_bf16x2(f[6], f[7]));
+  return make_uint4(pack2<E>(f[0], f[1]), pack2<E>(f[2], f[3]), pack2<E>(f[4], f[5]),
+                    pack2<E>(f[6], f[7]));
 }
 
-// x / |x| for row `row` of a bf16 tile whose rows are split in two 128B-swizzled
-// 64-column halves `half_stride` bytes apart; the calling thread takes half
-// `half` and its lane partner (lane ^ 1) the other half.
+// x / |x| for row `row` of a 16-bit tile whose rows are split in two
+// 128B-swizzled 64-column halves `half_stride` bytes apart; the calling thread
+// takes half `half` and its lane partner (lane ^ 1) the other half.
+template <typename E>
 __device__ __forceinline__ void l2norm_row_sw128(uint8_t* base, int half_stride, int row,
                                                  int half) {
   uint8_t* hb = base + half * half_stride;
@@ -105,7 +148,7 @@ __device__ __forceinline__ void l2norm_row_sw128(uint8_t* base, int half_stride,
 #pragma unroll
   for (int ch = 0; ch < 8; ++ch) {
     float v[8];
-    unpack8(*reinterpret_cast<const uint4*>(hb + sw128(row, 8 * ch)), v);
+    unpack8<E>(*reinterpret_cast<const uint4*>(hb + sw128(row, 8 * ch)), v);
 #pragma unroll
     for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
   }
@@ -115,10 +158,10 @@ __device__ __forceinline__ void l2norm_row_sw128(uint8_t* base, int half_stride,
   for (int ch = 0; ch < 8; ++ch) {
     uint4* p = reinterpret_cast<uint4*>(hb + sw128(row, 8 * ch));
     float v[8];
-    unpack8(*p, v);
+    unpack8<E>(*p, v);
 #pragma unroll
     for (int e = 0; e < 8; ++e) v[e] *= f;
-    *p = pack8(v);
+    *p = pack8<E>(v);
   }
 }
 
@@ -187,7 +230,7 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
-// Warp-level m16n8k16 bf16 MMA (fp32 accumulate) with ldmatrix operand loads:
+// Warp-level m16n8k16 MMA (16-bit inputs, fp32 accumulate) with ldmatrix operand loads:
 // the inverse's block products are too small for tcgen05 (M >= 64).
 // Fragments (g = lane / 4, c = lane % 4): A 16 x 16 row-major in four 8 x 8
 // matrices (rows 0-7 / 8-15 x cols 0-7 / 8-15), B 16 x 8 with b0 = rows 2c,
@@ -203,16 +246,25 @@ __device__ __forceinline__ void ldsm_x2_trans(uint32_t addr, uint32_t* r) {
                : "=r"(r[0]), "=r"(r[1])
                : "r"(addr));
 }
-__device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, const uint32_t* b) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+template <typename E>
+__device__ __forceinline__ void mma_16816(float* d, const uint32_t* a, const uint32_t* b) {
+  if constexpr (ElemT<E>::kFmt == 1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+  }
 }
 // Lane address of an ldmatrix.x4 A fragment (rows r0.., cols c0..) and of an
 // ldmatrix.x2.trans B fragment (rows k0.. of a row-major [k][n] block, cols
-// n0..): in a plain row-major bf16 array of `ld` elements per row ...
+// n0..): in a plain row-major 16-bit array of `ld` elements per row ...
 __device__ __forceinline__ uint32_t a_frag_addr(uint32_t base, int ld, int r0, int c0, int lane) {
   return base + ((r0 + (lane & 7) + 8 * ((lane >> 3) & 1)) * ld + c0 + 8 * (lane >> 4)) * 2;
 }
@@ -227,32 +279,35 @@ __device__ __forceinline__ uint32_t a_frag_addr_sw(uint32_t base, int r0, int c0
 __device__ __forceinline__ uint32_t b_frag_addr_sw(uint32_t base, int k0, int n0, int lane) {
   return base + sw128(k0 + (lane & 15), n0);
 }
-// Writes a 16 x 8 fp32 fragment times `sign` as bf16 at (r0, c0) of a
-// swizzled block / of a row-major bf16 array.
+// Writes a 16 x 8 fp32 fragment times `sign` as type E at (r0, c0) of a
+// swizzled block / of a row-major array.
+template <typename E>
 __device__ __forceinline__ void st_frag_sw(uint8_t* blk, int r0, int c0, const float* d, float sign,
                                            int lane) {
   const int g = lane >> 2, c = 2 * (lane & 3);
-  *reinterpret_cast<uint32_t*>(blk + sw128(r0 + g, c0 + c)) = pack_bf16x2(sign * d[0], sign * d[1]);
+  *reinterpret_cast<uint32_t*>(blk + sw128(r0 + g, c0 + c)) = pack2<E>(sign * d[0], sign * d[1]);
   *reinterpret_cast<uint32_t*>(blk + sw128(r0 + g + 8, c0 + c)) =
-      pack_bf16x2(sign * d[2], sign * d[3]);
+      pack2<E>(sign * d[2], sign * d[3]);
 }
+template <typename E>
 __device__ __forceinline__ void st_frag(uint8_t* arr, int ld, int r0, int c0, const float* d,
                                         int lane) {
   const int g = lane >> 2, c = 2 * (lane & 3);
-  *reinterpret_cast<uint32_t*>(arr + ((r0 + g) * ld + c0 + c) * 2) = pack_bf16x2(d[0], d[1]);
-  *reinterpret_cast<uint32_t*>(arr + ((r0 + g + 8) * ld + c0 + c) * 2) = pack_bf16x2(d[2], d[3]);
+  *reinterpret_cast<uint32_t*>(arr + ((r0 + g) * ld + c0 + c) * 2) = pack2<E>(d[0], d[1]);
+  *reinterpret_cast<uint32_t*>(arr + ((r0 + g + 8) * ld + c0 + c) * 2) = pack2<E>(d[2], d[3]);
 }
 
 // Everything the prep work needs (the tensor maps are kernel parameters).
+template <typename E>
 struct PrepParams {
-  const bf16* k;  // the raw inputs, for L2 prefetches
-  const bf16* q;
-  const bf16* v;
+  const E* k;  // the raw inputs, for L2 prefetches
+  const E* q;
+  const E* v;
   const CUtensorMap* tm_a1o;  // A1 as [rows][2][64] (3-D), box {64, 2, 128}
   const CUtensorMap* tm_uo;   // Ut as [rows][2][64], box {64, 2, 64}
   const CUtensorMap* tm_yo;   // y as [B][T][Hv][2][64] (5-D), box {64, 2, 1, 64, 1}
-  const bf16* g;
-  const bf16* beta;
+  const E* g;
+  const E* beta;
   float* wsGC;
   int T, Hk, Hv, NT, BH;
   int opts;  // kOpt* bits
@@ -264,12 +319,12 @@ struct PrepParams {
 // With `flags`, each finished tile (b*Hv + hv, n) is published by raising
 // flags[(b*Hv + hv) * NT + n] to kTilePublished: each I/O thread adds 1 once
 // its own stores of the tile are in global memory.
-template <int C>
-__device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw, int cta_rank,
+template <int C, typename E>
+__device__ __forceinline__ void prep_role(const PrepParams<E>& P, uint8_t* smem_raw, int cta_rank,
                                           int n_ctas, int* flags) {
   const int T = P.T, Hk = P.Hk, Hv = P.Hv, NT = P.NT, BH = P.BH, opts = P.opts;
-  const bf16* __restrict__ g = P.g;
-  const bf16* __restrict__ beta = P.beta;
+  const E* __restrict__ g = P.g;
+  const E* __restrict__ beta = P.beta;
   float* __restrict__ wsGC = P.wsGC;
   // Per group: K and Q landed (128 cp.async arrivals, stream A), G1, GW, F1, F2,
   // V landed (128 arrivals, stream B) -- each completes once per tile.
@@ -338,14 +393,14 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
   // stream B (warps 4-7) loads a tile's V at its start, once the previous Ut
   // store (staged over V) has read it.  Each of the 128 threads then arrives on
   // the tile's barrier when its copies have landed.
-  auto load_rows = [&](const bf16* src, int heads, int hh, int b, int t0, uint32_t dst_base,
+  auto load_rows = [&](const E* src, int heads, int hh, int b, int t0, uint32_t dst_base,
                        uint32_t half_stride) {
     const int u = tid & 127;
 #pragma unroll 4
     for (int i = 0; i < 8; ++i) {
       const int idx = u + 128 * i, r = idx >> 4, cc = idx & 15;
       const int tok = t0 + r;
-      const bf16* gp = src + (((size_t)b * T + (tok < T ? tok : T - 1)) * heads + hh) * kD + cc * 8;
+      const E* gp = src + (((size_t)b * T + (tok < T ? tok : T - 1)) * heads + hh) * kD + cc * 8;
       cp_async16(dst_base + (cc >> 3) * half_stride + sw128(r, (cc & 7) * 8), gp,
                  tok < T ? 16u : 0u);
     }
@@ -366,9 +421,9 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
   // Ut) and publish the tile once those have landed.
   const int io = tid == 64 ? 0 : (tid == 192 ? 1 : -1);
   // Gate and beta of token `tid` of a tile, read one tile ahead into registers
-  // as raw bf16 bits (converted when used, so the load is not waited for here).
+  // as raw 16-bit values (converted when used, so the load is not waited for here).
   // Padded tokens: decay 1 (gate 1.0, or log-gate 0.0), beta 0.
-  const uint16_t g_pad = (opts & kOptLogGate) ? 0x0000 : 0x3f80;
+  const uint16_t g_pad = (opts & kOptLogGate) ? 0x0000 : ElemT<E>::kOne;
   uint16_t g_next = g_pad, b_next = 0;
   auto load_gates = [&](int lin) {
     g_next = g_pad;
@@ -383,7 +438,6 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
       }
     }
   };
-  auto bits_to_f32 = [](uint16_t x) { return __uint_as_float((uint32_t)x << 16); };
   if (io == 0) prefetch_tmap(P.tm_a1o);
   if (io == 1) {
     prefetch_tmap(P.tm_yo);
@@ -417,7 +471,7 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
   for (int lin = gid; lin < total; lin += ngroups, ++it) {
   const size_t tile_id = (size_t)head_of(lin) * NT + tile_of(lin);
   const int next = lin + ngroups;
-  const float gv_cur = bits_to_f32(g_next), bt_cur = bits_to_f32(b_next);
+  const float gv_cur = ElemT<E>::bits(g_next), bt_cur = ElemT<E>::bits(b_next);
   load_gates(next);
   // Gates (step 2).  Padded tokens take g = 1, beta = 0.  Decay products are
   // carried as chunk-local prefix sums lam of log2 g: G_t = 2^lam_t and
@@ -461,7 +515,7 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
   // tile rewrites it.
   if (io >= 0) bulk_wait_read_all();
   if (opts & kOptL2NormQK) {  // rows 0-63 of each half are K, 64-127 Q
-    if (ok) l2norm_row_sw128(sm + kOffKQ, 16384, tid >> 1, tid & 1);
+    if (ok) l2norm_row_sw128<E>(sm + kOffKQ, 16384, tid >> 1, tid & 1);
     fence_proxy_async();
     gsync();
   }
@@ -471,11 +525,11 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
   // outside the gate warps (lane 1 of warp 4).
   if (tid == 129) {
     tc_fence_after();
-    const uint32_t id1 = idesc_bf16(128, 64, false, false);
+    const uint32_t id1 = idesc_e<E>(128, 64, false, false);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       const uint32_t a = sbase + kOffKQ + (kk >> 2) * 16384 + (kk & 3) * 32;
-      mma_bf16_ss(tmem, smem_desc(a, 16, 1024, kSw128), smem_desc(a, 16, 1024, kSw128), id1,
+      mma_f16_ss(tmem, smem_desc(a, 16, 1024, kSw128), smem_desc(a, 16, 1024, kSw128), id1,
                   kk > 0);
     }
     mma_commit(bar_g1);
@@ -522,18 +576,18 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
         uint8_t* xl1 = sm + kOffXl1;
         if (cbeg == 0 && t >= 16 && t < 32) {  // L_10: rows 16-31, cols 0-15
           uint8_t* row = xl1 + ((t - 16) * kLd1) * 2;
-          *reinterpret_cast<uint4*>(row) = pack8(v);
-          *reinterpret_cast<uint4*>(row + 16) = pack8(v + 8);
+          *reinterpret_cast<uint4*>(row) = pack8<E>(v);
+          *reinterpret_cast<uint4*>(row + 16) = pack8<E>(v + 8);
         }
         if (cbeg == 32 && t >= 48) {  // L_32: rows 48-63, cols 32-47
           uint8_t* row = xl1 + ((16 + t - 48) * kLd1) * 2;
-          *reinterpret_cast<uint4*>(row) = pack8(v);
-          *reinterpret_cast<uint4*>(row + 16) = pack8(v + 8);
+          *reinterpret_cast<uint4*>(row) = pack8<E>(v);
+          *reinterpret_cast<uint4*>(row + 16) = pack8<E>(v + 8);
         }
         if (cbeg == 0 && t >= 32) {  // L_BA: rows 32-63, cols 0-31
           uint8_t* row = sm + kOffXl2 + ((t - 32) * kLd2) * 2;
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) *reinterpret_cast<uint4*>(row + 2 * e) = pack8(v + e);
+          for (int e = 0; e < 32; e += 8) *reinterpret_cast<uint4*>(row + 2 * e) = pack8<E>(v + e);
         }
       }
       tc_fence_before();
@@ -562,8 +616,8 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r)
-          *reinterpret_cast<bf16*>(x5 + sw128(16 * bl + r, 16 * bl + jj)) =
-              __float2bfloat16_rn(x[r]);
+          *reinterpret_cast<E*>(x5 + sw128(16 * bl + r, 16 * bl + jj)) =
+              ElemT<E>::from(x[r]);
       } else {
         // above the diagonal, and across chunks (C < 64): 32 16-byte pieces a block
         for (int p = tid - 128; p < 16 * 32; p += 64) {
@@ -596,8 +650,8 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
       }
 #pragma unroll
       for (int e = 0; e < 32; e += 8) {
-        st_sm16(sm, kOffX1 + sw128(t, cbeg + e), pack8(top + e));
-        st_sm16(sm, kOffX2 + sw128(t, cbeg + e), pack8(v + e));
+        st_sm16(sm, kOffX1 + sw128(t, cbeg + e), pack8<E>(top + e));
+        st_sm16(sm, kOffX2 + sw128(t, cbeg + e), pack8<E>(v + e));
       }
       fence_proxy_async();
     }
@@ -619,8 +673,8 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
         uint32_t a[4], bb[2];
         ldsm_x4(a_frag_addr(sbase + kOffXl1, kLd1, 16 * p, 0, lane), a);
         ldsm_x2_trans(b_frag_addr_sw(x5a, c0, c0 + 8 * nh, lane), bb);
-        mma_bf16_16816(d, a, bb);
-        st_frag(zs, kLd1, 16 * p, 8 * nh, d, lane);
+        mma_16816<E>(d, a, bb);
+        st_frag<E>(zs, kLd1, 16 * p, 8 * nh, d, lane);
       }
       gsync();
       if (warp < 4) {
@@ -628,8 +682,8 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
         uint32_t a[4], bb[2];
         ldsm_x4(a_frag_addr_sw(x5a, R, R, lane), a);
         ldsm_x2_trans(b_frag_addr(zsa, kLd1, 16 * p, 8 * nh, lane), bb);
-        mma_bf16_16816(d, a, bb);
-        st_frag_sw(x5, R, c0 + 8 * nh, d, -1.f, lane);
+        mma_16816<E>(d, a, bb);
+        st_frag_sw<E>(x5, R, c0 + 8 * nh, d, -1.f, lane);
       }
       gsync();
     }
@@ -644,9 +698,9 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
         for (int k0 = 0; k0 < 32; k0 += 16) {
           ldsm_x4(a_frag_addr(sbase + kOffXl2, kLd2, 16 * mt, k0, lane), a);
           ldsm_x2_trans(b_frag_addr_sw(x5a, k0, 8 * nt, lane), bb);
-          mma_bf16_16816(d, a, bb);
+          mma_16816<E>(d, a, bb);
         }
-        st_frag(zs, kLd2, 16 * mt, 8 * nt, d, lane);
+        st_frag<E>(zs, kLd2, 16 * mt, 8 * nt, d, lane);
       }
       gsync();
       {
@@ -656,9 +710,9 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
         for (int k0 = 0; k0 < 32; k0 += 16) {
           ldsm_x4(a_frag_addr_sw(x5a, 32 + 16 * mt, 32 + k0, lane), a);
           ldsm_x2_trans(b_frag_addr(zsa, kLd2, k0, 8 * nt, lane), bb);
-          mma_bf16_16816(d, a, bb);
+          mma_16816<E>(d, a, bb);
         }
-        st_frag_sw(x5, 32 + 16 * mt, 8 * nt, d, -1.f, lane);
+        st_frag_sw<E>(x5, 32 + 16 * mt, 8 * nt, d, -1.f, lane);
       }
       gsync();
     }
@@ -673,8 +727,8 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
     const int t = tid >> 2, c0 = 16 * (tid & 3), cs = (t / C) * C;
     const float bt = bta[t], lt = lam[t], gcp = gc[t / C] * bt, gs = gsuf[t];
     float tl[16], ta[16], cp[16], cu[16];
-    unpack8(*reinterpret_cast<const uint4*>(sm + kOffX5 + sw128(t, c0)), tl);
-    unpack8(*reinterpret_cast<const uint4*>(sm + kOffX5 + sw128(t, c0 + 8)), tl + 8);
+    unpack8<E>(*reinterpret_cast<const uint4*>(sm + kOffX5 + sw128(t, c0)), tl);
+    unpack8<E>(*reinterpret_cast<const uint4*>(sm + kOffX5 + sw128(t, c0 + 8)), tl + 8);
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
       const int j = c0 + e;
@@ -683,12 +737,12 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
       cp[e] = gcp * tl[e];
       cu[e] = gs * ta[e];
     }
-    st_sm16(sm, kOffX3 + sw128(t, c0), pack8(ta));
-    st_sm16(sm, kOffX3 + sw128(t, c0 + 8), pack8(ta + 8));
-    st_sm16(sm, kOffX0 + sw128(t, c0), pack8(cp));
-    st_sm16(sm, kOffX0 + sw128(t, c0 + 8), pack8(cp + 8));
-    st_sm16(sm, kOffX4 + sw128(t, c0), pack8(cu));
-    st_sm16(sm, kOffX4 + sw128(t, c0 + 8), pack8(cu + 8));
+    st_sm16(sm, kOffX3 + sw128(t, c0), pack8<E>(ta));
+    st_sm16(sm, kOffX3 + sw128(t, c0 + 8), pack8<E>(ta + 8));
+    st_sm16(sm, kOffX0 + sw128(t, c0), pack8<E>(cp));
+    st_sm16(sm, kOffX0 + sw128(t, c0 + 8), pack8<E>(cp + 8));
+    st_sm16(sm, kOffX4 + sw128(t, c0), pack8<E>(cu));
+    st_sm16(sm, kOffX4 + sw128(t, c0 + 8), pack8<E>(cu + 8));
     fence_proxy_async();
   }
   ok = gsync_and(ok);
@@ -697,10 +751,10 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
   // W_M = diag(G) M T_L, rows 64-127 x cols 0-63 are W_Y = (Gam . QK^T) T_A.
   if (ok && tid == 0) {
     tc_fence_after();
-    const uint32_t idw = idesc_bf16(128, 128, false, true);
+    const uint32_t idw = idesc_e<E>(128, 128, false, true);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
-      mma_bf16_ss(tmem, smem_desc(sbase + kOffX1 + kk * 32, 16, 1024, kSw128),
+      mma_f16_ss(tmem, smem_desc(sbase + kOffX1 + kk * 32, 16, 1024, kSw128),
                   smem_desc(sbase + kOffX3 + kk * 2048, 16384, 1024, kSw128), idw, kk > 0);
     mma_commit(bar_gw);
   }
@@ -720,7 +774,7 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
     for (int e = 0; e < 32; ++e) v[e] *= s;
     const uint32_t dst = top ? kOffX1 : kOffX5;
 #pragma unroll
-    for (int e = 0; e < 32; e += 8) st_sm16(sm, dst + sw128(t, c0 + e), pack8(v + e));
+    for (int e = 0; e < 32; e += 8) st_sm16(sm, dst + sw128(t, c0 + e), pack8<E>(v + e));
     fence_proxy_async();
   }
   tc_fence_before();
@@ -735,15 +789,15 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
   }
   if (ok && tid == 0) {
     tc_fence_after();
-    const uint32_t idf = idesc_bf16(128, 128, false, true);
+    const uint32_t idf = idesc_e<E>(128, 128, false, true);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
-      mma_bf16_ss(tmem, smem_desc(sbase + kOffX0 + kk * 32, 16, 1024, kSw128),
+      mma_f16_ss(tmem, smem_desc(sbase + kOffX0 + kk * 32, 16, 1024, kSw128),
                   smem_desc(sbase + kOffKQ + kk * 2048, 16384, 1024, kSw128), idf, kk > 0);
     mma_commit(bar_f1);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
-      mma_bf16_ss(tmem + 128, smem_desc(sbase + kOffX4 + kk * 32, 16, 1024, kSw128),
+      mma_f16_ss(tmem + 128, smem_desc(sbase + kOffX4 + kk * 32, 16, 1024, kSw128),
                   smem_desc(sbase + kOffV + kk * 2048, 8192, 1024, kSw128), idf, kk > 0);
     mma_commit(bar_f2);
   }
@@ -777,14 +831,14 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
 #pragma unroll
         for (int e = 0; e < 32; e += 8) {
           float q8[8];
-          unpack8(*reinterpret_cast<const uint4*>(sm + qsrc + sw128(t, cc + e)), q8);
+          unpack8<E>(*reinterpret_cast<const uint4*>(sm + qsrc + sw128(t, cc + e)), q8);
 #pragma unroll
           for (int i = 0; i < 8; ++i) v[e + i] = fmaf(gt, q8[i], v[e + i]);
         }
       }
 #pragma unroll
       for (int e = 0; e < 32; e += 8)
-        st_sm16(sm, sbuf + sw128(2 * srow + h, cc + e), pack8(v + e));
+        st_sm16(sm, sbuf + sw128(2 * srow + h, cc + e), pack8<E>(v + e));
     }
     fence_proxy_async();
   }
@@ -818,17 +872,17 @@ __device__ __forceinline__ void prep_role(const PrepParams& P, uint8_t* smem_raw
   if (threadIdx.x < 32) tmem_dealloc(tmem_base_sh, 256 * kPrepGroups);
 }
 
-template <int C>
+template <int C, typename E>
 __global__ void __launch_bounds__(kPrepThreads, 1)
 prep_tc_kernel(const __grid_constant__ CUtensorMap tm_a1o, const __grid_constant__ CUtensorMap tm_uo,
-               const __grid_constant__ CUtensorMap tm_yo, const bf16* kin, const bf16* qin,
-               const bf16* vin, const bf16* __restrict__ g, const bf16* __restrict__ beta,
+               const __grid_constant__ CUtensorMap tm_yo, const E* kin, const E* qin,
+               const E* vin, const E* __restrict__ g, const E* __restrict__ beta,
                float* __restrict__ wsGC, int T, int Hk, int Hv, int NT, int BH, int opts,
                float scale) {
   extern __shared__ uint8_t smem_raw[];
-  const PrepParams P{kin, qin, vin, &tm_a1o, &tm_uo, &tm_yo, g, beta, wsGC,
+  const PrepParams<E> P{kin, qin, vin, &tm_a1o, &tm_uo, &tm_yo, g, beta, wsGC,
                      T, Hk, Hv, NT, BH, opts, scale};
-  prep_role<C>(P, smem_raw, blockIdx.x, gridDim.x, nullptr);
+  prep_role<C, E>(P, smem_raw, blockIdx.x, gridDim.x, nullptr);
 }
 
 // ============================================================================
@@ -887,7 +941,7 @@ enum : int {
   kNumQBars
 };
 
-template <int C>
+template <int C, typename E>
 __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CUtensorMap* tm_k,
                                              const CUtensorMap* tm_uy, const CUtensorMap* tm_yred,
                                              const float* wsGC, const int* flags,
@@ -1018,9 +1072,9 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
     // until the state group has read D(j); M^T(j+1) overwrites the TMEM operand
     // of D_S(j-1), complete once the S operand of chunk j is written.
     if (lane == 0) {
-      const uint32_t id_kt = idesc_bf16(128, 128, true, true);   // K^T x (Pt | Ut)
-      const uint32_t id_s = idesc_bf16(128, 128, false, true);   // (-M^T) x S^T
-      const uint32_t id_y = idesc_bf16(128, C, true, false);     // S x Qh^T (rows v, cols t)
+      const uint32_t id_kt = idesc_e<E>(128, 128, true, true);   // K^T x (Pt | Ut)
+      const uint32_t id_s = idesc_e<E>(128, 128, false, true);   // (-M^T) x S^T
+      const uint32_t id_y = idesc_e<E>(128, C, true, false);     // S x Qh^T (rows v, cols t)
       // Descriptor bases (per ring stage via a byte offset; see SmemDesc).
       const SmemDesc d_mn_mn = smem_desc_base(sbase, 8192, 1024, kSw128);   // MN-major, 64-row halves
       const SmemDesc d_s = smem_desc_base(sS, 16384, 1024, kSw128);         // S operand
@@ -1036,7 +1090,7 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
           const uint32_t ta = tM(j & 1);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ts(tD, ta + 8 * kk, smem_desc_at(d_s, kk * 2048), id_s, 1);
+            mma_f16_ts(tD, ta + 8 * kk, smem_desc_at(d_s, kk * 2048), id_s, 1);
           mma_commit(bar(kQDs));
         }
       } else {
@@ -1049,7 +1103,7 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
           const uint32_t off = ring_mn(j) * SM::kMN + (j % kCt) * C * 128;
 #pragma unroll
           for (int kk = 0; kk < C / 16; ++kk)
-            mma_bf16_ss(tM(j & 1), smem_desc_at(d_mn_mn, off + SM::kOffK + kk * 2048),
+            mma_f16_ss(tM(j & 1), smem_desc_at(d_mn_mn, off + SM::kOffK + kk * 2048),
                         smem_desc_at(d_mn_mn, off + SM::kOffP + kk * 2048), id_kt, kk > 0);
           mma_commit(bar(kQM + (j & 1)));
           return true;
@@ -1060,7 +1114,7 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
           const uint32_t off = ring_mn(j) * SM::kMN + (j % kCt) * C * 128;
 #pragma unroll
           for (int kk = 0; kk < C / 16; ++kk)
-            mma_bf16_ss(tD, smem_desc_at(d_mn_mn, off + SM::kOffK + kk * 2048),
+            mma_f16_ss(tD, smem_desc_at(d_mn_mn, off + SM::kOffK + kk * 2048),
                         smem_desc_at(d_mn_mn, off + SM::kOffU + kk * 2048), id_kt, kk > 0);
           mma_commit(bar(kQDN));
           // The tile's MN buffers are free once its last products finish.
@@ -1081,7 +1135,7 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
           const uint32_t qoff = ring_q(j) * SM::kQ + c * C * 128;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ss(tY, smem_desc_at(d_s, kk * 2048),
+            mma_f16_ss(tY, smem_desc_at(d_s, kk * 2048),
                         smem_desc_at(d_q, qoff + (kk >> 2) * 8192 + (kk & 3) * 32), id_y, kk > 0);
           mma_commit(bar(kQY));
           if (j + 1 < NC) {
@@ -1111,7 +1165,7 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
     auto write_op = [&]() {
       uint8_t* row = sm + SM::kOffS + h * 16384;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) st_sm16(row, sw128(L, 8 * ch), pack8(s + 8 * ch));
+      for (int ch = 0; ch < 8; ++ch) st_sm16(row, sw128(L, 8 * ch), pack8<E>(s + 8 * ch));
       fence_proxy_async();
       mbar_arrive(bar(kQSop));
     };
@@ -1160,7 +1214,7 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
         tmem_wait_ld();
         uint32_t p[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) p[i] = pack_bf16x2(-v[2 * i], -v[2 * i + 1]);
+        for (int i = 0; i < 32; ++i) p[i] = pack2<E>(-v[2 * i], -v[2 * i + 1]);
         tmem_st32(tb + 32 * hh, p);
       }
       tmem_wait_st();
@@ -1173,7 +1227,7 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
     const int atid = tid - 320;  // 0..127 in the aux group
     auto normalise_k = [&](int j) {
       if (!wait_mn(j)) return false;
-      l2norm_row_sw128(sm + (mn_addr(j) - sbase) + SM::kOffK, 8192, atid >> 1, atid & 1);
+      l2norm_row_sw128<E>(sm + (mn_addr(j) - sbase) + SM::kOffK, 8192, atid >> 1, atid & 1);
       fence_proxy_async();
       mbar_arrive(bar(kQKNorm + ring_mn(j)));
       return true;
@@ -1210,7 +1264,7 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
         for (int i = 0; i < (C < 32 ? C : 32); ++i) {
           const int row = c * C + t0 + i;
           const uint32_t off = row * 128 + ((((vv >> 3) ^ (row & 7))) << 4) + (vv & 7) * 2;
-          *reinterpret_cast<bf16*>(hbase + off) = __float2bfloat16_rn(d[i] * scale);
+          *reinterpret_cast<E*>(hbase + off) = ElemT<E>::from(d[i] * scale);
         }
       }
       fence_proxy_async();
@@ -1233,7 +1287,7 @@ __device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CU
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-template <int C>
+template <int C, typename E>
 __global__ void __launch_bounds__(kFusedThreads, 1)
 fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_q,
@@ -1243,24 +1297,24 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_yred,
                      const __grid_constant__ CUtensorMap tm_a1o,
                      const __grid_constant__ CUtensorMap tm_uo,
-                     const __grid_constant__ CUtensorMap tm_yo, const bf16* kin,
-                     const bf16* qin, const bf16* vin, const bf16* __restrict__ g,
-                     const bf16* __restrict__ beta, float* __restrict__ wsGC, int* flags,
+                     const __grid_constant__ CUtensorMap tm_yo, const E* kin,
+                     const E* qin, const E* vin, const E* __restrict__ g,
+                     const E* __restrict__ beta, float* __restrict__ wsGC, int* flags,
                      const float* state_in, float* state_out, int T, int Hk, int Hv, int NT,
                      int BH, int opts, float scale) {
   extern __shared__ uint8_t smem_raw[];
   if ((int)blockIdx.x < BH) {
-    scan_role128<C>(&tm_a1s, &tm_k, &tm_us, &tm_yred, wsGC, flags, state_in, state_out, T, Hk,
+    scan_role128<C, E>(&tm_a1s, &tm_k, &tm_us, &tm_yred, wsGC, flags, state_in, state_out, T, Hk,
                     Hv, NT, blockIdx.x, opts, scale, smem_raw);
   } else {
-    const PrepParams P{kin, qin, vin, &tm_a1o, &tm_uo, &tm_yo, g, beta, wsGC,
+    const PrepParams<E> P{kin, qin, vin, &tm_a1o, &tm_uo, &tm_yo, g, beta, wsGC,
                        T, Hk, Hv, NT, BH, opts, scale};
-    prep_role<C>(P, smem_raw, blockIdx.x - BH, gridDim.x - BH, flags);
+    prep_role<C, E>(P, smem_raw, blockIdx.x - BH, gridDim.x - BH, flags);
   }
 }
 
 // The scan alone (after prep_tc_kernel in stream order): one CTA per head.
-template <int C>
+template <int C, typename E>
 __global__ void __launch_bounds__(kFusedThreads, 1)
 scan_head_kernel(const __grid_constant__ CUtensorMap tm_a1s, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_us,
@@ -1268,7 +1322,7 @@ scan_head_kernel(const __grid_constant__ CUtensorMap tm_a1s, const __grid_consta
                  const float* state_in, float* state_out, int T, int Hk, int Hv, int NT,
                  int opts, float scale) {
   extern __shared__ uint8_t smem_raw[];
-  scan_role128<C>(&tm_a1s, &tm_k, &tm_us, &tm_yred, wsGC, nullptr, state_in, state_out, T, Hk,
+  scan_role128<C, E>(&tm_a1s, &tm_k, &tm_us, &tm_yred, wsGC, nullptr, state_in, state_out, T, Hk,
                   Hv, NT, blockIdx.x, opts, scale, smem_raw);
 }
 
@@ -1294,21 +1348,23 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [B, T, H, 128] bf16 -> box {64 cols, 1 head, 64 tokens, 1 batch}, 128B swizzle.
-bool make_bthd_map(CUtensorMap* m, const void* base, int B, int T, int H, int box_t = kTile) {
+// [B, T, H, 128] 16-bit elements of type dt -> box {64 cols, 1 head, 64
+// tokens, 1 batch}, 128B swizzle.
+bool make_bthd_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int B, int T, int H, int box_t = kTile) {
   const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
   const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2,
                                  (cuuint64_t)T * H * kD * 2};
   const cuuint32_t box[4] = {64, 1, (cuuint32_t)box_t, 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
-  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+  return encode_fn()(m, dt, 4, const_cast<void*>(base), dims,
                      strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-// [rows, 128] bf16 2-D view of a workspace region.  Swizzled boxes use the
-// swizzle whose span equals the box row (box_cols * 2 bytes: 32, 64 or 128).
-bool make_rows_map(CUtensorMap* m, const void* base, size_t rows, int box_cols, int box_rows,
+// [rows, 128] 2-D view of a workspace region of 16-bit elements.  Swizzled
+// boxes use the swizzle whose span equals the box row (box_cols * 2 bytes: 32,
+// 64 or 128).
+bool make_rows_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, size_t rows, int box_cols, int box_rows,
                    bool swizzle) {
   const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
@@ -1318,33 +1374,34 @@ bool make_rows_map(CUtensorMap* m, const void* base, size_t rows, int box_cols, 
   if (swizzle)
     sw = box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
                         : (box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
-  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+  return encode_fn()(m, dt, 2, const_cast<void*>(base), dims,
                      strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 
-// Rows of 128 bf16 values seen as [rows][2 halves][64] (3-D), box {64, 2,
+// Rows of 128 16-bit values seen as [rows][2 halves][64] (3-D), box {64, 2,
 // box_rows}: the box lands in shared memory as [row][half] 128-byte units.
-bool make_rows_halves_map(CUtensorMap* m, const void* base, size_t rows, int box_rows) {
+bool make_rows_halves_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, size_t rows, int box_rows) {
   const cuuint64_t dims[3] = {64, 2, (cuuint64_t)rows};
   const cuuint64_t strides[2] = {128, (cuuint64_t)kD * 2};
   const cuuint32_t box[3] = {64, 2, (cuuint32_t)box_rows};
   const cuuint32_t es[3] = {1, 1, 1};
-  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+  return encode_fn()(m, dt, 3, const_cast<void*>(base), dims,
                      strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-// [B, T, H, 128] bf16 seen as [B][T][H][2][64] (5-D), box {64, 2, 1, 64, 1}.
-bool make_bthd_halves_map(CUtensorMap* m, const void* base, int B, int T, int H) {
+// [B, T, H, 128] 16-bit elements seen as [B][T][H][2][64] (5-D), box {64, 2,
+// 1, 64, 1}.
+bool make_bthd_halves_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int B, int T, int H) {
   const cuuint64_t dims[5] = {64, 2, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
   const cuuint64_t strides[4] = {128, (cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2,
                                  (cuuint64_t)T * H * kD * 2};
   const cuuint32_t box[5] = {64, 2, 1, (cuuint32_t)kTile, 1};
   const cuuint32_t es[5] = {1, 1, 1, 1, 1};
-  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims,
+  return encode_fn()(m, dt, 5, const_cast<void*>(base), dims,
                      strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -1363,41 +1420,43 @@ int num_sms() {
   return cache[dev];
 }
 
-template <int C>
+template <int C, typename E>
 cudaError_t launch_c(const PrefillArgs& a) {
   const int NT = (a.T + kTile - 1) / kTile;
   const int BH = a.B * a.Hv;
   const WsLayout w = ws_layout(BH, NT);
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-  bf16* wsA1 = reinterpret_cast<bf16*>(ws + w.a1);
-  bf16* wsU = reinterpret_cast<bf16*>(ws + w.u);
+  E* wsA1 = reinterpret_cast<E*>(ws + w.a1);
+  E* wsU = reinterpret_cast<E*>(ws + w.u);
   float* wsGC = reinterpret_cast<float*>(ws + w.gc);
 
   if (!encode_fn()) return cudaErrorNotSupported;
   CUtensorMap tk, tq, tv, ta1s, tus, tyred, ta1o, tuo, tyo;
-  if (!make_bthd_map(&tk, a.k, a.B, a.T, a.Hk) || !make_bthd_map(&tq, a.q, a.B, a.T, a.Hk) ||
-      !make_bthd_map(&tv, a.v, a.B, a.T, a.Hv) ||
-      !make_rows_map(&ta1s, wsA1, (size_t)BH * NT * 128, 64, C, true) ||
-      !make_rows_map(&tus, wsU, (size_t)BH * NT * kTile, 64, 64, true) ||
-      !make_bthd_map(&tyred, a.y, a.B, a.T, a.Hv, C) ||
-      !make_rows_halves_map(&ta1o, wsA1, (size_t)BH * NT * 128, 128) ||
-      !make_rows_halves_map(&tuo, wsU, (size_t)BH * NT * kTile, kTile) ||
-      !make_bthd_halves_map(&tyo, a.y, a.B, a.T, a.Hv))
+  const CUtensorMapDataType dt = ElemT<E>::kTmap;
+  if (!make_bthd_map(&tk, dt, a.k, a.B, a.T, a.Hk) ||
+      !make_bthd_map(&tq, dt, a.q, a.B, a.T, a.Hk) ||
+      !make_bthd_map(&tv, dt, a.v, a.B, a.T, a.Hv) ||
+      !make_rows_map(&ta1s, dt, wsA1, (size_t)BH * NT * 128, 64, C, true) ||
+      !make_rows_map(&tus, dt, wsU, (size_t)BH * NT * kTile, 64, 64, true) ||
+      !make_bthd_map(&tyred, dt, a.y, a.B, a.T, a.Hv, C) ||
+      !make_rows_halves_map(&ta1o, dt, wsA1, (size_t)BH * NT * 128, 128) ||
+      !make_rows_halves_map(&tuo, dt, wsU, (size_t)BH * NT * kTile, kTile) ||
+      !make_bthd_halves_map(&tyo, dt, a.y, a.B, a.T, a.Hv))
     return cudaErrorInvalidValue;
 
   const float scale = 1.0f / sqrtf((float)kD);
   const int sms = num_sms();
-  const bf16* k = static_cast<const bf16*>(a.k);
-  const bf16* q = static_cast<const bf16*>(a.q);
-  const bf16* v = static_cast<const bf16*>(a.v);
-  const bf16* g = static_cast<const bf16*>(a.g);
-  const bf16* beta = static_cast<const bf16*>(a.beta);
+  const E* k = static_cast<const E*>(a.k);
+  const E* q = static_cast<const E*>(a.q);
+  const E* v = static_cast<const E*>(a.v);
+  const E* g = static_cast<const E*>(a.g);
+  const E* beta = static_cast<const E*>(a.beta);
   cudaError_t e;
   // Fused path: one scan CTA per head next to at least two thirds of the SMs
   // doing prep, in one cooperative launch.
   if (3 * BH <= sms) {
     int* flags = reinterpret_cast<int*>(ws + w.flags);
-    e = cudaFuncSetAttribute(fused_prefill_kernel<C>,
+    e = cudaFuncSetAttribute(fused_prefill_kernel<C, E>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kFusedSmem);
     if (e == cudaSuccess) e = cudaMemsetAsync(flags, 0, (size_t)BH * NT * sizeof(int), a.stream);
     if (e != cudaSuccess) return e;
@@ -1411,27 +1470,36 @@ cudaError_t launch_c(const PrefillArgs& a) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fused_prefill_kernel<C>, tk, tq, tv, ta1s, tus, tyred, ta1o,
+    return cudaLaunchKernelEx(&cfg, fused_prefill_kernel<C, E>, tk, tq, tv, ta1s, tus, tyred, ta1o,
                               tuo, tyo, k, q, v, g, beta, wsGC, flags, a.state_in, a.state_out,
                               a.T, a.Hk, a.Hv, NT, BH, a.options, scale);
   }
 
   // Split path: the persistent prep kernel on every SM, then one scan CTA per head.
-  e = cudaFuncSetAttribute(prep_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(prep_tc_kernel<C, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kPrepSmem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(scan_head_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(scan_head_kernel<C, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Scan128Smem::kTotal);
   if (e != cudaSuccess) return e;
   const int prep_ctas = std::min(sms, (BH * NT + kPrepGroups - 1) / kPrepGroups);
-  prep_tc_kernel<C><<<prep_ctas, kPrepThreads, kPrepSmem, a.stream>>>(
+  prep_tc_kernel<C, E><<<prep_ctas, kPrepThreads, kPrepSmem, a.stream>>>(
       ta1o, tuo, tyo, k, q, v, g, beta, wsGC, a.T, a.Hk, a.Hv, NT, BH, a.options, scale);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  scan_head_kernel<C><<<BH, kFusedThreads, Scan128Smem::kTotal, a.stream>>>(
+  scan_head_kernel<C, E><<<BH, kFusedThreads, Scan128Smem::kTotal, a.stream>>>(
       ta1s, tk, tus, tyred, wsGC, a.state_in, a.state_out, a.T, a.Hk, a.Hv, NT, a.options,
       scale);
   return cudaGetLastError();
+}
+
+template <typename E>
+cudaError_t launch_e(const PrefillArgs& a) {
+  switch (a.chunk) {
+    case 16: return launch_c<16, E>(a);
+    case 32: return launch_c<32, E>(a);
+    default: return launch_c<64, E>(a);
+  }
 }
 
 }  // namespace
@@ -1440,12 +1508,9 @@ size_t prefill_tc_workspace_bytes(int B, int T, int Hv) {
   return ws_layout(B * Hv, (T + kTile - 1) / kTile).total;
 }
 
+// dtype 1 bf16, 2 fp16 (the GDN_DTYPE_* codes).
 cudaError_t launch_prefill_tc(const PrefillArgs& a) {
-  switch (a.chunk) {
-    case 16: return launch_c<16>(a);
-    case 32: return launch_c<32>(a);
-    default: return launch_c<64>(a);
-  }
+  return a.dtype == 2 ? launch_e<__half>(a) : launch_e<bf16>(a);
 }
 
 int prefill_tc_device_error(bool clear) {

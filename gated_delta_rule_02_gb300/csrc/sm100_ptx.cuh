@@ -64,6 +64,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test whether the phase with parity `parity` has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Wait for the phase with parity `parity` to complete, for at most
 // kWaitLimitNs; on timeout set the device error word and return false.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
@@ -259,7 +271,7 @@ __device__ __forceinline__ void tc_fence_after() {
 
 // D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (bf16 or fp16 inputs,
 // fp32 accumulate).  Issued by one thread.
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -272,7 +284,7 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
 // D[tmem] (+)= A[tmem] * B[smem desc], kind::f16.  A sits in tensor memory
 // with row m in lane m and two 16-bit elements per 32-bit column (K = 16 spans
 // 8 columns).
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -365,13 +377,18 @@ __device__ __forceinline__ uint64_t smem_desc_at(SmemDesc d, uint32_t byte_off) 
   return ((uint64_t)d.hi << 32) | (uint64_t)(d.lo + (byte_off >> 4));
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and fp32 D:
-//   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
+// Instruction descriptor for kind::f16 with A and B of format `fmt` (0 fp16,
+// 1 bf16) and fp32 D:
+//   bits 4-5 D format (1 = f32), 7-9 A format, 10-12 B format,
 //   bit 15 A major (0 K, 1 MN), bit 16 B major, bits 17-22 N >> 3,
 //   bits 24-28 M >> 4.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+__host__ __device__ constexpr uint32_t idesc_kind_f16(int M, int N, bool a_mn, bool b_mn,
+                                                      uint32_t fmt) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((a_mn ? 1u : 0u) << 15) |
          ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+  return idesc_kind_f16(M, N, a_mn, b_mn, 1u);
 }
 
 }  // namespace ptx

@@ -21,6 +21,9 @@ import dataclasses
 import torch
 
 
+DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+
+
 @dataclasses.dataclass(frozen=True)
 class Workload:
     name: str
@@ -30,7 +33,7 @@ class Workload:
     Hv: int
     Dk: int
     Dv: int
-    dtype: str          # "f32" or "bf16"
+    dtype: str          # "f32", "bf16" or "f16"
     chunk: int
     u_max: float
     s0_std: float
@@ -41,13 +44,13 @@ class Workload:
 
     @property
     def torch_dtype(self):
-        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+        return DTYPES[self.dtype]
 
     def scaled(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
 
 
-# The five workloads of the benchmark plan, named by what they are.
+# The workloads of the benchmark plan, named by what they are.
 WORKLOADS = {
     "fp32_t64": Workload("fp32_t64", B=1, T=64, Hk=2, Hv=2, Dk=128, Dv=128,
                          dtype="f32", chunk=32, u_max=0.1, s0_std=0.1, seed=1000),
@@ -69,6 +72,11 @@ WORKLOADS = {
     "prefill_b64_t16": Workload("prefill_b64_t16", B=64, T=16, Hk=16, Hv=32, Dk=128,
                                 Dv=128, dtype="bf16", chunk=64, u_max=0.1,
                                 s0_std=0.1, seed=1005),
+    # The headline shape with fp16 inputs (the other 16-bit type the tensor
+    # cores take).
+    "prefill_t4096_f16": Workload("prefill_t4096_f16", B=1, T=4096, Hk=16, Hv=32, Dk=128,
+                                  Dv=128, dtype="f16", chunk=64, u_max=0.1,
+                                  s0_std=0.0, seed=1006),
 }
 
 
@@ -85,7 +93,7 @@ def make_inputs(B, T, Hk, Hv, Dk, Dv, dtype=torch.bfloat16, seed=0, u_max=0.1,
     so ``draw_state=False`` leaves the other tensors unchanged and omits it).
     """
     if isinstance(dtype, str):
-        dtype = torch.float32 if dtype == "f32" else torch.bfloat16
+        dtype = DTYPES[dtype]
     gen = torch.Generator().manual_seed(int(seed))
     q = _unit_rows(torch.randn((B, T, Hk, Dk), generator=gen))
     k = _unit_rows(torch.randn((B, T, Hk, Dk), generator=gen))

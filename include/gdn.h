@@ -68,8 +68,8 @@ extern "C" {
 /* Element types of q, k, v, g, beta and y. */
 #define GDN_DTYPE_F32   0
 #define GDN_DTYPE_BF16  1
-/* fp16: decode and T <= 32 on the row-packed kernels; longer prefills on the
- * fp32 CUDA-core chunked path (the tensor-core path is bf16 only). */
+/* fp16: as bf16 (decode and T <= 32 on the row-packed kernels; longer
+ * prefills with Dk = Dv = 128 on the tensor cores, in fp16 operands). */
 #define GDN_DTYPE_F16   2
 
 /*
@@ -86,8 +86,9 @@ extern "C" {
  *   GDN_OPT_L2NORM_QK    every q and k row (Dk values) is used as x / |x|,
  *                        computed in fp32 from the stored values (the step
  *                        before the recurrence in the MLX PR's test inputs); a
- *                        zero row stays zero.  For bf16 inputs the normalised
- *                        rows enter the tensor-core products rounded to bf16.
+ *                        zero row stays zero.  For bf16 or fp16 inputs the
+ *                        normalised rows enter the tensor-core products
+ *                        rounded to the input type.
  * Any other bit gives GDN_ERR_UNSUPPORTED.
  */
 #define GDN_OPT_TILED_HEADS 1
@@ -120,8 +121,10 @@ GDN_API size_t gdn_prefill_workspace_bytes(int B, int T, int Hk, int Hv, int Dk,
  *              entry do not matter and on return are unspecified.  It must
  *              not be used by anything else until the work on `stream` is done.
  *   stream     cudaStream_t, or NULL.
- * Dk and Dv are each 64, 128 or 256.  bf16 inputs with Dk = Dv = 128 run on
- * the tensor cores; every other head size and dtype runs the fp32 chunked
+ * Dk and Dv are each 64, 128 or 256.  bf16 and fp16 inputs with Dk = Dv = 128
+ * run on the tensor cores, whose operands (the inputs and the per-chunk
+ * intermediates) are then rounded to the input type and whose products
+ * accumulate in fp32; every other head size and dtype runs the fp32 chunked
  * path, which for Dk = Dv = 256 runs a chunk of 64 as two chunks of 32 (the
  * result differs only by rounding; gdn_prefill_workspace_bytes accounts for
  * it).  Returns GDN_OK or a GDN_ERR_* code.

@@ -42,6 +42,7 @@ class _Props:
 
 @pytest.mark.parametrize("name,expect", [
     ("prefill_t4096", 1),       # fused cooperative kernel: 3 * 32 <= 152
+    ("prefill_t4096_f16", 1),
     ("prefill_t65536", 1),
     ("prefill_b4_t2048", 2),    # 3 * 192 > 152: prep then scan
     ("prefill_b64_t16", 1),     # T <= 32: the short-T kernel
