@@ -300,9 +300,9 @@ __device__ __forceinline__ void st_frag(uint8_t* arr, int ld, int r0, int c0, co
 // Everything the prep work needs (the tensor maps are kernel parameters).
 template <typename E>
 struct PrepParams {
-  const E* k;  // the raw inputs, for L2 prefetches
-  const E* q;
-  const E* v;
+  const CUtensorMap* tm_k;    // the inputs as [B][T][H][128], box {64, 1, 64, 1}
+  const CUtensorMap* tm_q;
+  const CUtensorMap* tm_v;
   const CUtensorMap* tm_a1o;  // A1 as [rows][2][64] (3-D), box {64, 2, 128}
   const CUtensorMap* tm_uo;   // Ut as [rows][2][64], box {64, 2, 64}
   const CUtensorMap* tm_yo;   // y as [B][T][Hv][2][64] (5-D), box {64, 2, 1, 64, 1}
@@ -365,7 +365,7 @@ __device__ __forceinline__ void prep_role(const PrepParams<E>& P, uint8_t* smem_
 
   if (threadIdx.x == 0) {
     for (int q = 0; q < kPrepGroups; ++q) {
-      for (int i = 0; i < 6; ++i) mbar_init(smem_u32(&bars[q][i]), (i == 0 || i == 5) ? 128 : 1);
+      for (int i = 0; i < 6; ++i) mbar_init(smem_u32(&bars[q][i]), 1);
       abort_sh[q] = 0;
     }
     fence_mbar_init();
@@ -386,40 +386,37 @@ __device__ __forceinline__ void prep_role(const PrepParams<E>& P, uint8_t* smem_
   const int gid = cta_rank * kPrepGroups + grp;
   auto head_of = [&](int lin) { return lin % BH; };
   auto tile_of = [&](int lin) { return lin / BH; };
-  // Inputs come in with cp.async (16 bytes a thread, written straight into the
-  // 128B-swizzled operand layout; rows past T read as zeros), which does not
-  // queue behind the TMA stores of the outputs.  Stream A (warps 0-3) loads the
-  // next tile's K and Q once this tile's F1 and Qh epilogue are done with them;
-  // stream B (warps 4-7) loads a tile's V at its start, once the previous Ut
-  // store (staged over V) has read it.  Each of the 128 threads then arrives on
-  // the tile's barrier when its copies have landed.
-  auto load_rows = [&](const E* src, int heads, int hh, int b, int t0, uint32_t dst_base,
-                       uint32_t half_stride) {
-    const int u = tid & 127;
-#pragma unroll 4
-    for (int i = 0; i < 8; ++i) {
-      const int idx = u + 128 * i, r = idx >> 4, cc = idx & 15;
-      const int tok = t0 + r;
-      const E* gp = src + (((size_t)b * T + (tok < T ? tok : T - 1)) * heads + hh) * kD + cc * 8;
-      cp_async16(dst_base + (cc >> 3) * half_stride + sw128(r, (cc & 7) * 8), gp,
-                 tok < T ? 16u : 0u);
-    }
-  };
-  auto load_kq = [&](int lin) {  // stream A
+  // The two I/O threads issue the TMA copies of the group: io 0 loads K and Q
+  // (into the 128B-swizzled operand layout; rows past T read as zeros) and
+  // stores the tile's A1 rows, io 1 loads V and stores y_loc and Ut, and each
+  // publishes the tile once its stores have landed.  io 0 loads the next
+  // tile's K and Q as soon as this tile's F1 and Qh epilogue are done with
+  // them (before its stores, so the loads do not queue behind them); io 1
+  // loads a tile's V at its start, once the previous Ut store (staged over V)
+  // has read it.
+  const int io = tid == 64 ? 0 : (tid == 192 ? 1 : -1);
+  bool kq_pending = false, v_pending = false;  // loads issued and not yet waited for
+  auto load_kq = [&](int lin) {  // io 0
     const int bh = head_of(lin), b = bh / Hv, hv = bh - b * Hv;
     const int hk = key_head(hv, Hk, Hv, opts), t0 = tile_of(lin) * kTile;
-    load_rows(P.k, Hk, hk, b, t0, sbase + kOffKQ, 16384);
-    load_rows(P.q, Hk, hk, b, t0, sbase + kOffKQ + 8192, 16384);
-    cp_async_mbar_arrive(bar_tma);
+    fence_proxy_async();  // earlier generic reads of the buffers, before the copies
+    mbar_expect_tx(bar_tma, 32768);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      tma_load_4d(sbase + kOffKQ + h * 16384, P.tm_k, bar_tma, 64 * h, hk, t0, b);
+      tma_load_4d(sbase + kOffKQ + h * 16384 + 8192, P.tm_q, bar_tma, 64 * h, hk, t0, b);
+    }
+    kq_pending = true;
   };
-  auto load_v = [&](int lin) {  // stream B
+  auto load_v = [&](int lin) {  // io 1
     const int bh = head_of(lin), b = bh / Hv, hv = bh - b * Hv, t0 = tile_of(lin) * kTile;
-    load_rows(P.v, Hv, hv, b, t0, sbase + kOffV, 8192);
-    cp_async_mbar_arrive(bar_v);
+    fence_proxy_async();
+    mbar_expect_tx(bar_v, 16384);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      tma_load_4d(sbase + kOffV + h * 8192, P.tm_v, bar_v, 64 * h, hv, t0, b);
+    v_pending = true;
   };
-  // The two I/O threads issue the tile's TMA stores (io 0: A1; io 1: y_loc and
-  // Ut) and publish the tile once those have landed.
-  const int io = tid == 64 ? 0 : (tid == 192 ? 1 : -1);
   // Gate and beta of token `tid` of a tile, read one tile ahead into registers
   // as raw 16-bit values (converted when used, so the load is not waited for here).
   // Padded tokens: decay 1 (gate 1.0, or log-gate 0.0), beta 0.
@@ -438,14 +435,19 @@ __device__ __forceinline__ void prep_role(const PrepParams<E>& P, uint8_t* smem_
       }
     }
   };
-  if (io == 0) prefetch_tmap(P.tm_a1o);
+  if (io == 0) {
+    prefetch_tmap(P.tm_k);
+    prefetch_tmap(P.tm_q);
+    prefetch_tmap(P.tm_a1o);
+  }
   if (io == 1) {
+    prefetch_tmap(P.tm_v);
     prefetch_tmap(P.tm_yo);
     prefetch_tmap(P.tm_uo);
   }
   if (gid < total) {
-    if (streamA) load_kq(gid);
-    else load_v(gid);
+    if (io == 0) load_kq(gid);
+    if (io == 1) load_v(gid);
   }
   load_gates(gid);
 
@@ -510,7 +512,7 @@ __device__ __forceinline__ void prep_role(const PrepParams<E>& P, uint8_t* smem_
   }
 
   ok = ok && mbar_wait(bar_tma, it & 1);
-  fence_proxy_async();  // the cp.async writes of K, Q, seen before the tensor core reads them
+  kq_pending = false;
   // The previous tile's stores have read their staging (X0..X5, V) before this
   // tile rewrites it.
   if (io >= 0) bulk_wait_read_all();
@@ -535,7 +537,7 @@ __device__ __forceinline__ void prep_role(const PrepParams<E>& P, uint8_t* smem_
     mma_commit(bar_g1);
   }
   if (io >= 0) publish();        // the previous tile, stored a while ago
-  if (!streamA && it > 0) load_v(lin);  // V for F2, over the previous Ut staging
+  if (io == 1 && it > 0) load_v(lin);  // V for F2, over the previous Ut staging
   ok = ok && mbar_wait(bar_g1, it & 1);
   tc_fence_after();
   // Warps w and w+4 share TMEM lane quadrant w % 4 and take 32 columns each.
@@ -725,7 +727,7 @@ __device__ __forceinline__ void prep_role(const PrepParams<E>& P, uint8_t* smem_
   // T_L is zero above the diagonal and across chunks, and so is Gam here.
   if (ok) {
     const int t = tid >> 2, c0 = 16 * (tid & 3), cs = (t / C) * C;
-    const float bt = bta[t], lt = lam[t], gcp = gc[t / C] * bt, gs = gsuf[t];
+    const float bt = bta[t], lt = lam[t], gcp = -gc[t / C] * bt, gs = gsuf[t];
     float tl[16], ta[16], cp[16], cu[16];
     unpack8<E>(*reinterpret_cast<const uint4*>(sm + kOffX5 + sw128(t, c0)), tl);
     unpack8<E>(*reinterpret_cast<const uint4*>(sm + kOffX5 + sw128(t, c0 + 8)), tl + 8);
@@ -769,7 +771,7 @@ __device__ __forceinline__ void prep_role(const PrepParams<E>& P, uint8_t* smem_
     tmem_ld16(tmem + lane_base + (top ? 64 : 0) + c0, v);
     tmem_ld16(tmem + lane_base + (top ? 64 : 0) + c0 + 16, v + 16);
     tmem_wait_ld();
-    const float s = top ? -1.f : P.yscale;
+    const float s = top ? -P.yscale : P.yscale;
 #pragma unroll
     for (int e = 0; e < 32; ++e) v[e] *= s;
     const uint32_t dst = top ? kOffX1 : kOffX5;
@@ -783,10 +785,8 @@ __device__ __forceinline__ void prep_role(const PrepParams<E>& P, uint8_t* smem_
   // F1 = [cP; -W_M] K (TMEM columns 0..127), F2 = [cU; W_Y / sqrt(Dk)] V
   // (columns 128..255), issued by thread 0; F1 commits to bar_f1 (stream A),
   // F2 to bar_f2 (stream B: it also covers F1, issued before it).
-  if (ok && tid == 0) {
-    ok = mbar_wait(bar_v, it & 1);  // V of this tile has landed
-    fence_proxy_async();
-  }
+  if (ok && tid == 0) ok = mbar_wait(bar_v, it & 1);  // V of this tile has landed
+  if (io == 1) v_pending = false;  // (thread 0's wait covers it: F2 has read V by the stores)
   if (ok && tid == 0) {
     tc_fence_after();
     const uint32_t idf = idesc_e<E>(128, 128, false, true);
@@ -816,7 +816,7 @@ __device__ __forceinline__ void prep_role(const PrepParams<E>& P, uint8_t* smem_
     const int t = trow;
     const uint32_t src = tmem + lane_base + (streamA ? 0 : 128);
     const bool top = lrow < 64;
-    const float gt = gpw[t];
+    const float gt = gpw[t] * P.yscale;
     const int srow = streamA ? 2 * C * (t / C) + (t % C) + (top ? 0 : C) : t;
     const uint32_t sbuf = streamA ? kOffX0 : (top ? kOffV : kOffX4);
 #pragma unroll
@@ -846,7 +846,11 @@ __device__ __forceinline__ void prep_role(const PrepParams<E>& P, uint8_t* smem_
   tc_fence_before();  // the next tile's G1 rewrites these TMEM columns
   named_bar_sync(streamA ? streamA_id : streamB_id, 128);
   if (ok) {
-    if (io == 0) {  // A1 rows of the tile (Pt and Qh of each chunk)
+    if (io == 0) {
+      // K (read by F1) and Q (read by the Qh epilogue) are free: the next
+      // tile's come in while this tile's stores drain.
+      if (next < total) load_kq(next);
+      // A1 rows of the tile (Pt and Qh of each chunk)
       tma_store_3d(P.tm_a1o, sbase + kOffX0, 0, 0, (int)(tile_id * 128));
       bulk_commit();
     } else if (io == 1) {
@@ -857,16 +861,16 @@ __device__ __forceinline__ void prep_role(const PrepParams<E>& P, uint8_t* smem_
       bulk_commit();
     }
     unpublished = tile_id;
-    // K (read by F1) and Q (read by the Qh epilogue) are free: the next tile's
-    // come in while this tile's stores drain.
-    if (streamA && next < total) load_kq(next);
   }
   }  // tile loop
 
   gsync();
   if (ok && io >= 0) publish();  // the group's last tile
   if (io >= 0) bulk_wait_all();   // shared memory must outlive the stores' reads
-  cp_async_wait_all();            // and every copy into it must have landed
+  // and every load into it must have landed (loads issued for a tile the loop
+  // did not reach after a failed wait)
+  if (kq_pending) mbar_wait(bar_tma, it & 1);
+  if (v_pending) mbar_wait(bar_v, it & 1);
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x < 32) tmem_dealloc(tmem_base_sh, 256 * kPrepGroups);
@@ -874,14 +878,15 @@ __device__ __forceinline__ void prep_role(const PrepParams<E>& P, uint8_t* smem_
 
 template <int C, typename E>
 __global__ void __launch_bounds__(kPrepThreads, 1)
-prep_tc_kernel(const __grid_constant__ CUtensorMap tm_a1o, const __grid_constant__ CUtensorMap tm_uo,
-               const __grid_constant__ CUtensorMap tm_yo, const E* kin, const E* qin,
-               const E* vin, const E* __restrict__ g, const E* __restrict__ beta,
+prep_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_a1o,
+               const __grid_constant__ CUtensorMap tm_uo, const __grid_constant__ CUtensorMap tm_yo,
+               const E* __restrict__ g, const E* __restrict__ beta,
                float* __restrict__ wsGC, int T, int Hk, int Hv, int NT, int BH, int opts,
                float scale) {
   extern __shared__ uint8_t smem_raw[];
-  const PrepParams<E> P{kin, qin, vin, &tm_a1o, &tm_uo, &tm_yo, g, beta, wsGC,
-                     T, Hk, Hv, NT, BH, opts, scale};
+  const PrepParams<E> P{&tm_k, &tm_q, &tm_v, &tm_a1o, &tm_uo, &tm_yo, g, beta, wsGC,
+                        T, Hk, Hv, NT, BH, opts, scale};
   prep_role<C, E>(P, smem_raw, blockIdx.x, gridDim.x, nullptr);
 }
 
@@ -895,395 +900,368 @@ prep_tc_kernel(const __grid_constant__ CUtensorMap tm_a1o, const __grid_constant
 // the prep of later chunks.  Prep never waits for the scan and the launch is
 // cooperative (every CTA resident), so each wait ends.
 //
-// The scan role is the chunk update of scan_tc_kernel at R = 128:
-//   D = K^T Ut;  D += (-M^T) S^T;  Y = Qh S^T;  S <- G_C S + D^T,
-// with M^T = K^T Pt of chunk j+1 and D = K^T Ut of chunk j issued while the
-// state group finishes chunk j-1.  One S operand buffer: the state group
-// overwrites it only after Y of the chunk has completed.
+// The scan role carries S through the chunks in the form
+//   [Z | Y^T] = S [Pt; Qh]^T           (Z = S Pt^T; Y: step 7)
+//   D2 = Ut^T K + (-Z) K               (step 9 regrouped: Ut^T K - S Pt^T K = N - S M)
+//   S <- G_C S + D2
+//   y += Y / sqrt(Dk)                  (step 8, TMA reduction onto y_loc / sqrt(Dk))
+// with S itself held in tensor memory as the 16-bit A operand of the first
+// product (lane = value row) and -Z written back beside it as the A operand of
+// the last, so per chunk the tensor cores run 8 + 2 C/16 products, only
+// 8 + C/16 of them on the serial path, and no state operand passes through
+// shared memory.
 constexpr int kFusedThreads = kPrepThreads;  // 16 warps
 
-// Two rings of tile buffers: the MN ring (Pt, K, Ut: read by K^T [Pt | Ut],
-// released as soon as those products finish; two stages) and the Q ring (Qh,
-// later the staging of y; released after the y reduction has read it; three
-// stages, since it is held longer).
-struct Scan128Smem {
-  static constexpr uint32_t kOffP = 0;              // Pt, 2 x 64 rows x 128 B
-  static constexpr uint32_t kOffK = 16384;          // K,  2 x 64 rows x 128 B
-  static constexpr uint32_t kOffU = 32768;          // Ut, 2 x 64 rows x 128 B
-  static constexpr uint32_t kMN = 49152;
-  static constexpr uint32_t kQ = 16384;             // Qh, 2 x 64 rows x 128 B
-  static constexpr int kStagesMN = 2;
-  static constexpr int kStagesQ = 3;
-  static constexpr uint32_t kOffQ = kStagesMN * kMN;
-  static constexpr uint32_t kOffS = kOffQ + kStagesQ * kQ;   // S operand: 2 x 128 k-rows x 128 B
-
-  static constexpr uint32_t kOffGC = kOffS + 32768;          // G_C per Q stage (fp32 x 4)
-  static constexpr uint32_t kTotal = kOffGC + kStagesQ * 16 + 1024;
+// Shared memory of the scan: a ring of tile stages, each holding the tile's
+// A1 rows ([Pt; Qh] per chunk, two 64-column halves of 128 rows), its K rows
+// (two halves of 64 rows), its Ut rows (two halves of 64 rows), and the G_C of
+// its chunks.  A chunk's Qh rows, dead once [Z | Y^T] is complete, stage its
+// y reduction.
+struct ScanSmem {
+  static constexpr uint32_t kOffA1 = 0;
+  static constexpr uint32_t kOffK = 32768;
+  static constexpr uint32_t kOffU = 49152;
+  static constexpr uint32_t kStage = 65536;
+  static constexpr int kStages = 3;
+  static constexpr uint32_t kOffGC = kStages * kStage;  // fp32 x 4 per stage
+  static constexpr uint32_t kTotal = kOffGC + kStages * 16 + 1024;
 };
-constexpr uint32_t kFusedSmem = Scan128Smem::kTotal > kPrepSmem ? Scan128Smem::kTotal : kPrepSmem;
+constexpr uint32_t kFusedSmem = ScanSmem::kTotal > kPrepSmem ? ScanSmem::kTotal : kPrepSmem;
 
 enum : int {
-  kQFullMN = 0,
-  kQEmptyMN = kQFullMN + Scan128Smem::kStagesMN,  // MMA commit
-  kQFullQ = kQEmptyMN + Scan128Smem::kStagesMN,
-  kQEmptyQ = kQFullQ + Scan128Smem::kStagesQ,     // 257: state group + the y-reducing thread
-  kQKNorm = kQEmptyQ + Scan128Smem::kStagesQ,     // 128: K rows of the MN stage normalised
-  kQDs = kQKNorm + Scan128Smem::kStagesMN,
-  kQY,
-  kQM,                 // [2]
-  kQSop = kQM + 2,     // 256
-  kQDsFree,            // 256
-  kQMt,                // [2] 128
-  kQYFree = kQMt + 2,  // 128
-  kQYStaged,           // 128: Y of the chunk staged for the reduction
-  kQDN,                // D = K^T Ut of the chunk issued and complete
-  kQFin,               // 2: both issuers' last products complete
-  kNumQBars
+  kZFull = 0,                          // [stages] tile landed (TMA transaction count)
+  kZEmpty = kZFull + ScanSmem::kStages,  // [stages] 8 state warps (G_C read) + MMA commit + y reducer
+  kZKNorm = kZEmpty + ScanSmem::kStages, // [stages] 4 aux warps: the tile's K rows normalised
+  kZD1Full = kZKNorm + ScanSmem::kStages,  // [2] [Z | Y^T] of the chunk complete
+  kZD1Free = kZD1Full + 2,             // [2] 8 state warps (Z read) + 4 aux warps (Y read)
+  kZD2Full = kZD1Free + 2,             // Ut^T K + (-Z) K of the chunk complete
+  kZSReady,                            // 8 state warps: S_j in tensor memory
+  kZWReady,                            // 8 state warps: -Z of the chunk in tensor memory
+  kZYGo,                               // y of chunk j may be staged (the next chunk's product is issued)
+  kZDone,                              // the issuer's last products complete
+  kZNumBars
 };
 
+// Tensor-memory loads of N (8, 16, 32 or 64) columns and 16-bit pair stores of
+// N / 2 columns, chosen at compile time.
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, float* v) {
+  if constexpr (N == 8) {
+    tmem_ld8(taddr, v);
+  } else if constexpr (N == 16) {
+    tmem_ld16(taddr, v);
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; i += 32) tmem_ld32(taddr + i, v + i);
+  }
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t* r) {
+  if constexpr (N == 4) {
+    tmem_st4(taddr, r);
+  } else if constexpr (N == 8) {
+    tmem_st8(taddr, r);
+  } else if constexpr (N == 16) {
+    tmem_st16(taddr, r);
+  } else {
+    tmem_st32(taddr, r);
+  }
+}
+
+// The scan of head bh (one CTA, 512 threads):
+//   warp 0 lane 0   loads tile stages (after the tile's flag, in the fused launch)
+//   warp 1 lane 0   issues every product
+//   warps 2..9      state group: thread = (value row v, key half h) holds
+//                   S[v][64h .. 64h+63] in fp32 registers; writes -Z, updates S
+//                   and writes S back to tensor memory as the next A operand.
+//   warps 10..13    aux group: stages y of chunk j while the product of chunk
+//                   j+1 runs, normalises K tiles (option)
+// Tensor memory: [Z | Y^T] double-buffered at columns 0 and 128 (2C columns
+// each), D2 at 256 (128 columns), S (16-bit pairs) at 384 (64 columns), -Z
+// (16-bit pairs) at 448 (C / 2 columns).
 template <int C, typename E>
-__device__ __forceinline__ void scan_role128(const CUtensorMap* tm_a1c, const CUtensorMap* tm_k,
-                                             const CUtensorMap* tm_uy, const CUtensorMap* tm_yred,
-                                             const float* wsGC, const int* flags,
-                                             const float* state_in, float* state_out, int T,
-                                             int Hk, int Hv, int NT, int bh, int opts,
-                                             float scale, uint8_t* smem_raw) {
-  using SM = Scan128Smem;
-  constexpr int kCt = kTile / C;
+__device__ __forceinline__ void scan_role(const CUtensorMap* tm_a1c, const CUtensorMap* tm_k,
+                                          const CUtensorMap* tm_uc, const CUtensorMap* tm_yred,
+                                          const float* wsGC, const int* flags,
+                                          const float* state_in, float* state_out, int T,
+                                          int Hk, int Hv, int NT, int bh, int opts, float scale,
+                                          uint8_t* smem_raw) {
+  using SM = ScanSmem;
+  constexpr int kCt = kTile / C;  // chunks per tile
+  constexpr int kZc = C / 2;      // Z columns of each state thread
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~(uintptr_t)1023);
-  __shared__ uint64_t qbars[kNumQBars];
-  __shared__ uint32_t qtmem_sh;
+  __shared__ uint64_t zbars[kZNumBars];
+  __shared__ uint32_t tmem_sh;
   const uint32_t sbase = smem_u32(sm);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = bh / Hv, hv = bh - b * Hv, hk = key_head(hv, Hk, Hv, opts);
   const int NC = (T + C - 1) / C;
-  auto bar = [&](int i) { return smem_u32(&qbars[i]); };
+  const bool knorm = (opts & kOptL2NormQK) != 0;
+  auto bar = [&](int i) { return smem_u32(&zbars[i]); };
 
   if (tid == 0) {
-    for (int s = 0; s < SM::kStagesMN; ++s) {
-      mbar_init(bar(kQFullMN + s), 1);
-      mbar_init(bar(kQEmptyMN + s), 1);
-      mbar_init(bar(kQKNorm + s), 128);
+    for (int s = 0; s < SM::kStages; ++s) {
+      mbar_init(bar(kZFull + s), 1);
+      mbar_init(bar(kZEmpty + s), 10);
+      mbar_init(bar(kZKNorm + s), 4);
     }
-    for (int s = 0; s < SM::kStagesQ; ++s) {
-      mbar_init(bar(kQFullQ + s), 1);
-      mbar_init(bar(kQEmptyQ + s), 257);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(kZD1Full + x), 1);
+      mbar_init(bar(kZD1Free + x), 12);
     }
-    mbar_init(bar(kQDs), 1);
-    mbar_init(bar(kQY), 1);
-    mbar_init(bar(kQM), 1);
-    mbar_init(bar(kQM + 1), 1);
-    mbar_init(bar(kQSop), 256);
-    mbar_init(bar(kQDsFree), 256);
-    mbar_init(bar(kQMt), 128);
-    mbar_init(bar(kQMt + 1), 128);
-    mbar_init(bar(kQYFree), 128);
-    mbar_init(bar(kQYStaged), 128);
-    mbar_init(bar(kQDN), 1);
-    mbar_init(bar(kQFin), 2);
+    mbar_init(bar(kZD2Full), 1);
+    mbar_init(bar(kZSReady), 8);
+    mbar_init(bar(kZWReady), 8);
+    mbar_init(bar(kZYGo), 1);
+    mbar_init(bar(kZDone), 1);
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&qtmem_sh), 512);
+    tmem_alloc(smem_u32(&tmem_sh), 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = qtmem_sh;
-  const uint32_t tD = tmem, tY = tmem + 384;
-  auto tM = [&](int x) { return tmem + 128 + 128 * x; };  // fp32 M^T; cols 0-63 then -M^T bf16
-  const uint32_t sS = sbase + SM::kOffS;
-  auto ring_mn = [&](int j) { return (j / kCt) % SM::kStagesMN; };
-  auto ring_q = [&](int j) { return (j / kCt) % SM::kStagesQ; };
-  auto mn_addr = [&](int j) { return sbase + ring_mn(j) * SM::kMN; };
-  auto q_addr = [&](int j) { return sbase + SM::kOffQ + ring_q(j) * SM::kQ; };
+  const uint32_t tmem = tmem_sh;
+  auto tD1 = [&](int x) { return tmem + 128u * (uint32_t)x; };
+  const uint32_t tD2 = tmem + 256, tS = tmem + 384, tW = tmem + 448;
   auto last_of_tile = [&](int j) { return (j % kCt) == kCt - 1 || j == NC - 1; };
-  auto wait_mn = [&](int j) {
-    const int n = j / kCt;
-    return mbar_wait(bar(kQFullMN + n % SM::kStagesMN), (n / SM::kStagesMN) & 1);
-  };
-  // With L2-normalised keys the aux group rewrites each K tile first.
-  const bool knorm = (opts & kOptL2NormQK) != 0;
-  auto wait_knorm = [&](int j) {
-    const int n = j / kCt;
-    return mbar_wait(bar(kQKNorm + n % SM::kStagesMN), (n / SM::kStagesMN) & 1);
-  };
-  auto wait_q = [&](int j) {
-    const int n = j / kCt;
-    return mbar_wait(bar(kQFullQ + n % SM::kStagesQ), (n / SM::kStagesQ) & 1);
-  };
 
-  if ((warp == 0 || warp == 14) && lane == 0) {
-    // ---------------------- producers (MN ring, Q ring) ----------------------
-    const bool mn = warp == 0;
-    const int full0 = mn ? kQFullMN : kQFullQ, empty0 = mn ? kQEmptyMN : kQEmptyQ;
-    prefetch_tmap(tm_a1c);
-    if (mn) {
-      prefetch_tmap(tm_k);
-      prefetch_tmap(tm_uy);
-    }
-    const int stages = mn ? SM::kStagesMN : SM::kStagesQ;
-    int n = 0;
-    for (; n < NT; ++n) {
-      const int s = n % stages;
-      if (n >= stages && !mbar_wait(bar(empty0 + s), ((n / stages) - 1) & 1)) break;
-      const size_t tid_ws = (size_t)bh * NT + n;
-      if (flags) {
-        if (!wait_flag(flags + tid_ws, kTilePublished)) break;
-        fence_proxy_async_global();
-      }
-      const uint32_t fb = bar(full0 + s);
-      const int row = (int)(tid_ws * 128);
-      if (mn) {
-        const uint32_t st = sbase + s * SM::kMN;
-        mbar_expect_tx(fb, SM::kMN);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int c = 0; c < kCt; ++c)  // Pt rows of chunk c
-            tma_load_2d(st + SM::kOffP + h * 8192 + c * C * 128, tm_a1c, fb, 64 * h,
-                        row + 2 * C * c);
-          tma_load_4d(st + SM::kOffK + h * 8192, tm_k, fb, 64 * h, hk, n * kTile, b);
-          tma_load_2d(st + SM::kOffU + h * 8192, tm_uy, fb, 64 * h, (int)(tid_ws * kTile));
-        }
-      } else {
-        const uint32_t st = sbase + SM::kOffQ + s * SM::kQ;
-        mbar_expect_tx(fb, SM::kQ + 16);
-        bulk_load(sbase + SM::kOffGC + 16 * s, wsGC + tid_ws * 4, 16, fb);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int c = 0; c < kCt; ++c)  // Qh rows of chunk c
-            tma_load_2d(st + h * 8192 + c * C * 128, tm_a1c, fb, 64 * h, row + 2 * C * c + C);
-        }
-      }
-    }
-    for (int m = (n > stages ? n - stages : 0); m < n; ++m)
-      mbar_wait(bar(full0 + m % stages), (m / stages) & 1);
-  } else if (warp == 1 || warp == 15) {
-    // ---------------------------- MMA issuers ----------------------------
-    // Two threads issue the products, so that the serial one is not queued
-    // behind the others: warp 1 issues D += (-M^T) S^T only; warp 15 issues
-    // Y^T = S Qh^T (which needs only the chunk-start state), M^T of the next
-    // chunk and D = K^T Ut of the next chunk.  They are ordered through
-    // mbarriers: D_S(j) waits for D_N(j) (same accumulator); D_N(j+1) waits
-    // until the state group has read D(j); M^T(j+1) overwrites the TMEM operand
-    // of D_S(j-1), complete once the S operand of chunk j is written.
+  if (warp == 0) {
+    // ------------------------------ producer ------------------------------
     if (lane == 0) {
-      const uint32_t id_kt = idesc_e<E>(128, 128, true, true);   // K^T x (Pt | Ut)
-      const uint32_t id_s = idesc_e<E>(128, 128, false, true);   // (-M^T) x S^T
-      const uint32_t id_y = idesc_e<E>(128, C, true, false);     // S x Qh^T (rows v, cols t)
-      // Descriptor bases (per ring stage via a byte offset; see SmemDesc).
-      const SmemDesc d_mn_mn = smem_desc_base(sbase, 8192, 1024, kSw128);   // MN-major, 64-row halves
-      const SmemDesc d_s = smem_desc_base(sS, 16384, 1024, kSw128);         // S operand
-      const SmemDesc d_q = smem_desc_base(sbase + SM::kOffQ, 16, 1024, kSw128);  // Qh, K-major
-      bool ok = true;
-      if (warp == 1) {
-        for (int j = 0; j < NC && ok; ++j) {
-          // D += (-M^T) S^T   (the serial step), on D = K^T Ut of the chunk
-          if (!(ok = mbar_wait(bar(kQDN), j & 1))) break;
-          if (!(ok = mbar_wait(bar(kQSop), j & 1))) break;
-          if (!(ok = mbar_wait(bar(kQMt + (j & 1)), (j >> 1) & 1))) break;
-          tc_fence_after();
-          const uint32_t ta = tM(j & 1);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_f16_ts(tD, ta + 8 * kk, smem_desc_at(d_s, kk * 2048), id_s, 1);
-          mma_commit(bar(kQDs));
+      prefetch_tmap(tm_a1c);
+      prefetch_tmap(tm_k);
+      prefetch_tmap(tm_uc);
+      int n = 0;
+      for (; n < NT; ++n) {
+        const int s = n % SM::kStages;
+        if (n >= SM::kStages && !mbar_wait(bar(kZEmpty + s), ((n / SM::kStages) - 1) & 1)) break;
+        const size_t tile = (size_t)bh * NT + n;
+        if (flags) {
+          if (!wait_flag(flags + tile, kTilePublished)) break;
+          fence_proxy_async_global();
         }
-      } else {
-        // M^T of chunk j into tM(j & 1), once its tile's MN buffers have landed.
-        auto issue_mt = [&](int j) {
-          if (j % kCt == 0) {
-            if (!(knorm ? wait_knorm(j) : wait_mn(j))) return false;
-            tc_fence_after();
-          }
-          const uint32_t off = ring_mn(j) * SM::kMN + (j % kCt) * C * 128;
+        const uint32_t fb = bar(kZFull + s), st = sbase + s * SM::kStage;
+        mbar_expect_tx(fb, SM::kStage + 16);
+        bulk_load(sbase + SM::kOffGC + 16 * s, wsGC + tile * 4, 16, fb);
 #pragma unroll
-          for (int kk = 0; kk < C / 16; ++kk)
-            mma_f16_ss(tM(j & 1), smem_desc_at(d_mn_mn, off + SM::kOffK + kk * 2048),
-                        smem_desc_at(d_mn_mn, off + SM::kOffP + kk * 2048), id_kt, kk > 0);
-          mma_commit(bar(kQM + (j & 1)));
-          return true;
-        };
-        // D = K^T Ut of chunk j into tD (after M^T(j): its MN buffers have landed).
-        auto issue_dn = [&](int j) {
-          tc_fence_after();
-          const uint32_t off = ring_mn(j) * SM::kMN + (j % kCt) * C * 128;
-#pragma unroll
-          for (int kk = 0; kk < C / 16; ++kk)
-            mma_f16_ss(tD, smem_desc_at(d_mn_mn, off + SM::kOffK + kk * 2048),
-                        smem_desc_at(d_mn_mn, off + SM::kOffU + kk * 2048), id_kt, kk > 0);
-          mma_commit(bar(kQDN));
-          // The tile's MN buffers are free once its last products finish.
-          if (last_of_tile(j)) mma_commit(bar(kQEmptyMN + ring_mn(j)));
-        };
-        if (NC > 0) {
-          ok = issue_mt(0);
-          if (ok) issue_dn(0);
-        }
-        for (int j = 0; j < NC && ok; ++j) {
-          const int c = j % kCt;
-          // Y^T = S Qh^T (A = the S operand read MN-major, B = Qh rows): the state
-          // group rewrites S once it completes.
-          if (!(ok = mbar_wait(bar(kQSop), j & 1))) break;
-          if (c == 0 && !(ok = wait_q(j))) break;
-          if (j > 0 && !(ok = mbar_wait(bar(kQYFree), (j - 1) & 1))) break;
-          tc_fence_after();
-          const uint32_t qoff = ring_q(j) * SM::kQ + c * C * 128;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_f16_ss(tY, smem_desc_at(d_s, kk * 2048),
-                        smem_desc_at(d_q, qoff + (kk >> 2) * 8192 + (kk & 3) * 32), id_y, kk > 0);
-          mma_commit(bar(kQY));
-          if (j + 1 < NC) {
-            // M^T of chunk j+1, converted by the aux group while chunk j finishes.
-            if (!(ok = issue_mt(j + 1))) break;
-            // D = K^T Ut of chunk j+1 once chunk j's D has been read.
-            if (!(ok = mbar_wait(bar(kQDsFree), j & 1))) break;
-            issue_dn(j + 1);
-          }
+        for (int h = 0; h < 2; ++h) {
+          tma_load_2d(st + SM::kOffA1 + h * 16384, tm_a1c, fb, 64 * h, (int)(tile * 128));
+          tma_load_4d(st + SM::kOffK + h * 8192, tm_k, fb, 64 * h, hk, n * kTile, b);
+          tma_load_2d(st + SM::kOffU + h * 8192, tm_uc, fb, 64 * h, (int)(tile * kTile));
         }
       }
-      mma_commit(bar(kQFin));
-      mbar_wait(bar(kQFin), 0);
+      // The stages still in flight land before the CTA ends.
+      for (int m = (n > SM::kStages ? n - SM::kStages : 0); m < n; ++m)
+        mbar_wait(bar(kZFull + m % SM::kStages), (m / SM::kStages) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------- issuer -------------------------------
+    // Per chunk: [Z | Y^T] = S [Pt; Qh]^T once S_j is in tensor memory;
+    // D2 = Ut^T K right after it (D2 of the previous chunk has been read by
+    // then); D2 += (-Z) K once -Z is in tensor memory.
+    if (lane == 0) {
+      const uint32_t id_z = idesc_e<E>(128, 2 * C, false, false);  // S (TMEM) x [Pt; Qh]^T
+      const uint32_t id_n = idesc_e<E>(128, 128, true, true);      // Ut^T x K (both MN-major)
+      const uint32_t id_w = idesc_e<E>(128, 128, false, true);     // (-Z) (TMEM) x K
+      const SmemDesc d_a1 = smem_desc_base(sbase + SM::kOffA1, 16, 1024, kSw128);  // K-major rows
+      const SmemDesc d_mn = smem_desc_base(sbase, 8192, 1024, kSw128);  // MN-major 64-col halves
+      bool ok = true;
+      for (int j = 0; j < NC && ok; ++j) {
+        const int c = j % kCt, n = j / kCt, st = n % SM::kStages;
+        if (c == 0 && !(ok = mbar_wait(bar(kZFull + st), (n / SM::kStages) & 1))) break;
+        if (j >= 2 && !(ok = mbar_wait(bar(kZD1Free + (j & 1)), ((j >> 1) - 1) & 1))) break;
+        if (!(ok = mbar_wait_poll(bar(kZSReady), j & 1))) break;
+        tc_fence_after();
+        const uint32_t aoff = st * SM::kStage + 2 * C * c * 128;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_f16_ts(tD1(j & 1), tS + 8 * kk,
+                     smem_desc_at(d_a1, aoff + (kk >> 2) * 16384 + (kk & 3) * 32), id_z, kk > 0);
+        mma_commit(bar(kZD1Full + (j & 1)));
+        if (j > 0) mbar_arrive(bar(kZYGo));  // y of chunk j-1 may be staged now
+        if (knorm && c == 0 && !(ok = mbar_wait(bar(kZKNorm + st), (n / SM::kStages) & 1))) break;
+        tc_fence_after();
+        const uint32_t toff = st * SM::kStage + c * C * 128;  // token row c C of the tile
+#pragma unroll
+        for (int kk = 0; kk < C / 16; ++kk)
+          mma_f16_ss(tD2, smem_desc_at(d_mn, toff + SM::kOffU + kk * 2048),
+                     smem_desc_at(d_mn, toff + SM::kOffK + kk * 2048), id_n, kk > 0);
+        if (!(ok = mbar_wait_poll(bar(kZWReady), j & 1))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < C / 16; ++kk)
+          mma_f16_ts(tD2, tW + 8 * kk, smem_desc_at(d_mn, toff + SM::kOffK + kk * 2048), id_w, 1);
+        mma_commit(bar(kZD2Full));
+        if (last_of_tile(j)) mma_commit(bar(kZEmpty + st));
+        if (j == NC - 1) mbar_arrive(bar(kZYGo));  // y of the last chunk
+      }
+      // Every product issued has completed before the tensor memory is freed.
+      mma_commit(bar(kZDone));
+      mbar_wait(bar(kZDone), 0);
     }
     __syncwarp();
   } else if (warp >= 2 && warp < 10) {
-    // ----------------------------- state group ----------------------------
-    // Thread = TMEM lane k (key column); value rows 64h .. 64h+63.
+    // ---------------------------- state group -----------------------------
     const int q = warp & 3, h = (warp - 2) >> 2;
-    const int L = q * 32 + lane;
-    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    const size_t sidx = ((size_t)bh * kD + 64 * h) * kD + L;
-    bool ok = true;
+    const int v = 32 * q + lane;
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    float* srow_out = state_out + ((size_t)bh * kD + v) * kD + 64 * h;
     float s[64];
+    if (state_in) {
+      const float4* src = reinterpret_cast<const float4*>(state_in + ((size_t)bh * kD + v) * kD +
+                                                          64 * h);
 #pragma unroll
-    for (int r = 0; r < 64; ++r) s[r] = state_in ? state_in[sidx + (size_t)r * kD] : 0.f;
-    auto write_op = [&]() {
-      uint8_t* row = sm + SM::kOffS + h * 16384;
+      for (int i = 0; i < 16; ++i) {
+        const float4 x = src[i];
+        s[4 * i] = x.x;
+        s[4 * i + 1] = x.y;
+        s[4 * i + 2] = x.z;
+        s[4 * i + 3] = x.w;
+      }
+    } else {
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) st_sm16(row, sw128(L, 8 * ch), pack8<E>(s + 8 * ch));
-      fence_proxy_async();
-      mbar_arrive(bar(kQSop));
+      for (int i = 0; i < 64; ++i) s[i] = 0.f;
+    }
+    // S (16-bit pairs) into tensor memory, then one arrival per warp.
+    auto write_s = [&]() {
+      uint32_t p[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) p[i] = pack2<E>(s[2 * i], s[2 * i + 1]);
+      tmem_st32(tS + lane_base + 32 * h, p);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kZSReady));
     };
-    write_op();
+    write_s();
+    bool ok = true;
     for (int j = 0; j < NC; ++j) {
-      const int c = j % kCt;
-      if (c == 0 && !(ok = wait_q(j))) break;
-      const float Gc = ld_shared_f32(sbase + SM::kOffGC + 16 * ring_q(j) + 4 * c);
-      if (last_of_tile(j)) mbar_arrive(bar(kQEmptyQ + ring_q(j)));
-      if (!(ok = mbar_wait(bar(kQDs), j & 1))) break;
+      const int c = j % kCt, n = j / kCt, st = n % SM::kStages;
+      // -Z (tokens t = c C + h C/2 + i, i < C/2: this thread's columns) to
+      // tensor memory as the A operand of D2 += (-Z) K.
+      if (c == 0) ok = ok && mbar_wait(bar(kZFull + st), (n / SM::kStages) & 1);
+      ok = ok && mbar_wait_poll(bar(kZD1Full + (j & 1)), (j >> 1) & 1);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      float z[kZc];
+      tmem_ld_n<kZc>(tD1(j & 1) + lane_base + kZc * h, z);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kZD1Free + (j & 1)));
+      uint32_t w[kZc / 2];
+#pragma unroll
+      for (int i = 0; i < kZc; i += 2) w[i / 2] = pack2<E>(z[i], z[i + 1]);
+      tmem_st_n<kZc / 2>(tW + lane_base + (kZc / 2) * h, w);
+      const float gcv = ld_shared_f32(sbase + SM::kOffGC + 16 * st + 4 * c);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(kZWReady));
+        if (last_of_tile(j)) mbar_arrive(bar(kZEmpty + st));  // done with the stage's G_C
+      }
+      // S <- G_C S + D2; S_{j+1} to tensor memory as the next A operand.
+      ok = mbar_wait_poll(bar(kZD2Full), j & 1);
+      if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      for (int hh = 0; hh < 2; ++hh) {
         float d[32];
-        tmem_ld32(tD + lane_base + 64 * h + 32 * half, d);
+        tmem_ld32(tD2 + lane_base + 64 * h + 32 * hh, d);
         tmem_wait_ld();
 #pragma unroll
-        for (int r = 0; r < 32; ++r) s[32 * half + r] = fmaf(Gc, s[32 * half + r], d[r]);
+        for (int r = 0; r < 32; ++r) s[32 * hh + r] = fmaf(gcv, s[32 * hh + r], d[r]);
       }
-      tc_fence_before();
-      mbar_arrive(bar(kQDsFree));
-      if (j + 1 < NC) {
-        // Y of chunk j still reads the S operand.
-        if (!(ok = mbar_wait(bar(kQY), j & 1))) break;
-        write_op();
-      }
+      if (j + 1 < NC) write_s();
     }
     if (ok) {
+      float4* dst = reinterpret_cast<float4*>(srow_out);
 #pragma unroll
-      for (int r = 0; r < 64; ++r) state_out[sidx + (size_t)r * kD] = s[r];
+      for (int i = 0; i < 16; ++i)
+        dst[i] = make_float4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]);
     }
   } else if (warp >= 10 && warp < 14) {
     // ------------------------------ aux group -----------------------------
-    const int qd = warp & 3;
-    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+    const int q = warp & 3;
+    const bool reducer = warp == 10 && lane == 0;
+    const int atid = tid - 320;  // 0..127
     bool ok = true;
-    auto convert = [&](int j) {
-      if (!mbar_wait(bar(kQM + (j & 1)), (j >> 1) & 1)) return false;
-      tc_fence_after();
-      const uint32_t tb = tM(j & 1) + lane_base;
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float v[64];
-        tmem_ld32(tb + 64 * hh, v);
-        tmem_ld32(tb + 64 * hh + 32, v + 32);
-        tmem_wait_ld();
-        uint32_t p[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) p[i] = pack2<E>(-v[2 * i], -v[2 * i + 1]);
-        tmem_st32(tb + 32 * hh, p);
+    for (int j = 0; j < NC; ++j) {
+      const int c = j % kCt, n = j / kCt, st = n % SM::kStages;
+      if (c == 0) ok = ok && mbar_wait(bar(kZFull + st), (n / SM::kStages) & 1);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok && knorm && c == 0) {
+        // The tile's K rows as x / |x| (two threads a row), before W K reads them.
+        l2norm_row_sw128<E>(sm + st * SM::kStage + SM::kOffK, 8192, atid >> 1, atid & 1);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kZKNorm + st));
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(kQMt + (j & 1)));
-      return true;
-    };
-    // Normalise the K rows of the tile holding chunk j (64 rows, two threads
-    // per row), then release it to the issuer.
-    const int atid = tid - 320;  // 0..127 in the aux group
-    auto normalise_k = [&](int j) {
-      if (!wait_mn(j)) return false;
-      l2norm_row_sw128<E>(sm + (mn_addr(j) - sbase) + SM::kOffK, 8192, atid >> 1, atid & 1);
-      fence_proxy_async();
-      mbar_arrive(bar(kQKNorm + ring_mn(j)));
-      return true;
-    };
-    if (knorm && NC > 0) ok = normalise_k(0);
-    if (ok && NC > 0) ok = convert(0);
-    for (int j = 0; j < NC && ok; ++j) {
-      const int c = j % kCt;
-      if (knorm && j + 1 < NC && (j + 1) % kCt == 0 && !(ok = normalise_k(j + 1))) break;
-      if (j + 1 < NC && !(ok = convert(j + 1))) break;
-      // Y^T: lane v (value row), columns t < C.  Y / sqrt(Dk) goes, as bf16 and
-      // transposed, into this chunk's Qh rows (dead once Y is complete) and is
-      // added to y (which holds y_loc / sqrt(Dk)) by a TMA reduction.
-      const int v = 32 * qd + lane;
-      const uint32_t qst = q_addr(j);
-      uint8_t* hbase = sm + (qst - sbase) + (v >> 6) * 8192;
-      const int vv = v & 63;
-      if (!(ok = mbar_wait(bar(kQY), j & 1))) break;
-      tc_fence_after();
+      if (ok) ok = mbar_wait(bar(kZYGo), j & 1);
+      if (ok) ok = mbar_wait(bar(kZD1Full + (j & 1)), (j >> 1) & 1);
+      ok = __all_sync(0xffffffffu, ok);
+      const uint32_t yoff = st * SM::kStage + SM::kOffA1 + (2 * C * c + C) * 128;
+      if (ok) {
+        tc_fence_after();
+        // Y^T (lanes v, columns t; already / sqrt(Dk): Qh is stored scaled) in
+        // 16 x 8 fragments: block (lh, cb) covers lanes 32q + 16 lh .. + 15 and
+        // tokens 8 cb .. 8 cb + 7.
+        constexpr int kCb = C / 8;
+        float yv[2][kCb][4];
 #pragma unroll
-      for (int t0 = 0; t0 < C; t0 += 32) {
-        float d[32];
-        if constexpr (C >= 32) {
-          tmem_ld32(tY + lane_base + t0, d);
-        } else {
-          tmem_ld16(tY + lane_base + t0, d);
-        }
+        for (int lh = 0; lh < 2; ++lh)
+#pragma unroll
+          for (int cb = 0; cb < kCb; ++cb)
+            tmem_ld_16x256b(tD1(j & 1) + ((uint32_t)(32 * q + 16 * lh) << 16) + C + 8 * cb,
+                            yv[lh][cb]);
         tmem_wait_ld();
-        if (t0 + 32 >= C) {
-          tc_fence_before();
-          mbar_arrive(bar(kQYFree));
-        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kZD1Free + (j & 1)));
+        // Stored transposed into the chunk's Qh rows, the box layout of the y
+        // reduction (C token rows of 128 bytes per 64-column half): each 8 x 8
+        // block becomes 8 token rows of 8 consecutive values (16 bytes).
+        const int mi = lane >> 3, r8 = lane & 7;
 #pragma unroll
-        for (int i = 0; i < (C < 32 ? C : 32); ++i) {
-          const int row = c * C + t0 + i;
-          const uint32_t off = row * 128 + ((((vv >> 3) ^ (row & 7))) << 4) + (vv & 7) * 2;
-          *reinterpret_cast<E*>(hbase + off) = ElemT<E>::from(d[i] * scale);
+        for (int lh = 0; lh < 2; ++lh) {
+          const int v0 = 32 * q + 16 * lh + 8 * (mi & 1);
+          const uint32_t hbase = sbase + yoff + (v0 >> 6) * 16384;
+#pragma unroll
+          for (int cb = 0; cb < kCb; cb += 2) {
+            const int t = 8 * (cb + (mi >> 1)) + r8;
+            const uint32_t addr = hbase + t * 128 + ((((v0 & 63) >> 3) ^ (t & 7)) << 4);
+            stmatrix_x4_trans(addr, pack2<E>(yv[lh][cb][0], yv[lh][cb][1]),
+                              pack2<E>(yv[lh][cb][2], yv[lh][cb][3]),
+                              pack2<E>(yv[lh][cb + 1][0], yv[lh][cb + 1][1]),
+                              pack2<E>(yv[lh][cb + 1][2], yv[lh][cb + 1][3]));
+          }
         }
+        fence_proxy_async();
       }
-      fence_proxy_async();
-      mbar_arrive(bar(kQYStaged));
-      if (warp == 10 && lane == 0) {
-        if (!(ok = mbar_wait(bar(kQYStaged), j & 1))) break;
+      ok = named_bar_and(3, 128, ok);
+      if (!ok) break;
+      if (reducer) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh)
-          tma_reduce_add_4d(tm_yred, qst + hh * 8192 + c * C * 128, 64 * hh, hv, j * C, b);
+          tma_reduce_add_4d(tm_yred, sbase + yoff + hh * 16384, 64 * hh, hv, j * C, b);
         bulk_commit();
-        bulk_wait_read_all();  // the Q buffers may be refilled once the reduction has read them
-        if (last_of_tile(j)) mbar_arrive(bar(kQEmptyQ + ring_q(j)));
+        if (last_of_tile(j)) {  // the stage may be refilled once the reductions have read it
+          bulk_wait_read_all();
+          mbar_arrive(bar(kZEmpty + st));
+        }
       }
+      __syncwarp();
     }
-    if (warp == 10 && lane == 0) bulk_wait_all();
+    if (reducer) bulk_wait_all();
   }
-  // the idle lanes of warps 0 and 14 have no scan work
   tc_fence_before();
-  if (warp != 0 && warp != 14) named_bar_sync(1, kFusedThreads - 64);
+  __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
@@ -1297,18 +1275,17 @@ fused_prefill_kernel(const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_yred,
                      const __grid_constant__ CUtensorMap tm_a1o,
                      const __grid_constant__ CUtensorMap tm_uo,
-                     const __grid_constant__ CUtensorMap tm_yo, const E* kin,
-                     const E* qin, const E* vin, const E* __restrict__ g,
+                     const __grid_constant__ CUtensorMap tm_yo, const E* __restrict__ g,
                      const E* __restrict__ beta, float* __restrict__ wsGC, int* flags,
                      const float* state_in, float* state_out, int T, int Hk, int Hv, int NT,
                      int BH, int opts, float scale) {
   extern __shared__ uint8_t smem_raw[];
   if ((int)blockIdx.x < BH) {
-    scan_role128<C, E>(&tm_a1s, &tm_k, &tm_us, &tm_yred, wsGC, flags, state_in, state_out, T, Hk,
+    scan_role<C, E>(&tm_a1s, &tm_k, &tm_us, &tm_yred, wsGC, flags, state_in, state_out, T, Hk,
                     Hv, NT, blockIdx.x, opts, scale, smem_raw);
   } else {
-    const PrepParams<E> P{kin, qin, vin, &tm_a1o, &tm_uo, &tm_yo, g, beta, wsGC,
-                       T, Hk, Hv, NT, BH, opts, scale};
+    const PrepParams<E> P{&tm_k, &tm_q, &tm_v, &tm_a1o, &tm_uo, &tm_yo, g, beta, wsGC,
+                          T, Hk, Hv, NT, BH, opts, scale};
     prep_role<C, E>(P, smem_raw, blockIdx.x - BH, gridDim.x - BH, flags);
   }
 }
@@ -1322,7 +1299,7 @@ scan_head_kernel(const __grid_constant__ CUtensorMap tm_a1s, const __grid_consta
                  const float* state_in, float* state_out, int T, int Hk, int Hv, int NT,
                  int opts, float scale) {
   extern __shared__ uint8_t smem_raw[];
-  scan_role128<C, E>(&tm_a1s, &tm_k, &tm_us, &tm_yred, wsGC, nullptr, state_in, state_out, T, Hk,
+  scan_role<C, E>(&tm_a1s, &tm_k, &tm_us, &tm_yred, wsGC, nullptr, state_in, state_out, T, Hk,
                   Hv, NT, blockIdx.x, opts, scale, smem_raw);
 }
 
@@ -1436,7 +1413,7 @@ cudaError_t launch_c(const PrefillArgs& a) {
   if (!make_bthd_map(&tk, dt, a.k, a.B, a.T, a.Hk) ||
       !make_bthd_map(&tq, dt, a.q, a.B, a.T, a.Hk) ||
       !make_bthd_map(&tv, dt, a.v, a.B, a.T, a.Hv) ||
-      !make_rows_map(&ta1s, dt, wsA1, (size_t)BH * NT * 128, 64, C, true) ||
+      !make_rows_map(&ta1s, dt, wsA1, (size_t)BH * NT * 128, 64, 128, true) ||
       !make_rows_map(&tus, dt, wsU, (size_t)BH * NT * kTile, 64, 64, true) ||
       !make_bthd_map(&tyred, dt, a.y, a.B, a.T, a.Hv, C) ||
       !make_rows_halves_map(&ta1o, dt, wsA1, (size_t)BH * NT * 128, 128) ||
@@ -1446,9 +1423,6 @@ cudaError_t launch_c(const PrefillArgs& a) {
 
   const float scale = 1.0f / sqrtf((float)kD);
   const int sms = num_sms();
-  const E* k = static_cast<const E*>(a.k);
-  const E* q = static_cast<const E*>(a.q);
-  const E* v = static_cast<const E*>(a.v);
   const E* g = static_cast<const E*>(a.g);
   const E* beta = static_cast<const E*>(a.beta);
   cudaError_t e;
@@ -1471,7 +1445,7 @@ cudaError_t launch_c(const PrefillArgs& a) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, fused_prefill_kernel<C, E>, tk, tq, tv, ta1s, tus, tyred, ta1o,
-                              tuo, tyo, k, q, v, g, beta, wsGC, flags, a.state_in, a.state_out,
+                              tuo, tyo, g, beta, wsGC, flags, a.state_in, a.state_out,
                               a.T, a.Hk, a.Hv, NT, BH, a.options, scale);
   }
 
@@ -1480,14 +1454,14 @@ cudaError_t launch_c(const PrefillArgs& a) {
                            kPrepSmem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(scan_head_kernel<C, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Scan128Smem::kTotal);
+                             ScanSmem::kTotal);
   if (e != cudaSuccess) return e;
   const int prep_ctas = std::min(sms, (BH * NT + kPrepGroups - 1) / kPrepGroups);
   prep_tc_kernel<C, E><<<prep_ctas, kPrepThreads, kPrepSmem, a.stream>>>(
-      ta1o, tuo, tyo, k, q, v, g, beta, wsGC, a.T, a.Hk, a.Hv, NT, BH, a.options, scale);
+      tk, tq, tv, ta1o, tuo, tyo, g, beta, wsGC, a.T, a.Hk, a.Hv, NT, BH, a.options, scale);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  scan_head_kernel<C, E><<<BH, kFusedThreads, Scan128Smem::kTotal, a.stream>>>(
+  scan_head_kernel<C, E><<<BH, kFusedThreads, ScanSmem::kTotal, a.stream>>>(
       ta1s, tk, tus, tyred, wsGC, a.state_in, a.state_out, a.T, a.Hk, a.Hv, NT, a.options,
       scale);
   return cudaGetLastError();
