@@ -915,22 +915,25 @@ constexpr int kFusedThreads = kPrepThreads;  // 16 warps
 // Shared memory of the scan: a ring of tile stages, each holding the tile's
 // A1 rows ([Pt; Qh] per chunk, two 64-column halves of 128 rows), its K rows
 // (two halves of 64 rows), its Ut rows (two halves of 64 rows), and the G_C of
-// its chunks.  A chunk's Qh rows, dead once [Z | Y^T] is complete, stage its
-// y reduction.
+// its chunks; and two y staging buffers (chunk parity), each C token rows of
+// 128 bytes per 64-column half, the box layout of the y reduction.  A stage is
+// free once its chunks' products are done and their G_C has been read.
 struct ScanSmem {
   static constexpr uint32_t kOffA1 = 0;
   static constexpr uint32_t kOffK = 32768;
   static constexpr uint32_t kOffU = 49152;
   static constexpr uint32_t kStage = 65536;
   static constexpr int kStages = 3;
-  static constexpr uint32_t kOffGC = kStages * kStage;  // fp32 x 4 per stage
+  static constexpr uint32_t kOffY = kStages * kStage;     // 2 buffers x 2 halves x 8 KB
+  static constexpr uint32_t kOffGC = kOffY + 2 * 16384;  // fp32 x 4 per stage
   static constexpr uint32_t kTotal = kOffGC + kStages * 16 + 1024;
 };
+static_assert(ScanSmem::kTotal <= 232448, "scan shared memory");
 constexpr uint32_t kFusedSmem = ScanSmem::kTotal > kPrepSmem ? ScanSmem::kTotal : kPrepSmem;
 
 enum : int {
   kZFull = 0,                          // [stages] tile landed (TMA transaction count)
-  kZEmpty = kZFull + ScanSmem::kStages,  // [stages] 8 state warps (G_C read) + MMA commit + y reducer
+  kZEmpty = kZFull + ScanSmem::kStages,  // [stages] 8 state warps (G_C read) + MMA commit
   kZKNorm = kZEmpty + ScanSmem::kStages, // [stages] 4 aux warps: the tile's K rows normalised
   kZD1Full = kZKNorm + ScanSmem::kStages,  // [2] [Z | Y^T] of the chunk complete
   kZD1Free = kZD1Full + 2,             // [2] 8 state warps (Z read) + 4 aux warps (Y read)
@@ -1003,7 +1006,7 @@ __device__ __forceinline__ void scan_role(const CUtensorMap* tm_a1c, const CUten
   if (tid == 0) {
     for (int s = 0; s < SM::kStages; ++s) {
       mbar_init(bar(kZFull + s), 1);
-      mbar_init(bar(kZEmpty + s), 10);
+      mbar_init(bar(kZEmpty + s), 9);
       mbar_init(bar(kZKNorm + s), 4);
     }
     for (int x = 0; x < 2; ++x) {
@@ -1071,10 +1074,18 @@ __device__ __forceinline__ void scan_role(const CUtensorMap* tm_a1c, const CUten
       const SmemDesc d_a1 = smem_desc_base(sbase + SM::kOffA1, 16, 1024, kSw128);  // K-major rows
       const SmemDesc d_mn = smem_desc_base(sbase, 8192, 1024, kSw128);  // MN-major 64-col halves
       bool ok = true;
+      // The next chunk's tile and [Z | Y^T] buffer, tested (not waited for)
+      // while this chunk's -Z is being written, so that once S_j is ready the
+      // product is issued without further checks on the serial path.
+      bool next_tile_ready = false, next_buf_free = false;
       for (int j = 0; j < NC && ok; ++j) {
         const int c = j % kCt, n = j / kCt, st = n % SM::kStages;
-        if (c == 0 && !(ok = mbar_wait(bar(kZFull + st), (n / SM::kStages) & 1))) break;
-        if (j >= 2 && !(ok = mbar_wait(bar(kZD1Free + (j & 1)), ((j >> 1) - 1) & 1))) break;
+        if (c == 0 && !next_tile_ready &&
+            !(ok = mbar_wait_poll(bar(kZFull + st), (n / SM::kStages) & 1)))
+          break;
+        if (j >= 2 && !next_buf_free &&
+            !(ok = mbar_wait_poll(bar(kZD1Free + (j & 1)), ((j >> 1) - 1) & 1)))
+          break;
         if (!(ok = mbar_wait_poll(bar(kZSReady), j & 1))) break;
         tc_fence_after();
         const uint32_t aoff = st * SM::kStage + 2 * C * c * 128;
@@ -1091,6 +1102,13 @@ __device__ __forceinline__ void scan_role(const CUtensorMap* tm_a1c, const CUten
         for (int kk = 0; kk < C / 16; ++kk)
           mma_f16_ss(tD2, smem_desc_at(d_mn, toff + SM::kOffU + kk * 2048),
                      smem_desc_at(d_mn, toff + SM::kOffK + kk * 2048), id_n, kk > 0);
+        if (j + 1 < NC) {
+          const int n1 = (j + 1) / kCt;
+          next_tile_ready = ((j + 1) % kCt != 0) ||
+                            mbar_test_wait(bar(kZFull + n1 % SM::kStages), (n1 / SM::kStages) & 1);
+          next_buf_free = j + 1 < 2 ||
+                          mbar_test_wait(bar(kZD1Free + ((j + 1) & 1)), (((j + 1) >> 1) - 1) & 1);
+        }
         if (!(ok = mbar_wait_poll(bar(kZWReady), j & 1))) break;
         tc_fence_after();
 #pragma unroll
@@ -1194,7 +1212,9 @@ __device__ __forceinline__ void scan_role(const CUtensorMap* tm_a1c, const CUten
     bool ok = true;
     for (int j = 0; j < NC; ++j) {
       const int c = j % kCt, n = j / kCt, st = n % SM::kStages;
-      if (c == 0) ok = ok && mbar_wait(bar(kZFull + st), (n / SM::kStages) & 1);
+      // (Only the K normalisation reads the stage; its barrier keeps the stage
+      // from being refilled before it is done.)
+      if (knorm && c == 0) ok = ok && mbar_wait(bar(kZFull + st), (n / SM::kStages) & 1);
       ok = __all_sync(0xffffffffu, ok);
       if (ok && knorm && c == 0) {
         // The tile's K rows as x / |x| (two threads a row), before W K reads them.
@@ -1206,7 +1226,7 @@ __device__ __forceinline__ void scan_role(const CUtensorMap* tm_a1c, const CUten
       if (ok) ok = mbar_wait(bar(kZYGo), j & 1);
       if (ok) ok = mbar_wait(bar(kZD1Full + (j & 1)), (j >> 1) & 1);
       ok = __all_sync(0xffffffffu, ok);
-      const uint32_t yoff = st * SM::kStage + SM::kOffA1 + (2 * C * c + C) * 128;
+      const uint32_t yoff = SM::kOffY + (j & 1) * 16384;  // this chunk's y staging
       if (ok) {
         tc_fence_after();
         // Y^T (lanes v, columns t; already / sqrt(Dk): Qh is stored scaled) in
@@ -1224,14 +1244,14 @@ __device__ __forceinline__ void scan_role(const CUtensorMap* tm_a1c, const CUten
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kZD1Free + (j & 1)));
-        // Stored transposed into the chunk's Qh rows, the box layout of the y
-        // reduction (C token rows of 128 bytes per 64-column half): each 8 x 8
-        // block becomes 8 token rows of 8 consecutive values (16 bytes).
+        // Stored transposed into the y staging (C token rows of 128 bytes per
+        // 64-column half): each 8 x 8 block becomes 8 token rows of 8
+        // consecutive values (16 bytes).
         const int mi = lane >> 3, r8 = lane & 7;
 #pragma unroll
         for (int lh = 0; lh < 2; ++lh) {
           const int v0 = 32 * q + 16 * lh + 8 * (mi & 1);
-          const uint32_t hbase = sbase + yoff + (v0 >> 6) * 16384;
+          const uint32_t hbase = sbase + yoff + (v0 >> 6) * 8192;
 #pragma unroll
           for (int cb = 0; cb < kCb; cb += 2) {
             const int t = 8 * (cb + (mi >> 1)) + r8;
@@ -1244,17 +1264,17 @@ __device__ __forceinline__ void scan_role(const CUtensorMap* tm_a1c, const CUten
         }
         fence_proxy_async();
       }
+      // The previous chunk's reduction has read its buffer before any aux
+      // thread passes this barrier, so the buffer it wrote this chunk's y into
+      // (two chunks back) and the one of the next chunk are free.
+      if (reducer) bulk_wait_read_all();
       ok = named_bar_and(3, 128, ok);
       if (!ok) break;
       if (reducer) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh)
-          tma_reduce_add_4d(tm_yred, sbase + yoff + hh * 16384, 64 * hh, hv, j * C, b);
+          tma_reduce_add_4d(tm_yred, sbase + yoff + hh * 8192, 64 * hh, hv, j * C, b);
         bulk_commit();
-        if (last_of_tile(j)) {  // the stage may be refilled once the reductions have read it
-          bulk_wait_read_all();
-          mbar_arrive(bar(kZEmpty + st));
-        }
       }
       __syncwarp();
     }
