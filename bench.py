@@ -46,10 +46,10 @@ FLUSH_BYTES = 256 << 20
 # reported as null.
 _KDIR = os.path.join(ROOT, "gated_delta_rule_02_gb300", "csrc")
 MEASURED_TRAFFIC = {
-    "prefill_t4096": {"sources": ["prefill_tc.cu", "sm100_ptx.cuh"], "sha": "3b6621bfa1cbb5e0",
+    "prefill_t4096": {"sources": ["prefill_tc.cu", "sm100_ptx.cuh"], "sha": "3230ab1f70e45acc",
                       "bytes": 157.1e6},
     "prefill_b4_t2048": {"sources": ["prefill_tc.cu", "sm100_ptx.cuh"],
-                         "sha": "3b6621bfa1cbb5e0", "bytes": 1049.7e6},
+                         "sha": "3230ab1f70e45acc", "bytes": 1049.7e6},
     "decode_b64": {"sources": ["decode.cu"], "sha": "48a64c9af36e1446", "bytes": 210.7e6},
 }
 

@@ -13,18 +13,18 @@
 //   T_L = (I + L)^-1,  L[t][j] = beta_j KK^T[t][j]          (step 4), by blocked
 //       forward substitution; step 5 needs no second inverse:
 //       (I + A)^-1 diag(beta) = diag(beta) (Gam . T_L),  A[t][j] = beta_t Gam[t][j] KK^T[t][j]
-//   G2  [T_L; diag(beta)(Gam . T_L)] [K | V]  -> P = T_L K, U = (I + A)^-1 (beta V)
-//   G3  [diag(G) M 0; 0 Gam.QK^T] [P; U]  -> the state-free part of step 7
-//       (M[t][i] = beta_i QK^T[t][i], i <= t) and y_local (step 6)
-//   and writes, per tile, in bf16: to the workspace A1 = per chunk [Pt; Qh] with
-//   Pt = G_C beta P (step 9), Qh = G Q - G M P (step 7), and Ut = Gam[C-1][.] U
-//   (step 9), plus G_C (fp32) per chunk; y_local / sqrt(Dk) straight into y.
-// scan (scan_role128): one CTA per (b, hv) carries S (128 x 128, fp32) through
-// the chunks.  Step 9 is regrouped as S <- G_C S - S M + N with M = Pt^T K and
-// N = Ut^T K, so per chunk only the product with M waits for the state:
-//   D  = K^T Ut + (-M^T) S^T;  S <- G_C S + D^T                       (step 9)
-//   Y^T = S Qh^T;  y += Y / sqrt(Dk)  (TMA reduction)                 (steps 7-8)
-// M^T = K^T Pt is formed a chunk ahead on the tensor cores.
+//   GW, F1, F2 (coefficient form, below): with P = T_L K and U = (I + A)^-1 (beta V),
+//   it writes, per tile, in the input type: to the workspace A1 = per chunk
+//   [-Pt; Qh / sqrt(Dk)] with Pt = G_C beta P (step 9), Qh = G Q - G M P (step 7,
+//   M[t][i] = beta_i QK^T[t][i], i <= t), and Ut = Gam[C-1][.] U (step 9), plus
+//   G_C (fp32) per chunk; y_local / sqrt(Dk) (step 6) straight into y.
+// scan (scan_role): one CTA per (b, hv) carries S (128 x 128, fp32) through the
+// chunks.  With Z = S Pt^T, step 9 reads S <- G_C S + (Ut^T - Z) K (the
+// innovation form of the update: Ut^T K - S Pt^T K), and steps 7-8 y = Y / sqrt(Dk)
+// + y_local with Y^T = S Qh^T, so per chunk
+//   [-Z | Y^T / sqrt(Dk)] = S A1^T      (S as a 16-bit tensor-memory operand)
+//   D2 = Ut^T K + (-Z) K;  S <- G_C S + D2;  y += Y / sqrt(Dk) (TMA reduction)
+// and only the first product and (-Z) K wait for the state.
 //
 // Launches: fused_prefill_kernel runs both roles in one cooperative launch
 // (prep publishes each tile through a flag, the scan waits for it); for many
@@ -181,11 +181,13 @@ __device__ __forceinline__ void l2norm_row_sw128(uint8_t* base, int half_stride,
 //          with M[t][i] = beta_i QK^T[t][i] (i <= t)
 //   T_L    16 x 16 diagonal blocks by substitution (fp32), then the 16 -> 32
 //          -> 64 merges T_BA = -T_BB (L_BA T_AA) on warp-level bf16 MMAs  (step 4)
-//   coefs  cP = diag(G_C beta) T_L, cU = diag(Gam[C-1][.]) T_A
+//   coefs  cP = -diag(G_C beta) T_L, cU = diag(Gam[C-1][.]) T_A
 //   GW  A3 [T_L | T_A]  -> W_M = diag(G) M T_L,  W_Y = (Gam . QK^T) T_A
-//   F1  [cP; -W_M] K    -> Pt = G_C beta P (step 9), Qh - diag(G) Q  (step 7)
+//   F1  [cP; -W_M / sqrt(Dk)] K -> -Pt = -G_C beta P (step 9),
+//                                  (Qh - diag(G) Q) / sqrt(Dk)  (step 7)
 //   F2  [cU; W_Y / sqrt(Dk)] V -> Ut = Gam[C-1][.] U (step 9), y_loc / sqrt(Dk) (step 6)
-// so every row of the two final products is an output.
+// so every row of the two final products is an output; the epilogue adds
+// diag(G) Q / sqrt(Dk) to the Qh rows.
 constexpr int kPrepGroups = 2;
 constexpr int kPrepGroupThreads = 256;
 constexpr int kPrepThreads = kPrepGroups * kPrepGroupThreads;
