@@ -123,8 +123,9 @@ int gdn_device_status(int clear) {
   if (cudaDeviceSynchronize() != cudaSuccess) return GDN_ERR_CUDA;
   const int a = gdn::prefill_tc_device_error(clear != 0);
   const int b = gdn::wait_hook_device_error(clear != 0);
-  if (a < 0 || b < 0) return GDN_ERR_CUDA;
-  return (a || b) ? GDN_ERR_DEVICE_TIMEOUT : GDN_OK;
+  const int c = gdn::short_tc_device_error(clear != 0);
+  if (a < 0 || b < 0 || c < 0) return GDN_ERR_CUDA;
+  return (a || b || c) ? GDN_ERR_DEVICE_TIMEOUT : GDN_OK;
 }
 
 int gdn_selftest_wait_timeout(void* stream) {

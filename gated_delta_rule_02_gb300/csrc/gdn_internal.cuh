@@ -97,6 +97,11 @@ int wait_hook_device_error(bool clear);
 // no workspace.
 constexpr int kShortT = 32;
 cudaError_t launch_prefill_short(const PrefillArgs& a);
+// The same on the tensor cores, one chunk per head (16-bit inputs, Dk = Dv =
+// kHeadDim); launch_prefill_short routes there when short_tc_applies.
+bool short_tc_applies(const PrefillArgs& a);
+cudaError_t launch_prefill_short_tc(const PrefillArgs& a);
+int short_tc_device_error(bool clear);
 
 // Streaming single-step decode.
 cudaError_t launch_decode(const DecodeArgs& a);

@@ -314,6 +314,7 @@ cudaError_t launch_short_dk(const PrefillArgs& a) {
 }  // namespace
 
 cudaError_t launch_prefill_short(const PrefillArgs& a) {
+  if (short_tc_applies(a)) return launch_prefill_short_tc(a);
   if (a.dtype == 0) return launch_short_dk<float>(a);
   if (a.dtype == 2) return launch_short_dk<__half>(a);
   return launch_short_dk<__nv_bfloat16>(a);

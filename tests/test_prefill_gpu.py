@@ -13,7 +13,7 @@ from parity_util import TOL, gpu_prefill, oracle_prefill, rel_err
 
 pytestmark = pytest.mark.gpu
 
-F32, BF16 = torch.float32, torch.bfloat16
+F32, BF16, F16 = torch.float32, torch.bfloat16, torch.float16
 
 SMALL = [
     # (B, T, Hk, Hv, chunk, dtype, u_max)
@@ -101,12 +101,20 @@ def test_prefill_vanishing_gate_is_finite(cuda_device):
 
 
 SHORT = [
-    # (B, T, Hk, Hv, dtype): T <= 32 runs the short-T sequential kernel
+    # (B, T, Hk, Hv, dtype): T <= 32 runs a short-T kernel: 16-bit inputs the
+    # one-chunk tensor-core kernel (16 or 32 token rows), fp32 inputs the
+    # sequential one
     (1, 1, 1, 1, BF16),
     (2, 7, 2, 6, BF16),     # GQA 3:1
     (3, 16, 4, 8, F32),
     (1, 31, 16, 32, BF16),
     (2, 32, 8, 16, F32),
+    (4, 16, 16, 32, BF16),  # a full 16-row chunk, 128 heads
+    (2, 17, 2, 4, BF16),    # one token past the 16-row chunk
+    (1, 32, 2, 2, BF16),    # a full 32-row chunk
+    (2, 16, 2, 4, F16),
+    (1, 32, 1, 3, F16),
+    (3, 9, 2, 2, F16),
 ]
 
 
