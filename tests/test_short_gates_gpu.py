@@ -1,11 +1,14 @@
-"""Gates that push the short-T kernel's scaled state to its limits.
+"""Gates at the limits of the short-T kernels.
 
-The short-T kernel keeps each head's state as gam * St, gam the product of the
-gates since the last renormalisation, and brings the registers back to scale
-when gam * g_t leaves [2^-24, 2^24].  These cases drive that branch: long runs of
-small gates (the product falls below 2^-24 within a few tokens), exact zero gates
-(a reset of the state), gates of one (no decay), and a mix, on two of the four
-heads while the other two keep the random gates; compared with the fp64 oracle.
+The sequential short-T kernel (fp32 inputs, head sizes other than 128/128)
+keeps each head's state as gam * St, gam the product of the gates since the
+last renormalisation, and brings the registers back to scale when gam * g_t
+leaves [2^-24, 2^24]; the one-chunk tensor-core kernel (16-bit inputs at
+128/128) forms its decays from log2 prefix sums, clamped at -1000 per token.
+These cases drive both: long runs of small gates (the product falls below
+2^-24 within a few tokens), exact zero gates (a reset of the state), gates of
+one (no decay), and a mix, on two of the four heads while the other two keep
+the random gates; compared with the fp64 oracle.
 """
 import pytest
 import torch
