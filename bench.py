@@ -204,8 +204,8 @@ def roofline(alg_bytes, seconds, hbm_gbs, kind, traffic=None):
 
 
 def prefill_launches(w, dev):
-    """Kernels one gdn_prefill call launches: T <= 32 one (the sequential
-    short-T kernel); bf16 or fp16 with 128-wide heads runs prep and scan as
+    """Kernels one gdn_prefill call launches: T <= 32 one (a short-T
+    kernel); bf16 or fp16 with 128-wide heads runs prep and scan as
     one cooperative kernel when B*Hv is at most a third of the SMs, else as
     two; the fp32 chunked path always two."""
     if w.T <= 32:
@@ -475,7 +475,7 @@ METRIC = "GDN prefill tokens/s (B=1 T=4096 Hk=16 Hv=32 D=128 bf16 C=64) and deco
 
 # The other prefill workloads of the plan, timed after the headline one.
 EXTRA_PREFILL = ["fp32_t64", "prefill_b4_t2048", "prefill_t65536", "prefill_b64_t16",
-                 "prefill_t4096_f16"]
+                 "prefill_t4096_f16", "prefill_t4096_d64", "prefill_t4096_d256"]
 
 
 def prefill_entry(gdn, w, dev, steps, warmup, hbm, peak_kind, world):

@@ -1,8 +1,26 @@
 // The C ABI of libgdn.so (declared in include/gdn.h): argument checking and
 // dispatch.  Every check runs on the host before anything is enqueued, so a
 // rejected call leaves every output untouched.
+#include <mutex>
+
 #include "../../include/gdn.h"
 #include "gdn_internal.cuh"
+
+namespace gdn {
+TmapEncodeFn tmap_encoder() {
+  static TmapEncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<TmapEncodeFn>(p);
+  });
+  return fn;
+}
+}  // namespace gdn
 
 namespace {
 
@@ -57,6 +75,7 @@ size_t gdn_prefill_workspace_bytes(int B, int T, int Hk, int Hv, int Dk, int Dv,
   if (chunk != 16 && chunk != 32 && chunk != 64) return 0;
   if (T <= gdn::kShortT) return 0;  // the short-T sequential kernel needs none
   if (use_tc(Dk, Dv, dtype)) return gdn::prefill_tc_workspace_bytes(B, T, Hv);
+  if (gdn::mma_path_applies(Dk, Dv, dtype, T)) return gdn::prefill_mma_workspace_bytes(B, T, Hv);
   return gdn::prefill_simt_workspace_bytes(B, T, Hv, chunk, Dk, Dv);
 }
 
@@ -80,9 +99,10 @@ int gdn_prefill_ex(const void* q, const void* k, const void* v, const void* g,
   gdn::PrefillArgs a{q, k, v, g, beta, state_in, state_out, y, B, T, Hk, Hv, chunk,
                      dtype, options, Dk, Dv, workspace, workspace_bytes,
                      static_cast<cudaStream_t>(stream)};
-  cudaError_t e = T <= gdn::kShortT        ? gdn::launch_prefill_short(a)
-                  : use_tc(Dk, Dv, dtype) ? gdn::launch_prefill_tc(a)
-                                          : gdn::launch_prefill_simt(a);
+  cudaError_t e = T <= gdn::kShortT                       ? gdn::launch_prefill_short(a)
+                  : use_tc(Dk, Dv, dtype)                ? gdn::launch_prefill_tc(a)
+                  : gdn::mma_path_applies(Dk, Dv, dtype, T) ? gdn::launch_prefill_mma(a)
+                                                         : gdn::launch_prefill_simt(a);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -124,8 +144,9 @@ int gdn_device_status(int clear) {
   const int a = gdn::prefill_tc_device_error(clear != 0);
   const int b = gdn::wait_hook_device_error(clear != 0);
   const int c = gdn::short_tc_device_error(clear != 0);
-  if (a < 0 || b < 0 || c < 0) return GDN_ERR_CUDA;
-  return (a || b || c) ? GDN_ERR_DEVICE_TIMEOUT : GDN_OK;
+  const int d = gdn::prefill_mma_device_error(clear != 0);
+  if (a < 0 || b < 0 || c < 0 || d < 0) return GDN_ERR_CUDA;
+  return (a || b || c || d) ? GDN_ERR_DEVICE_TIMEOUT : GDN_OK;
 }
 
 int gdn_selftest_wait_timeout(void* stream) {

@@ -1,6 +1,7 @@
 // Internal interface between the C ABI (gdn_api.cu) and the kernel files.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -102,6 +103,22 @@ cudaError_t launch_prefill_short(const PrefillArgs& a);
 bool short_tc_applies(const PrefillArgs& a);
 cudaError_t launch_prefill_short_tc(const PrefillArgs& a);
 int short_tc_device_error(bool clear);
+
+// Chunked prefill on warp-level tensor-core MMAs for 16-bit inputs with Dk =
+// Dv = 64 and T > kShortT: a prep launch over every (head, chunk) and a scan
+// launch over heads, through a workspace of prefill_mma_workspace_bytes.
+bool mma_path_applies(int Dk, int Dv, int dtype, int T);
+size_t prefill_mma_workspace_bytes(int B, int T, int Hv);
+cudaError_t launch_prefill_mma(const PrefillArgs& a);
+int prefill_mma_device_error(bool clear);
+
+// cuTensorMapEncodeTiled, looked up once through the runtime's driver entry
+// point (nullptr if unavailable).
+typedef CUresult (*TmapEncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+TmapEncodeFn tmap_encoder();
 
 // Streaming single-step decode.
 cudaError_t launch_decode(const DecodeArgs& a);

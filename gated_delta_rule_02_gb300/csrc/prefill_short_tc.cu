@@ -25,14 +25,15 @@
 // tensor and arrive as zeros), its gates in registers, and, once the current
 // state has been read into registers, its state as one 64 KB TMA box.  The new
 // state leaves from registers by streaming stores.
-#include <mutex>
 #include <type_traits>
 
 #include "gdn_internal.cuh"
 #include "sm100_ptx.cuh"
+#include "warp_mma.cuh"
 
 namespace gdn {
 namespace {
+using namespace wm;
 
 constexpr int kD = 128;
 constexpr int kThr = 256;
@@ -72,113 +73,6 @@ struct ShortTcSmem {
   alignas(8) uint64_t bar_st;      // the state's box landed
   alignas(8) uint64_t bar_tok[2];  // a token buffer's boxes landed
 };
-
-__device__ __forceinline__ uint32_t s_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-template <typename E>
-__device__ __forceinline__ uint32_t pk(float a, float b);
-template <>
-__device__ __forceinline__ uint32_t pk<__nv_bfloat16>(float a, float b) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-template <>
-__device__ __forceinline__ uint32_t pk<__half>(float a, float b) {
-  __half2 h = __floats2half2_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-__device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t* r) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm4t(uint32_t addr, uint32_t* r) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm2(uint32_t addr, uint32_t* r) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
-               : "=r"(r[0]), "=r"(r[1])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm2t(uint32_t addr, uint32_t* r) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
-               : "=r"(r[0]), "=r"(r[1])
-               : "r"(addr));
-}
-// D (+)= A B, m16n8k16, 16-bit in, fp32 accumulate.  Fragments (g = lane / 4,
-// c = lane % 4): A rows g, g+8 x cols 2c, 2c+1 and 8+2c, 9+2c; B rows 2c, 2c+1
-// and 8+2c, 9+2c of column g; D (g, 2c), (g, 2c+1), (g+8, 2c), (g+8, 2c+1).
-template <typename E>
-__device__ __forceinline__ void mma(float* d, const uint32_t* a, const uint32_t* b) {
-  if constexpr (std::is_same_v<E, __half>) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-  } else {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-  }
-}
-__device__ __forceinline__ void stsm4t(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                       uint32_t d) {
-  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr),
-               "r"(a), "r"(b), "r"(c), "r"(d)
-               : "memory");
-}
-// ldmatrix lane addresses (row-major 16-bit array, `ld` elements per row):
-// A (m16 x k16) at (r0, c0); B (k16 x n8) from an [n][k] array (rows n0..,
-// cols k0..); B from a [k][n] array (rows k0.., cols n0..), transposing.
-template <typename E>
-__device__ __forceinline__ uint32_t a_addr(const E* base, int ld, int r0, int c0, int lane) {
-  return s_u32(base + (r0 + (lane & 15)) * ld + c0 + 8 * (lane >> 4));
-}
-template <typename E>
-__device__ __forceinline__ uint32_t bnk_addr(const E* base, int ld, int n0, int k0, int lane) {
-  return s_u32(base + (n0 + (lane & 7)) * ld + k0 + 8 * ((lane >> 3) & 1));
-}
-template <typename E>
-__device__ __forceinline__ uint32_t bkn_addr(const E* base, int ld, int k0, int n0, int lane) {
-  return s_u32(base + (k0 + (lane & 15)) * ld + n0);
-}
-// A (m16 x k16) of the transpose of a [k][m] array (rows k0.., cols m0..).
-template <typename E>
-__device__ __forceinline__ uint32_t at_addr(const E* base, int ld, int k0, int m0, int lane) {
-  return s_u32(base + (k0 + (lane & 7) + 8 * (lane >> 4)) * ld + m0 + 8 * ((lane >> 3) & 1));
-}
-
-// One doubling step of the blocked inverse: for every diagonal 2B x 2B block
-// at (o, o), o = 2B p, whose B x B diagonal blocks T11, T22 are in tl, writes
-// its lower-left block T21 = -T22 (L21 T11) (L from lm, M = L21 T11 through
-// the scratch array mt).  All threads of the block call it.
-template <int B, int TC>
-__device__ __forceinline__ void combine_blocks(const float (*lm)[kFS], float (*tl)[kFS],
-                                               float (*mt)[kFS], int tid) {
-  constexpr int kEl = (TC / (2 * B)) * B * B;
-  for (int e = tid; e < kEl; e += kThr) {
-    const int p = e / (B * B), i = (e / B) % B, j = e % B, o = 2 * B * p;
-    float acc = 0.f;
-#pragma unroll
-    for (int k = 0; k < B; ++k) acc = fmaf(lm[o + B + i][o + k], tl[o + k][o + j], acc);
-    mt[o + B + i][o + j] = acc;
-  }
-  __syncthreads();
-  for (int e = tid; e < kEl; e += kThr) {
-    const int p = e / (B * B), i = (e / B) % B, j = e % B, o = 2 * B * p;
-    float acc = 0.f;
-#pragma unroll
-    for (int k = 0; k < B; ++k) acc = fmaf(tl[o + B + i][o + B + k], mt[o + B + k][o + j], acc);
-    tl[o + B + i][o + j] = -acc;
-  }
-  __syncthreads();
-}
 
 // fp32 element (row r, column c) of the swizzled state boxes.
 __device__ __forceinline__ int st_index(int r, int c) {
@@ -398,20 +292,7 @@ short_tc_kernel(const __grid_constant__ CUtensorMap tm_state,
     // block size b, every lower-left block of a 2b x 2b diagonal block from
     //   T21 = -T22 (L21 T11).
     if (warp == 0) {
-      if (lane < TC) {
-        const int o = lane & ~7, c = lane & 7;
-        float x[8];
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          float a = (r == c) ? 1.f : 0.f;
-#pragma unroll
-          for (int s2 = 0; s2 < r; ++s2) a = fmaf(-lm[o + r][o + s2], x[s2], a);
-          x[r] = a;
-        }
-#pragma unroll
-        for (int r = 0; r < 8; ++r) tlf[o + r][o + c] = x[r];
-        for (int r = 0; r < o; ++r) tlf[r][o + c] = 0.f;  // above the block
-      }
+      inverse_diag_blocks<TC, kFS>(lm, tlf, lane);
     } else {
       // The next head's loads (sm.st is free: every warp has read its rows),
       // then A3: diag(G) M and Gam . QK^T, masked to j <= t.
@@ -434,8 +315,8 @@ short_tc_kernel(const __grid_constant__ CUtensorMap tm_state,
       }
     }
     __syncthreads();
-    combine_blocks<8, TC>(lm, tlf, qk, tid);
-    if constexpr (TC == 32) combine_blocks<16, TC>(lm, tlf, qk, tid);
+    combine_blocks<8, TC, kThr, kFS>(lm, tlf, qk, tid);
+    if constexpr (TC == 32) combine_blocks<16, TC, kThr, kFS>(lm, tlf, qk, tid);
     // T_L, T_A = diag(beta)(Gam . T_L), cP = -diag(G_C beta) T_L and
     // cU = diag(Gam_end) T_A in 16 bits (zero above the diagonal).
     for (int e = tid; e < TC * TC; e += kThr) {
@@ -602,28 +483,11 @@ short_tc_kernel(const __grid_constant__ CUtensorMap tm_state,
   }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-EncodeTiledFn tiled_encoder() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
 // The fp32 states [nheads * 128 rows][128] seen as {32 columns, rows, 4
 // column groups} (the groups 128 bytes apart), box {32, 128, 4}: one head,
 // landing as [group][row][32], 128-byte swizzle.
 bool make_state_map(CUtensorMap* m, const float* base, int nheads) {
-  const EncodeTiledFn enc = tiled_encoder();
+  const TmapEncodeFn enc = tmap_encoder();
   if (!enc) return false;
   const cuuint64_t dims[3] = {32, (cuuint64_t)nheads * kD, 4};
   const cuuint64_t strides[2] = {kD * sizeof(float), 32 * sizeof(float)};
@@ -652,7 +516,7 @@ int sm_count() {
 // [half][token][64], 128-byte swizzle; tokens past T read as zeros.
 bool make_token_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int B, int T, int H,
                     int tc) {
-  const EncodeTiledFn enc = tiled_encoder();
+  const TmapEncodeFn enc = tmap_encoder();
   if (!enc) return false;
   const cuuint64_t dims[5] = {64, (cuuint64_t)T, 2, (cuuint64_t)H, (cuuint64_t)B};
   const cuuint64_t strides[4] = {(cuuint64_t)H * kD * 2, 128, (cuuint64_t)kD * 2,

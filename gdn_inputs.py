@@ -77,6 +77,13 @@ WORKLOADS = {
     "prefill_t4096_f16": Workload("prefill_t4096_f16", B=1, T=4096, Hk=16, Hv=32, Dk=128,
                                   Dv=128, dtype="f16", chunk=64, u_max=0.1,
                                   s0_std=0.0, seed=1006),
+    # The headline shape at the other head sizes of the plan (64 and 256).
+    "prefill_t4096_d64": Workload("prefill_t4096_d64", B=1, T=4096, Hk=16, Hv=32, Dk=64,
+                                  Dv=64, dtype="bf16", chunk=64, u_max=0.1,
+                                  s0_std=0.0, seed=1007),
+    "prefill_t4096_d256": Workload("prefill_t4096_d256", B=1, T=4096, Hk=16, Hv=32, Dk=256,
+                                   Dv=256, dtype="bf16", chunk=64, u_max=0.1,
+                                   s0_std=0.0, seed=1008),
 }
 
 

@@ -1,6 +1,7 @@
 """Head sizes other than 128 (Dk, Dv in {64, 128, 256}): the decode kernel, the
-short-T sequential kernel and the fp32 SIMT chunked path (which serves every
-dtype when the head size is not the tensor-core one), against the fp64 oracle.
+short-T sequential kernel, the warp-level tensor-core chunked path (16-bit
+inputs at Dk = Dv = 64) and the fp32 SIMT chunked path (every other case),
+against the fp64 oracle.
 """
 import numpy as np
 import pytest
@@ -51,8 +52,9 @@ def test_short_prefill_head_sizes(cuda_device, dtype, Dk, Dv):
 @pytest.mark.parametrize("Dk,Dv", PAIRS)
 @pytest.mark.parametrize("chunk", [16, 64])
 def test_chunked_prefill_head_sizes(cuda_device, dtype, Dk, Dv, chunk):
-    """T = 100 (several chunks and a ragged tail) on the SIMT chunked path; at
-    Dk = Dv = 256 a chunk of 64 runs as two chunks of 32."""
+    """T = 100 (several chunks and a ragged tail) on the chunked paths: at Dk =
+    Dv = 64 with 16-bit inputs the warp-level tensor-core one, else the SIMT one
+    (where at Dk = Dv = 256 a chunk of 64 runs as two chunks of 32)."""
     ins = gdn_inputs.make_inputs(1, 100, 2, 4, Dk, Dv, dtype=dtype, seed=350 + Dk + Dv + chunk)
     y, s = gpu_prefill(ins, chunk, cuda_device)
     yo, so = oracle_prefill(ins)
@@ -73,3 +75,32 @@ def test_head_sizes_with_l2norm_and_null_state(cuda_device, Dk, Dv):
         yo, so = oracle_prefill(ins, zero_state=True)
         assert rel_err(y, yo) <= 1e-4, (T, rel_err(y, yo))
         assert rel_err(s, so) <= 1e-4
+
+
+MMA_CASES = [
+    # (B, T, Hk, Hv, dtype): Dk = Dv = 64, 16-bit inputs, T > 32
+    (1, 33, 1, 1, torch.bfloat16),    # one chunk and one token
+    (1, 64, 2, 4, torch.bfloat16),    # two whole chunks
+    (2, 257, 2, 6, torch.bfloat16),   # GQA 3:1, B = 2, ragged tail
+    (1, 1000, 4, 8, torch.float16),
+    (3, 95, 1, 2, torch.float16),
+]
+
+
+@pytest.mark.parametrize("B,T,Hk,Hv,dtype", MMA_CASES)
+def test_mma_prefill_d64(cuda_device, B, T, Hk, Hv, dtype):
+    ins = gdn_inputs.make_inputs(B, T, Hk, Hv, 64, 64, dtype=dtype, seed=390 + T + Hv,
+                                 u_max=0.5, s0_std=0.1)
+    y, s = gpu_prefill(ins, 32, cuda_device)
+    yo, so = oracle_prefill(ins)
+    assert rel_err(y, yo) <= TOL[dtype], rel_err(y, yo)
+    assert rel_err(s, so) <= TOL[dtype], rel_err(s, so)
+
+
+@pytest.mark.parametrize("mode", ["null", "inplace"])
+def test_mma_prefill_d64_state_modes(cuda_device, mode):
+    ins = gdn_inputs.make_inputs(2, 130, 2, 4, 64, 64, dtype=torch.bfloat16, seed=395, s0_std=0.1)
+    y, s = gpu_prefill(ins, 64, cuda_device, state_mode=mode)
+    yo, so = oracle_prefill(ins, zero_state=(mode == "null"))
+    assert rel_err(y, yo) <= TOL[torch.bfloat16]
+    assert rel_err(s, so) <= TOL[torch.bfloat16]

@@ -75,6 +75,18 @@ def test_prefill_options(cuda_device, options, B, T, Hk, Hv, chunk, dtype):
     assert rel_err(s, so) <= TOL[dtype], rel_err(s, so)
 
 
+@pytest.mark.parametrize("options", [TILED, LOGG, L2N, TILED | LOGG | L2N])
+def test_prefill_options_head_size_64(cuda_device, options):
+    """The same conventions on the warp-level tensor-core path (16-bit inputs,
+    Dk = Dv = 64), q and k rows of varied length under L2N."""
+    ins = gdn_inputs.make_inputs(2, 100, 2, 4, 64, 64, BF16, seed=520, u_max=0.5, s0_std=0.1)
+    if options & L2N:
+        ins = _unnormalised(ins)
+    y, s, yo, so = _run(ins, options, 32, cuda_device)
+    assert rel_err(y, yo) <= TOL[BF16], rel_err(y, yo)
+    assert rel_err(s, so) <= TOL[BF16], rel_err(s, so)
+
+
 def test_tiled_differs_from_grouped(cuda_device):
     """The option changes the result (the two maps pair different heads)."""
     ins = gdn_inputs.make_inputs(1, 40, 2, 4, 128, 128, BF16, seed=7, s0_std=0.1)

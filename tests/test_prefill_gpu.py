@@ -156,7 +156,8 @@ def test_prefill_short_and_chunked_paths_agree(cuda_device):
     assert rel_err(s, so) <= TOL[BF16]
 
 
-FULL = ["prefill_t4096", "prefill_b4_t2048", "prefill_t65536", "prefill_b64_t16"]
+FULL = ["prefill_t4096", "prefill_b4_t2048", "prefill_t65536", "prefill_b64_t16",
+        "prefill_t4096_d64", "prefill_t4096_d256"]
 
 
 @pytest.mark.parametrize("name", FULL)
