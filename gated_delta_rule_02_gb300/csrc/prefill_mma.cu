@@ -13,10 +13,11 @@
 //     -Pt = cP K;  Qh = (G Q - diag(G) M T_L K) / sqrt(Dk);  Ut = cU V;
 //     y_loc = (Gam . QK^T) T_A V / sqrt(Dk)
 //   into a workspace block [-Pt; Qh; Ut; K; y_loc] (5C rows of 64) and G_C;
-//   scan, one CTA of four warps per head, S in registers (warp w: value rows
-//   16w .. 16w + 15 in the m16n8 accumulator layout), chunk after chunk:
+//   scan, one CTA per head, S in registers (warp w < 4: value rows 16w .. 16w
+//   + 15 in the m16n8 accumulator layout), chunk after chunk:
 //     [-Z | Y] = S [-Pt; Qh]^T;  y = y_loc + Y;  S <- G_C S + (Ut^T - Z) K,
-// the workspace blocks coming in by TMA three chunks ahead.
+// the workspace blocks coming in by TMA up to three chunks ahead, issued by a
+// fifth warp; the four state warps meet no CTA-wide barrier on the way.
 #include "gdn_internal.cuh"
 #include "sm100_ptx.cuh"
 #include "warp_mma.cuh"
@@ -27,7 +28,7 @@ namespace {
 constexpr int kD = 64;            // head size (Dk = Dv)
 constexpr int kC = 32;            // chunk
 constexpr int kPT = 128;          // prep threads
-constexpr int kST = 128;          // scan threads: four warps x 16 value rows
+constexpr int kST = 160;          // scan threads: four warps x 16 value rows + a loader warp
 constexpr int kFS = kC + 1;       // fp32 row stride of the C x C arrays
 constexpr int kCS = kC + 8;       // 16-bit row stride of the C x C arrays (80 B)
 constexpr int kYS = kD + 8;       // 16-bit row stride of the y staging (144 B)
@@ -54,7 +55,8 @@ template <typename E>
 struct ScanSmem {
   E stage[kStages][kBlkRows * kD];  // workspace blocks, 128-byte swizzled rows
   E ys[kC][kYS];                    // Y staging [t][v], each warp its 16 columns
-  alignas(8) uint64_t full[kStages];
+  alignas(8) uint64_t full[kStages];   // a block landed
+  alignas(8) uint64_t empty[kStages];  // the four state warps are done with a stage
 };
 
 __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
@@ -265,17 +267,35 @@ mma_scan_kernel(const __grid_constant__ CUtensorMap tm_ws, const float* __restri
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, cq = lane & 3, r0 = 16 * warp + gq;
   constexpr int NT8 = kC / 8, NK16 = kC / 16;
-  auto issue = [&](int n) {  // thread 0: chunk n's block into stage n % kStages
-    const int st = n % kStages;
-    const uint32_t fb = s_u32(&sm.full[st]);
-    ptx::mbar_expect_tx(fb, kBlkBytes);
-    ptx::tma_load_2d(s_u32(sm.stage[st]), &tm_ws, fb, 0, (bh * NC + n) * kBlkRows);
-  };
   if (tid == 0) {
     ptx::prefetch_tmap(&tm_ws);
-    for (int s2 = 0; s2 < kStages; ++s2) ptx::mbar_init(s_u32(&sm.full[s2]), 1);
+    for (int s2 = 0; s2 < kStages; ++s2) {
+      ptx::mbar_init(s_u32(&sm.full[s2]), 1);
+      ptx::mbar_init(s_u32(&sm.empty[s2]), 4);
+    }
     ptx::fence_mbar_init();
-    for (int n = 0; n < kStages && n < NC; ++n) issue(n);
+  }
+  __syncthreads();  // the barriers' initialisation
+  if (warp == 4) {
+    // Loader: chunk n's block into stage n % kStages once the state warps
+    // are done with chunk n - kStages there.  A wait that runs out (2 s) is
+    // recorded in the device error word; the loads issued land before the
+    // CTA ends.
+    if (lane == 0) {
+      int n = 0;
+      for (; n < NC; ++n) {
+        const int st = n % kStages;
+        if (n >= kStages &&
+            !ptx::mbar_wait(s_u32(&sm.empty[st]), ((n / kStages) - 1) & 1))
+          break;
+        const uint32_t fb = s_u32(&sm.full[st]);
+        ptx::mbar_expect_tx(fb, kBlkBytes);
+        ptx::tma_load_2d(s_u32(sm.stage[st]), &tm_ws, fb, 0, (bh * NC + n) * kBlkRows);
+      }
+      for (int m = (n > kStages ? n - kStages : 0); m < n; ++m)
+        ptx::mbar_wait(s_u32(&sm.full[m % kStages]), (m / kStages) & 1);
+    }
+    return;
   }
   // S rows r0 and r0 + 8, columns 8j + 2cq, +1 (j < 8): the accumulator layout
   // of eight m16n8 tiles.
@@ -295,7 +315,6 @@ mma_scan_kernel(const __grid_constant__ CUtensorMap tm_ws, const float* __restri
       s[j][3] = hi.y;
     }
   }
-  __syncthreads();  // the barriers' initialisation
   float gc_next = __ldg(wsgc + (size_t)bh * NC);
   for (int j = 0; j < NC; ++j) {
     const int st = j % kStages;
@@ -303,7 +322,7 @@ mma_scan_kernel(const __grid_constant__ CUtensorMap tm_ws, const float* __restri
     if (j + 1 < NC) gc_next = __ldg(wsgc + (size_t)bh * NC + j + 1);
     // A block that never lands (2 s) is recorded in the device error word and
     // the head is left unwritten.
-    if (!__syncthreads_and(ptx::mbar_wait(s_u32(&sm.full[st]), (j / kStages) & 1))) return;
+    if (!__all_sync(0xffffffffu, ptx::mbar_wait(s_u32(&sm.full[st]), (j / kStages) & 1))) return;
     const uint32_t base = s_u32(sm.stage[st]);
     // [-Z | Y] = S [-Pt; Qh]^T: B from rows 0 .. 2C of the block.
     float zy[2 * NT8][4];
@@ -381,8 +400,8 @@ mma_scan_kernel(const __grid_constant__ CUtensorMap tm_ws, const float* __restri
         }
       }
     }
-    __syncthreads();  // every warp is done with the stage and its ys columns
-    if (tid == 0 && j + kStages < NC) issue(j + kStages);
+    __syncwarp();  // this warp is done with the stage and its ys columns
+    if (lane == 0) ptx::mbar_arrive(s_u32(&sm.empty[st]));
   }
   float* dst = state_out + (size_t)bh * kD * kD;
 #pragma unroll
