@@ -51,8 +51,8 @@ MEASURED_TRAFFIC = {
     "prefill_b4_t2048": {"sources": ["prefill_tc.cu", "sm100_ptx.cuh"],
                          "sha": "3230ab1f70e45acc", "bytes": 1049.7e6},
     "decode_b64": {"sources": ["decode.cu"], "sha": "48a64c9af36e1446", "bytes": 210.7e6},
-    "prefill_b64_t16": {"sources": ["prefill_short_tc.cu", "sm100_ptx.cuh"],
-                        "sha": "a66b4311873b82c7", "bytes": 238.7e6},
+    "prefill_b64_t16": {"sources": ["prefill_short_tc.cu", "warp_mma.cuh", "sm100_ptx.cuh"],
+                        "sha": "aea52e59a7d765cc", "bytes": 238.7e6},
 }
 
 

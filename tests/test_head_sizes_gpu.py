@@ -84,6 +84,7 @@ MMA_CASES = [
     (2, 257, 2, 6, torch.bfloat16),   # GQA 3:1, B = 2, ragged tail
     (1, 1000, 4, 8, torch.float16),
     (3, 95, 1, 2, torch.float16),
+    (4, 40, 8, 64, torch.bfloat16),   # 256 heads
 ]
 
 
