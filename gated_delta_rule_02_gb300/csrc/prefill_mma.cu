@@ -27,7 +27,7 @@ namespace {
 
 constexpr int kD = 64;            // head size (Dk = Dv)
 constexpr int kC = 32;            // chunk
-constexpr int kPT = 128;          // prep threads
+constexpr int kPT = 256;          // prep threads: eight warps
 constexpr int kST = 160;          // scan threads: four warps x 16 value rows + a loader warp
 constexpr int kFS = kC + 1;       // fp32 row stride of the C x C arrays
 constexpr int kCS = kC + 8;       // 16-bit row stride of the C x C arrays (80 B)
