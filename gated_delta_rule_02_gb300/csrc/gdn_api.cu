@@ -76,6 +76,8 @@ size_t gdn_prefill_workspace_bytes(int B, int T, int Hk, int Hv, int Dk, int Dv,
   if (T <= gdn::kShortT) return 0;  // the short-T sequential kernel needs none
   if (use_tc(Dk, Dv, dtype)) return gdn::prefill_tc_workspace_bytes(B, T, Hv);
   if (gdn::mma_path_applies(Dk, Dv, dtype, T)) return gdn::prefill_mma_workspace_bytes(B, T, Hv);
+  if (gdn::mma256_path_applies(Dk, Dv, dtype, T))
+    return gdn::prefill_mma256_workspace_bytes(B, T, Hv);
   return gdn::prefill_simt_workspace_bytes(B, T, Hv, chunk, Dk, Dv);
 }
 
@@ -102,6 +104,7 @@ int gdn_prefill_ex(const void* q, const void* k, const void* v, const void* g,
   cudaError_t e = T <= gdn::kShortT                       ? gdn::launch_prefill_short(a)
                   : use_tc(Dk, Dv, dtype)                ? gdn::launch_prefill_tc(a)
                   : gdn::mma_path_applies(Dk, Dv, dtype, T) ? gdn::launch_prefill_mma(a)
+                  : gdn::mma256_path_applies(Dk, Dv, dtype, T) ? gdn::launch_prefill_mma256(a)
                                                          : gdn::launch_prefill_simt(a);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
@@ -145,8 +148,9 @@ int gdn_device_status(int clear) {
   const int b = gdn::wait_hook_device_error(clear != 0);
   const int c = gdn::short_tc_device_error(clear != 0);
   const int d = gdn::prefill_mma_device_error(clear != 0);
-  if (a < 0 || b < 0 || c < 0 || d < 0) return GDN_ERR_CUDA;
-  return (a || b || c || d) ? GDN_ERR_DEVICE_TIMEOUT : GDN_OK;
+  const int f = gdn::prefill_mma256_device_error(clear != 0);
+  if (a < 0 || b < 0 || c < 0 || d < 0 || f < 0) return GDN_ERR_CUDA;
+  return (a || b || c || d || f) ? GDN_ERR_DEVICE_TIMEOUT : GDN_OK;
 }
 
 int gdn_selftest_wait_timeout(void* stream) {

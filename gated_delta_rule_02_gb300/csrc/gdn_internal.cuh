@@ -111,6 +111,12 @@ bool mma_path_applies(int Dk, int Dv, int dtype, int T);
 size_t prefill_mma_workspace_bytes(int B, int T, int Hv);
 cudaError_t launch_prefill_mma(const PrefillArgs& a);
 int prefill_mma_device_error(bool clear);
+// The same for Dk = Dv = 256: the state of a head over four CTAs of 64 value
+// rows, keys split over warp pairs.
+bool mma256_path_applies(int Dk, int Dv, int dtype, int T);
+size_t prefill_mma256_workspace_bytes(int B, int T, int Hv);
+cudaError_t launch_prefill_mma256(const PrefillArgs& a);
+int prefill_mma256_device_error(bool clear);
 
 // cuTensorMapEncodeTiled, looked up once through the runtime's driver entry
 // point (nullptr if unavailable).

@@ -1,6 +1,7 @@
 """Head sizes other than 128 (Dk, Dv in {64, 128, 256}): the decode kernel, the
-short-T sequential kernel, the warp-level tensor-core chunked path (16-bit
-inputs at Dk = Dv = 64) and the fp32 SIMT chunked path (every other case),
+short-T sequential kernel, the warp-level tensor-core chunked paths (16-bit
+inputs at Dk = Dv = 64 and at 256) and the fp32 SIMT chunked path (every other
+case),
 against the fp64 oracle.
 """
 import numpy as np
@@ -53,8 +54,8 @@ def test_short_prefill_head_sizes(cuda_device, dtype, Dk, Dv):
 @pytest.mark.parametrize("chunk", [16, 64])
 def test_chunked_prefill_head_sizes(cuda_device, dtype, Dk, Dv, chunk):
     """T = 100 (several chunks and a ragged tail) on the chunked paths: at Dk =
-    Dv = 64 with 16-bit inputs the warp-level tensor-core one, else the SIMT one
-    (where at Dk = Dv = 256 a chunk of 64 runs as two chunks of 32)."""
+    Dv = 64 or 256 with 16-bit inputs the warp-level tensor-core ones, else the
+    SIMT one (where at Dk = Dv = 256 a chunk of 64 runs as two chunks of 32)."""
     ins = gdn_inputs.make_inputs(1, 100, 2, 4, Dk, Dv, dtype=dtype, seed=350 + Dk + Dv + chunk)
     y, s = gpu_prefill(ins, chunk, cuda_device)
     yo, so = oracle_prefill(ins)
@@ -101,6 +102,35 @@ def test_mma_prefill_d64(cuda_device, B, T, Hk, Hv, dtype):
 @pytest.mark.parametrize("mode", ["null", "inplace"])
 def test_mma_prefill_d64_state_modes(cuda_device, mode):
     ins = gdn_inputs.make_inputs(2, 130, 2, 4, 64, 64, dtype=torch.bfloat16, seed=395, s0_std=0.1)
+    y, s = gpu_prefill(ins, 64, cuda_device, state_mode=mode)
+    yo, so = oracle_prefill(ins, zero_state=(mode == "null"))
+    assert rel_err(y, yo) <= TOL[torch.bfloat16]
+    assert rel_err(s, so) <= TOL[torch.bfloat16]
+
+
+MMA256_CASES = [
+    # (B, T, Hk, Hv, dtype): Dk = Dv = 256, 16-bit inputs, T > 32 (the head's
+    # state over four CTAs, keys split over warp pairs)
+    (1, 33, 1, 1, torch.bfloat16),
+    (2, 100, 2, 4, torch.bfloat16),
+    (1, 257, 1, 3, torch.float16),
+]
+
+
+@pytest.mark.parametrize("B,T,Hk,Hv,dtype", MMA256_CASES)
+def test_mma_prefill_d256(cuda_device, B, T, Hk, Hv, dtype):
+    ins = gdn_inputs.make_inputs(B, T, Hk, Hv, 256, 256, dtype=dtype, seed=410 + T + Hv,
+                                 u_max=0.5, s0_std=0.1)
+    y, s = gpu_prefill(ins, 32, cuda_device)
+    yo, so = oracle_prefill(ins)
+    assert rel_err(y, yo) <= TOL[dtype], rel_err(y, yo)
+    assert rel_err(s, so) <= TOL[dtype], rel_err(s, so)
+
+
+@pytest.mark.parametrize("mode", ["null", "inplace"])
+def test_mma_prefill_d256_state_modes(cuda_device, mode):
+    ins = gdn_inputs.make_inputs(1, 70, 2, 2, 256, 256, dtype=torch.bfloat16, seed=415,
+                                 s0_std=0.1)
     y, s = gpu_prefill(ins, 64, cuda_device, state_mode=mode)
     yo, so = oracle_prefill(ins, zero_state=(mode == "null"))
     assert rel_err(y, yo) <= TOL[torch.bfloat16]

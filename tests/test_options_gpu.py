@@ -87,6 +87,16 @@ def test_prefill_options_head_size_64(cuda_device, options):
     assert rel_err(s, so) <= TOL[BF16], rel_err(s, so)
 
 
+@pytest.mark.parametrize("options", [TILED | LOGG | L2N])
+def test_prefill_options_head_size_256(cuda_device, options):
+    """The conventions on the head-size-256 warp-level tensor-core path."""
+    ins = gdn_inputs.make_inputs(1, 70, 2, 4, 256, 256, BF16, seed=530, u_max=0.5, s0_std=0.1)
+    ins = _unnormalised(ins)
+    y, s, yo, so = _run(ins, options, 32, cuda_device)
+    assert rel_err(y, yo) <= TOL[BF16], rel_err(y, yo)
+    assert rel_err(s, so) <= TOL[BF16], rel_err(s, so)
+
+
 def test_tiled_differs_from_grouped(cuda_device):
     """The option changes the result (the two maps pair different heads)."""
     ins = gdn_inputs.make_inputs(1, 40, 2, 4, 128, 128, BF16, seed=7, s0_std=0.1)
