@@ -11,8 +11,10 @@
 
 namespace gdn {
 
-// Head sizes: the tensor-core prefill is built for Dk = Dv = kHeadDim; the
-// decode, short-T and fp32 SIMT kernels take Dk and Dv from {64, 128, 256}.
+// Head sizes: the tcgen05 prefill and the tensor-core short-T kernel are built
+// for Dk = Dv = kHeadDim, the warp-level MMA prefills for 64/64 and 256/256;
+// the decode, sequential short-T and fp32 SIMT kernels take Dk and Dv from
+// {64, 128, 256}.
 constexpr int kHeadDim = 128;
 __host__ __device__ constexpr bool head_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
 
@@ -81,7 +83,8 @@ struct DecodeArgs {
   cudaStream_t stream;
 };
 
-// fp32 SIMT chunked path (any dtype and head size; the exact path for fp32 inputs).
+// fp32 SIMT chunked path (any dtype and head size; serves fp32 inputs and the
+// head pairs the tensor-core paths do not take).
 size_t prefill_simt_workspace_bytes(int B, int T, int Hv, int chunk, int Dk, int Dv);
 cudaError_t launch_prefill_simt(const PrefillArgs& a);
 

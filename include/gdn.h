@@ -113,21 +113,25 @@ GDN_API size_t gdn_prefill_workspace_bytes(int B, int T, int Hk, int Hv, int Dk,
  *   chunk      tokens per chunk: 16, 32 or 64.  Any T >= 1 is accepted; a
  *              last chunk shorter than `chunk` behaves as if padded with
  *              g = 1, beta = 0 tokens (metaltile-std kernel, chunk loop).
- *              Sequences of T <= 32 run the sequential rule instead (state on
- *              chip, fp32 arithmetic, no workspace; the short-T routing of
- *              the MLX PR "Pack gated_delta_seq", Performance).
+ *              Sequences of T <= 32 run a kernel of their own with the state
+ *              on chip and no workspace (the short-T routing of the MLX PR
+ *              "Pack gated_delta_seq", Performance): for bf16 / fp16 inputs
+ *              with Dk = Dv = 128 the sequence as one chunk on warp-level
+ *              tensor-core MMAs, otherwise the sequential rule in fp32.
  *   workspace  device scratch of at least gdn_prefill_workspace_bytes(...)
  *              bytes, 256-byte aligned, owned by the caller; its contents on
  *              entry do not matter and on return are unspecified.  It must
  *              not be used by anything else until the work on `stream` is done.
  *   stream     cudaStream_t, or NULL.
- * Dk and Dv are each 64, 128 or 256.  bf16 and fp16 inputs with Dk = Dv = 128
- * run on the tensor cores, whose operands (the inputs and the per-chunk
+ * Dk and Dv are each 64, 128 or 256.  bf16 and fp16 inputs with Dk = Dv = 128,
+ * 64 or 256 run on the tensor cores (tcgen05 at 128, warp-level MMAs in
+ * chunks of 32 at 64 and 256), whose operands (the inputs and the per-chunk
  * intermediates) are then rounded to the input type and whose products
- * accumulate in fp32; every other head size and dtype runs the fp32 chunked
- * path, which for Dk = Dv = 256 runs a chunk of 64 as two chunks of 32 (the
- * result differs only by rounding; gdn_prefill_workspace_bytes accounts for
- * it).  Returns GDN_OK or a GDN_ERR_* code.
+ * accumulate in fp32; every other head pair and fp32 inputs run the fp32
+ * chunked path, which for Dk = Dv = 256 runs a chunk of 64 as two chunks of
+ * 32.  The chunk size changes the result only by rounding, and
+ * gdn_prefill_workspace_bytes accounts for the one each path uses.  Returns
+ * GDN_OK or a GDN_ERR_* code.
  */
 GDN_API int gdn_prefill(const void *q, const void *k, const void *v, const void *g,
                 const void *beta, const float *state_in, float *state_out, void *y,
@@ -196,9 +200,9 @@ GDN_API int gdn_prefill_noalloc(const void *q, const void *k, const void *v, con
                                 int chunk, int dtype, void *stream);
 
 /*
- * Device-side health: every wait inside the tensor-core kernels (on an
- * mbarrier fed by TMA or by the tensor core, or on a tile flag that another
- * CTA raises) is bounded; a wait that gives up
+ * Device-side health: every wait inside the tensor-core and TMA-fed kernels
+ * (on an mbarrier fed by TMA or by the tensor core, or on a tile flag that
+ * another CTA raises) is bounded; a wait that gives up
  * sets a device error word and the kernel returns early, leaving its outputs
  * unspecified.  This call synchronises the device, reads that word and
  * returns GDN_OK, GDN_ERR_DEVICE_TIMEOUT, or GDN_ERR_CUDA if it cannot be

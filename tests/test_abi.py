@@ -58,9 +58,17 @@ def test_workspace_bytes(L):
     assert w(1, 4096, 16, 32, 128, 128, 48, 1) == 0      # bad chunk
     assert w(1, 4096, 16, 32, 96, 128, 64, 1) == 0       # unsupported head size
     assert w(1, 4096, 16, 32, 128, 512, 64, 1) == 0
-    # head sizes 64 and 256 run the fp32 SIMT chunked path (any dtype) ...
-    assert w(1, 4096, 16, 32, 64, 64, 64, 1) > 0
-    assert w(1, 4096, 16, 32, 256, 64, 64, 1) > w(1, 4096, 16, 32, 64, 64, 64, 1)
+    # 16-bit inputs at Dk = Dv = 64 or 256 run the warp-level MMA paths, always
+    # in chunks of 32: a block of 5 x 32 rows (-Pt, Qh, Ut, K, y_loc) per
+    # (head, chunk), plus G_C or a flag per chunk
+    nc = 4096 // 32
+    assert w(1, 4096, 16, 32, 64, 64, 64, 1) == w(1, 4096, 16, 32, 64, 64, 16, 2)
+    assert w(1, 4096, 16, 32, 64, 64, 64, 1) >= 32 * nc * 5 * 32 * 64 * 2
+    assert w(1, 4096, 16, 32, 256, 256, 64, 1) == w(1, 4096, 16, 32, 256, 256, 32, 2)
+    assert w(1, 4096, 16, 32, 256, 256, 64, 1) >= 32 * nc * 5 * 32 * 256 * 2
+    # every other head pair, and fp32, runs the SIMT chunked path ...
+    assert w(1, 4096, 16, 32, 64, 64, 64, 0) > 0
+    assert w(1, 4096, 16, 32, 256, 64, 64, 1) > w(1, 4096, 16, 32, 64, 128, 64, 1) > 0
     # ... where Dk = Dv = 256 with chunk 64 runs as chunks of 32 (shared memory)
     assert w(1, 4096, 16, 32, 256, 256, 64, 0) == w(1, 4096, 16, 32, 256, 256, 32, 0)
     assert w(1, 4096, 16, 32, 128, 128, 64, 0) != w(1, 4096, 16, 32, 128, 128, 32, 0)
