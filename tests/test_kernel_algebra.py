@@ -15,7 +15,12 @@ Each identity here is one the kernels rely on beyond the plain recurrence:
     both factors products of decays, and the clamp of log2 g that makes a
     vanishing gate underflow to exact forgetting;
   * the short-T kernel's scaled state, S = gam * St with renormalisation when
-    gam * g leaves [2^-24, 2^24], and its output identity y = g z + d (k . q).
+    gam * g leaves [2^-24, 2^24], and its output identity y = g z + d (k . q);
+  * the warp-level MMA kernels' blockwise inverse (8 x 8 diagonal blocks by
+    forward substitution, then T21 = -T22 (L21 T11) doubling the block size) and
+    their coefficient form: cP = -G_C diag(beta) T_L, cU = diag(Gam_end) T_A,
+    W_M = diag(G) M T_L, W_Y = (Gam . QK^T) T_A, with the innovation-form update
+    S <- G_C S + (Ut^T - Z) K.
 A ragged tail is padded with g = 1, beta = 0 and zero q, k, v, as the kernels do.
 """
 import numpy as np
@@ -212,3 +217,92 @@ def test_two_chunks_compose_into_one_affine_step():
         S = S @ (F1 @ F2) + (N1 @ F2 + N2)
     assert rel_err(np.vstack(ys), yo[0, :, 0]) < 1e-12
     assert rel_err(S, so[0, 0]) < 1e-12
+
+
+def blockwise_inverse(L):
+    """(I + L)^-1 for strictly lower-triangular L of size C (a multiple of 8)
+    the way the warp-MMA kernels form it: the 8 x 8 diagonal blocks by forward
+    substitution, then, doubling the block size B, every lower-left block of a
+    2B x 2B diagonal block from T21 = -T22 (L21 T11)."""
+    C = L.shape[0]
+    T = np.zeros((C, C))
+    for o in range(0, C, 8):
+        for c in range(8):
+            x = np.zeros(8)
+            for r in range(8):
+                x[r] = (1.0 if r == c else 0.0) - L[o + r, o:o + r] @ x[:r]
+            T[o:o + 8, o + c] = x
+    B = 8
+    while B < C:
+        for o in range(0, C, 2 * B):
+            L21 = L[o + B:o + 2 * B, o:o + B]
+            T11 = T[o:o + B, o:o + B]
+            T22 = T[o + B:o + 2 * B, o + B:o + 2 * B]
+            T[o + B:o + 2 * B, o:o + B] = -T22 @ (L21 @ T11)
+        B *= 2
+    return T
+
+
+@pytest.mark.parametrize("C", [16, 32, 64])
+def test_blockwise_inverse_equals_the_inverse(C):
+    rng = np.random.default_rng(40 + C)
+    K = rng.standard_normal((C, 24))
+    K /= np.linalg.norm(K, axis=1, keepdims=True)
+    bc = rng.uniform(0.0, 1.0, C)
+    L = np.tril((K @ K.T) * bc[None, :], -1)
+    ref = np.linalg.inv(np.eye(C) + L)
+    assert np.max(np.abs(blockwise_inverse(L) - ref)) < 1e-12 * max(1.0, np.max(np.abs(ref)))
+
+
+def coefficient_chunk_model(q, k, v, g, beta, s0, C):
+    """One head through the coefficient form of the warp-level MMA kernels
+    (short-T, head sizes 64 and 256): per chunk cP = -G_C diag(beta) T_L,
+    T_A = diag(beta)(Gam . T_L), cU = diag(Gam_end) T_A, W_M = diag(G) M T_L,
+    W_Y = (Gam . QK^T) T_A; -Pt = cP K, Qh = (G Q - W_M K) / sqrt(Dk),
+    Ut = cU V, y_loc = W_Y V / sqrt(Dk); then [-Z | Y] = S [-Pt; Qh]^T,
+    y = Y + y_loc and S <- G_C S + (Ut^T - Z) K."""
+    T, Dk = k.shape
+    Dv = v.shape[1]
+    n = -(-T // C)
+    pad = n * C - T
+    q = np.vstack([q, np.zeros((pad, Dk))])
+    k = np.vstack([k, np.zeros((pad, Dk))])
+    v = np.vstack([v, np.zeros((pad, Dv))])
+    g = np.concatenate([g, np.ones(pad)])
+    beta = np.concatenate([beta, np.zeros(pad)])
+    sc = 1.0 / np.sqrt(Dk)
+    S = s0.copy()
+    ys = []
+    for c in range(n):
+        sl = slice(c * C, (c + 1) * C)
+        Q, K, V, gc, bc = q[sl], k[sl], v[sl], g[sl], beta[sl]
+        _, G, gam = gate_tables(gc)
+        GC = G[-1]
+        KK, QK = K @ K.T, Q @ K.T
+        TL = blockwise_inverse(np.tril(KK * bc[None, :], -1))
+        TA = bc[:, None] * (gam * TL)
+        cP = -GC * bc[:, None] * TL
+        cU = gam[-1][:, None] * TA
+        WM = (G[:, None] * np.tril(QK * bc[None, :])) @ TL
+        WY = (gam * QK) @ TA
+        negPt = cP @ K
+        Qh = (G[:, None] * Q - WM @ K) * sc
+        Ut = cU @ V
+        y_loc = (WY @ V) * sc
+        negZ, Y = S @ negPt.T, S @ Qh.T
+        ys.append(Y.T + y_loc)
+        S = GC * S + (Ut.T + negZ) @ K
+    return np.vstack(ys)[:T], S
+
+
+@pytest.mark.parametrize("C,T", [(16, 16), (16, 9), (32, 32), (32, 70), (32, 257)])
+def test_warp_mma_coefficient_form_equals_the_rule(C, T):
+    rng = np.random.default_rng(2000 + C + T)
+    Hk, Hv, Dk, Dv = 1, 2, 16, 12
+    q, k, v, g, beta, s0 = rand_problem(rng, T, Hk, Hv, Dk, Dv)
+    yo, so = oracle.gdn_sequential(q, k, v, g, beta, s0)
+    for hv in range(Hv):
+        y, s = coefficient_chunk_model(q[0, :, 0], k[0, :, 0], v[0, :, hv], g[0, :, hv],
+                                       beta[0, :, hv], s0[0, hv], C)
+        assert rel_err(y, yo[0, :, hv]) < 1e-10
+        assert rel_err(s, so[0, hv]) < 1e-10
