@@ -55,6 +55,7 @@ template <typename E>
 struct ScanSmem {
   E stage[kStages][kBlkRows * kD];  // workspace blocks, 128-byte swizzled rows
   E ys[kC][kYS];                    // Y staging [t][v], each warp its 16 columns
+  float gcs[kStages];  // G_C of the chunk in each stage (set by the loader)
   alignas(8) uint64_t full[kStages];   // a block landed
   alignas(8) uint64_t empty[kStages];  // the four state warps are done with a stage
 };
@@ -289,6 +290,7 @@ mma_scan_kernel(const __grid_constant__ CUtensorMap tm_ws, const float* __restri
             !ptx::mbar_wait(s_u32(&sm.empty[st]), ((n / kStages) - 1) & 1))
           break;
         const uint32_t fb = s_u32(&sm.full[st]);
+        sm.gcs[st] = __ldg(wsgc + (size_t)bh * NC + n);  // released by the arrival below
         ptx::mbar_expect_tx(fb, kBlkBytes);
         ptx::tma_load_2d(s_u32(sm.stage[st]), &tm_ws, fb, 0, (bh * NC + n) * kBlkRows);
       }
@@ -315,14 +317,12 @@ mma_scan_kernel(const __grid_constant__ CUtensorMap tm_ws, const float* __restri
       s[j][3] = hi.y;
     }
   }
-  float gc_next = __ldg(wsgc + (size_t)bh * NC);
   for (int j = 0; j < NC; ++j) {
     const int st = j % kStages;
-    const float gcv = gc_next;
-    if (j + 1 < NC) gc_next = __ldg(wsgc + (size_t)bh * NC + j + 1);
     // A block that never lands (2 s) is recorded in the device error word and
     // the head is left unwritten.
     if (!__all_sync(0xffffffffu, ptx::mbar_wait(s_u32(&sm.full[st]), (j / kStages) & 1))) return;
+    const float gcv = sm.gcs[st];
     const uint32_t base = s_u32(sm.stage[st]);
     // [-Z | Y] = S [-Pt; Qh]^T: B from rows 0 .. 2C of the block.
     float zy[2 * NT8][4];

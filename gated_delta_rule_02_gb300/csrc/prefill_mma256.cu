@@ -66,6 +66,7 @@ struct ScanSmem {
   E stage_b[kStages][2 * kC * 64];  // [row][64] of Ut, y_loc (this quarter's columns)
   float xbuf[8][2][32][32];         // partial [-Z | Y] of each warp, by chunk parity
   E ys[kC][kYS];                    // Y staging [t][v] of the four writing warps
+  float gcs[kStages];  // G_C of the chunk in each stage (set by the loader)
   alignas(8) uint64_t full[kStages];
   alignas(8) uint64_t empty[kStages];
 };
@@ -335,6 +336,7 @@ mma256_scan_kernel(const __grid_constant__ CUtensorMap tm_wa,
         if (n >= kStages && !ptx::mbar_wait(s_u32(&sm.empty[st]), ((n / kStages) - 1) & 1))
           break;
         const uint32_t fb = s_u32(&sm.full[st]);
+        sm.gcs[st] = __ldg(wsgc + (size_t)bh * NC + n);  // released by the arrival below
         const int row = (bh * NC + n) * kBlkRows;
         ptx::mbar_expect_tx(fb, kBytesA + kBytesB);
         tma_load_3d(s_u32(sm.stage_a[st]), &tm_wa, fb, 0, row, 0);
@@ -363,14 +365,12 @@ mma256_scan_kernel(const __grid_constant__ CUtensorMap tm_wa,
       s[j][3] = hi.y;
     }
   }
-  float gc_next = __ldg(wsgc + (size_t)bh * NC);
   for (int j = 0; j < NC; ++j) {
     const int st = j % kStages, par = j & 1;
-    const float gcv = gc_next;
-    if (j + 1 < NC) gc_next = __ldg(wsgc + (size_t)bh * NC + j + 1);
     // A chunk that never lands (2 s) is recorded in the device error word and
     // the quarter is left unwritten.
     if (!__all_sync(0xffffffffu, ptx::mbar_wait(s_u32(&sm.full[st]), (j / kStages) & 1))) return;
+    const float gcv = sm.gcs[st];
     const uint32_t ba = s_u32(sm.stage_a[st]), bb8 = s_u32(sm.stage_b[st]);
     // This warp's key half of [-Z | Y] = S [-Pt; Qh]^T (B: rows 0 .. 2C of part A).
     float zy[2 * NT8][4];
