@@ -29,7 +29,7 @@ namespace {
 
 constexpr int kD = 256;           // head size (Dk = Dv)
 constexpr int kC = 32;            // chunk
-constexpr int kPT = 256;          // prep threads
+constexpr int kPT = 512;          // prep threads
 constexpr int kST = 288;          // scan threads: 8 state warps + a loader warp
 constexpr int kFS = kC + 1;       // fp32 row stride of the C x C arrays
 constexpr int kCS = kC + 8;       // 16-bit row stride of the C x C arrays (80 B)
