@@ -8,7 +8,7 @@
 // scan of a head runs on four CTAs of 64 value rows each (the rows of S evolve
 // independently given the chunk's coefficients), and inside a CTA the 256 keys
 // are split over warp pairs:
-//   prep, one CTA of eight warps per (head, chunk), all at once: L = KK^T
+//   prep, one CTA of sixteen warps per (head, chunk), all at once: L = KK^T
 //     diag(beta), QK^T, T_L blockwise, the coefficients, W_M and W_Y, then
 //     -Pt = cP K, Qh / sqrt(Dk), Ut = cU V and y_loc / sqrt(Dk) into a workspace
 //     block [-Pt; Qh; K; Ut; y_loc] (5C rows of 256) and G_C beside it;
